@@ -1,0 +1,405 @@
+"""Benchmark of the SSD prefill (and, on request, the multi-step decode).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mamba2_2p7b|long_16k|hybrid_llama3_8b|tiny_f32|multistep_k8]
+
+One step = one ssd_fwd call over the whole workload (all four kernels of the
+chunked algorithm) with inputs resident in HBM.  Default workload: one Mamba-2
+2.7B SSD layer (batch 8, T 2048, 80 heads, P 64, N 128, chunk 256, bf16 I/O,
+fp32 state), synthetic seeded inputs.  Metric: tokens x heads per second,
+reported in M tok*heads/s, plus the fraction of the layer's roofline.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer has no exchange between (batch, head) pairs); rank 0 prints one
+JSON line with the whole-job throughput over the max time across ranks.
+
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_model_09_b300 import synth  # noqa: E402
+
+METRIC = "SSD fwd Mtok·heads/s at Mamba-2 2.7B shape; % of roofline (TC or HBM)"
+UNIT = "Mtok·heads/s"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sus=m["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------- work model
+def fwd_work(s: synth.FwdShape):
+    """Algorithmic bytes / flops of the layer and of each stage (per call).
+
+    Layer (mandatory I/O): x, y, B, C (io dtype), dt (f32), h0 if given,
+    h_final (f32).  Flops count causal work only: P*Q(Q+1) (masked scores times
+    x), 2QNP (chunk state), 2QNP (output from the initial state) per
+    (b, chunk, head), plus N*Q(Q+1) per (b, chunk, distinct B/C group pair) for
+    C B^T.  Stage bytes count each stage's own inputs/outputs once."""
+    io = 2 if s.io == synth.BF16 else 4
+    b, T, H, P, N, Q = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.chunk
+    nc = math.ceil(T / Q)
+    x = b * T * H * P * io
+    Bb = b * T * s.ngroups_b * N * io
+    Cb = b * T * s.ngroups_c * N * io
+    dt = b * T * H * 4
+    st = b * H * N * P * 4
+    h0 = st if s.h0 != "zero" else 0
+    pairs = max(s.ngroups_b, s.ngroups_c)
+    flops = b * nc * H * (P * Q * (Q + 1) + 4 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)
+    layer_bytes = 2 * x + Bb + Cb + dt + h0 + st
+    cs = b * H * nc * Q * 4
+    S = b * nc * H * N * P * 4
+    hin = b * nc * H * N * P * (2 if s.io == synth.BF16 else 4)
+    stage_bytes = [dt + cs, x + Bb + cs + S, S + b * H * nc * 4 + h0 + hin + st,
+                   x + Bb + Cb + cs + hin + x]
+    stage_flops = [0, 2 * b * nc * H * Q * N * P,
+                   2 * b * nc * H * N * P,
+                   b * nc * H * (P * Q * (Q + 1) + 2 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)]
+    return dict(layer_bytes=layer_bytes, flops=flops, stage_bytes=stage_bytes,
+                stage_flops=stage_flops, tok_heads=b * T * H,
+                h2d=x + Bb + Cb + dt + h0 + 2 * H * 4, d2h=x + st)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "--id=" + gpu_id, "--query-gpu=" + self.FIELDS,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        with open(self.f.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(dev) -> str:
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        return str(dev)
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("SSD_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def time_oracle_fwd(shape, inp, pairs, threads=0):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.ssd_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
+                   pairs=pairs, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(shape, inp, budget_s=20.0):
+    """The oracle as it stands, on the host's cores, on a bounded sample of the
+    workload: as many (b, h) pairs (whole sequences) as fit ~budget_s."""
+    import oracle
+    H = shape.nheads
+    total = shape.batch * H
+    cores = oracle.default_threads()
+    probe = list(range(min(total, max(cores, 8))))
+    tp = time_oracle_fwd(shape, inp, probe)
+    per_pair = tp / len(probe)
+    n = int(min(total, max(len(probe), budget_s / max(per_pair, 1e-9))))
+    pairs = list(range(n))
+    t = time_oracle_fwd(shape, inp, pairs)
+    rate = n * shape.seqlen / t / 1e6
+    return {"value": round(rate, 4), "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
+            "sample": "%d of %d (batch, head) pairs, whole %d-token sequences (%.1f s, fp64)"
+                      % (n, total, shape.seqlen, t)}
+
+
+def run_reference(args, shape, work):
+    """--impl reference: the fp64 oracle on bounded samples of the workload."""
+    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload])
+    import oracle
+    cores = oracle.default_threads()
+    total = shape.batch * shape.nheads
+    probe = list(range(min(total, cores)))
+    per_pair = time_oracle_fwd(shape, inp, probe) / len(probe)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(total, budget / max(per_pair, 1e-9))))
+    pairs = list(range(n))
+    for _ in range(args.warmup):
+        time_oracle_fwd(shape, inp, pairs)
+    t = sum(time_oracle_fwd(shape, inp, pairs) for _ in range(args.steps))
+    ms = t / args.steps * 1e3
+    value = n * shape.seqlen / (t / args.steps) / 1e6
+    sample = "%d of %d (batch, head) pairs per step, whole sequences" % (n, total)
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": config_of(args, shape, "cpu"),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": min(cores, n),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line, ensure_ascii=False))
+
+
+def config_of(args, shape, where):
+    c = {"workload": args.workload, "batch": shape.batch, "seq_len": shape.seqlen,
+         "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+         "ngroups_b": shape.ngroups_b, "ngroups_c": shape.ngroups_c, "chunk": shape.chunk,
+         "io": "bf16" if shape.io == synth.BF16 else "f32", "state": "f32",
+         "h0": shape.h0, "parallelism": "replicas%d" % args.gpus}
+    if where == "gpu":
+        c["l2"] = "no flush; inputs+outputs %.0f MB > 126 MB L2" % (fwd_work(shape)["layer_bytes"] / 1e6)
+    return c
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, shape, work, world, rank, local):
+    import torch
+    from state_space_model_09_b300 import ssd as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload] + 17 * rank)
+    io_t = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
+    host = {}
+    for k, v in inp.items():
+        if v is None:
+            host[k] = None
+            continue
+        t = torch.from_numpy(v)
+        if k in ("x", "B", "C"):
+            t = t.to(io_t)
+        host[k] = t.pin_memory()
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    b, T, H, P = d["x"].shape
+    N = d["B"].shape[3]
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((b, H, N, P), dtype=torch.float32, device=dev)
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    ws = S.workspace_for(dims, shape.chunk, dev)
+    stream = torch.cuda.current_stream(dev)
+    names = [S.ssd_fwd_stage_name(dims, shape.chunk, i) for i in range(S.ssd_fwd_num_stages(dims, shape.chunk))]
+
+    def step():
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], shape.chunk, y, hf,
+                  ws, True, stream, dims)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    S.ssd_check_device_error(stream)
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    clocks = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    S.ssd_check_device_error(stream)
+    ms = max_over_ranks(ms, world, dev)
+
+    # ---- per-kernel durations (CUDA events on the launching stream)
+    nst = len(names)
+    ks = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(ks)]
+    for i in range(ks):
+        S.ssd_fwd_profiled(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], shape.chunk,
+                           y, hf, ws, evs[i], True, stream, dims)
+    torch.cuda.synchronize()
+    stage_ms = [statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(ks))
+                for k in range(nst)]
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    hh = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
+    ke = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k in ("x", "dt", "A", "B", "C", "D", "h0"):
+            if host[k] is not None:
+                d[k].copy_(host[k], non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+        hh.copy_(hf, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / ke, world, dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in host if host[k] is not None)
+    d2h = yh.numel() * yh.element_size() + hh.numel() * hh.element_size()
+
+    if rank != 0:
+        return
+    pk = peaks()
+    value = world * work["tok_heads"] / (ms * 1e-3) / 1e6
+    t_hbm = work["layer_bytes"] / (pk["hbm"] * 1e9)
+    t_tc = work["flops"] / (pk["bf16"] * 1e12)
+    dom = int(np.argmax(stage_ms))
+    dom_bytes = work["stage_bytes"][dom]
+    dom_flops = work["stage_flops"][dom]
+    dom_s = stage_ms[dom] * 1e-3
+    if dom_flops / (pk["bf16"] * 1e12) > dom_bytes / (pk["hbm"] * 1e9):
+        roof = {"bound": "tensor", "achieved": round(dom_flops / dom_s / 1e12, 2),
+                "peak": pk["bf16"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(dom_bytes / dom_s / 1e9, 1), "peak": pk["hbm"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = None
+    roof["kernel"] = names[dom]
+    roof["algorithmic_bytes"] = dom_bytes
+    roof["algorithmic_flops"] = dom_flops
+    roof["peak_source"] = pk["source"] + " (burst)"
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
+        "config": config_of(args, shape, "gpu"),
+        "roofline": roof,
+        "layer_roofline": {"bytes": work["layer_bytes"], "flops": work["flops"],
+                           "t_bound_us": round(max(t_hbm, t_tc) * 1e6, 2),
+                           "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                           "frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+                           "peaks": "%s HBM %.1f GB/s, bf16 %.1f TFLOP/s" % (pk["source"], pk["hbm"], pk["bf16"])},
+        "stages_ms": {n: round(t, 5) for n, t in zip(names, stage_ms)},
+        "gpu_launches": nst * args.steps,
+        "e2e": {"value": round(world * work["tok_heads"] / (e2e_ms * 1e-3) / 1e6, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, inp)
+    print(json.dumps(line, ensure_ascii=False))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mamba2_2p7b",
+                    choices=[k for k, v in synth.WORKLOADS.items() if isinstance(v, synth.FwdShape)])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = synth.WORKLOADS[args.workload]
+    work = fwd_work(shape)
+    if args.impl == "reference":
+        # the oracle is host code: rank 0 alone runs it, other ranks exit 0
+        if int(os.environ.get("RANK", "0")) == 0:
+            run_reference(args, shape, work)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, shape, work, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba-2 SSD (state-space duality) layer and
+ * the K-token multi-step verification decode, on one NVIDIA B300 (sm_103a).
+ *
+ * The operation.  For every batch row b and head h the layer carries a state
+ * h of shape N x P and runs the selective recurrence with a scalar decay per
+ * head (Mamba-2's SSD restriction of the SSM, cloud.tencent page "Mamba 2 ...
+ * SSD", sections "核心创新——SSD" and "SSD算法"):
+ *
+ *     dt_t = softplus(dt_raw_t)         (if dims.dt_softplus; else dt_raw_t)
+ *     h_t  = exp(dt_t * A_h) * h_{t-1} + B_t x_t^T
+ *     y_t  = C_t^T h_t + D_h * x_t
+ *
+ * ssd_fwd evaluates it with the chunked block decomposition of that page
+ * (section "SSD算法" and "深入解析分块与状态传递机制"): Q x Q diagonal blocks in
+ * quadratic, attention-like form; the final state of every chunk from a zero
+ * initial state; a short scan that passes states across chunks; then each
+ * chunk's output from its true initial state.  ssd_multistep is the
+ * MultiStep verification of speculative decoding ("Mamba in the Llama",
+ * csdn page, section "推测解码"): K draft tokens advanced from a cached state,
+ * returning the K outputs, the state at the last accepted position j and the
+ * state after all K.
+ *
+ * Conventions shared by every call.
+ *   - Pointers are DEVICE pointers unless stated otherwise; every tensor is
+ *     contiguous and row-major, 16-byte aligned (the kernels stage tiles with
+ *     the Tensor Memory Accelerator, which needs that alignment).
+ *   - x, y        [batch, T, H, P]   io dtype (float32 or bfloat16)
+ *     dt          [batch, T, H]      float32 (raw dt; see dt_softplus)
+ *     B           [batch, T, G_B, N] io dtype
+ *     C           [batch, T, G_C, N] io dtype
+ *     A, D        [H]                float32 (A_h < 0 decays; D may be NULL = 0)
+ *     states      [batch, H, N, P]   float32, P fastest
+ *     Head h reads group h / (H / G) of B and C.
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     never allocates, frees or synchronises; all work is enqueued on
+ *     `stream` (a cudaStream_t, NULL = legacy default stream).
+ *   - Inputs are read-only.  Outputs must not alias inputs or each other.
+ *   - Argument errors are detected on the host before anything is launched.
+ *   - Results: y is rounded to nearest even into the io dtype; states stay
+ *     float32.
+ */
+#ifndef LIBSSD_SSD_H
+#define LIBSSD_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_VERSION 10000 /* major * 10000 + minor * 100 + patch */
+
+typedef enum ssd_status {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, aliasing, short workspace */
+    SSD_ERR_UNSUPPORTED = 2, /* a shape or chunk outside the supported envelope */
+    SSD_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+    SSD_ERR_TIMEOUT = 4      /* a kernel's bounded wait ran out (see ssd_check_device_error) */
+} ssd_status;
+
+typedef enum ssd_dtype { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Problem description shared by ssd_fwd and ssd_multistep.
+ *   batch, seqlen (T; K for ssd_multistep), nheads (H), headdim (P),
+ *   dstate (N), ngroups_b (G_B), ngroups_c (G_C): sizes, all >= 1.
+ *   P and N: multiples of 16, at most 256.  H % G_B == 0, H % G_C == 0.
+ *   io_dtype: SSD_F32 or SSD_BF16 -- the dtype of x, B, C and y.
+ *   dt_softplus: 1 = apply softplus (z > 20 -> z) to dt; 0 = dt is used as given. */
+typedef struct ssd_dims {
+    int64_t batch;
+    int64_t seqlen;
+    int64_t nheads;
+    int64_t headdim;
+    int64_t dstate;
+    int64_t ngroups_b;
+    int64_t ngroups_c;
+    int32_t io_dtype;
+    int32_t dt_softplus;
+} ssd_dims;
+
+/* Bytes of device workspace ssd_fwd needs for these dims and chunk length
+ * (chunk in {64, 128, 256}).  Returns 0 for arguments ssd_fwd would reject.
+ * The workspace holds the in-chunk cumulative decays [b, H, nc, Q], the
+ * chunk-final states and the chunk initial states [b, nc, H, N, P]
+ * (nc = ceil(T / Q)). */
+size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk);
+
+/* Chunked SSD prefill (cloud.tencent Mamba-2 page, section "SSD算法").
+ *   h0:       initial state [b, H, N, P] or NULL (zero state).
+ *   chunk:    Q, the block size of the decomposition: 64, 128 or 256.  The
+ *             result does not depend on it beyond rounding; it sets the
+ *             schedule.  The last chunk may be short (any T >= 1).
+ *   y:        output [b, T, H, P], io dtype.
+ *   h_final:  output state after token T [b, H, N, P], or NULL.
+ *   workspace/workspace_bytes: device scratch of at least
+ *             ssd_fwd_workspace_size() bytes; contents need no initialisation
+ *             and are garbage afterwards.
+ * Returns SSD_OK once every kernel is enqueued on `stream`. */
+ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                   const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
+                   void *y, float *h_final, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Number of kernels ssd_fwd launches for these arguments (its stages), or 0
+ * for arguments it would reject. */
+int32_t ssd_fwd_num_stages(const ssd_dims *dims, int32_t chunk);
+
+/* Name of stage i of ssd_fwd for these arguments ("dt_cumsum",
+ * "chunk_state", "state_passing", "chunk_scan", ...), or NULL. */
+const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i);
+
+/* ssd_fwd, additionally recording events[i] (a cudaEvent_t, host array of
+ * ssd_fwd_num_stages() + 1 entries) on `stream` just before stage i and
+ * events[num_stages] after the last stage, so a caller can time each kernel
+ * on the stream it runs on.  Same arguments and results as ssd_fwd. */
+ssd_status ssd_fwd_profiled(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                            const void *B, const void *C, const float *D, const float *h0,
+                            int32_t chunk, void *y, float *h_final, void *workspace,
+                            size_t workspace_bytes, void *const *events, void *stream);
+
+/* K-token multi-step verification decode ("Mamba in the Llama", section
+ * "推测解码": MultiStep returns the K outputs, the state at the last verified
+ * position j and the state at K; FirstConflict then keeps h_j, which equals
+ * h_K when all K drafts are accepted).
+ *   dims.seqlen = K, 1 <= K <= 16.
+ *   x [b, K, H, P], dt [b, K, H], B [b, K, G_B, N], C [b, K, G_C, N].
+ *   h_cache:  cached state [b, H, N, P] (float32) to advance from.
+ *   j:        DEVICE int32 [b], accepted-token count per batch row, 0..K.
+ *             h_j is the state after the first j tokens of this call
+ *             (j = 0 gives h_cache back).  Values outside 0..K make the
+ *             kernel write h_j for no position; the host cannot check them.
+ *   y [b, K, H, P] (io dtype), h_j and h_K [b, H, N, P] (float32): outputs.
+ *   h_j and h_K may not alias h_cache or each other. */
+ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                         const void *B, const void *C, const float *D, const float *h_cache,
+                         const int32_t *j, void *y, float *h_j, float *h_K, void *stream);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word: SSD_OK, or SSD_ERR_TIMEOUT if a kernel gave up a bounded wait since
+ * the last check (its outputs are then invalid).  Diagnostic call; the only
+ * entry point that synchronises. */
+ssd_status ssd_check_device_error(void *stream);
+
+/* Static, never-NULL description of a status code. */
+const char *ssd_status_string(ssd_status status);
+
+/* SSD_VERSION of the built library. */
+int32_t ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSSD_SSD_H */

@@ -1,0 +1,468 @@
+// ssd_api.cu -- host side of libssd: argument validation, workspace layout,
+// TMA descriptor encoding and kernel launches behind the C ABI of ssd.h.
+//
+// ssd_fwd runs the four steps of the chunked SSD algorithm (Mamba-2 page,
+// section "SSD算法" and "深入解析分块与状态传递机制") as four kernels on the
+// caller's stream:
+//   0 dt_cumsum      softplus(dt) * A, in-chunk inclusive running sums
+//   1 chunk_state    chunk-final states from zero initial state (green)
+//   2 state_passing  scan of those states across chunks (yellow)
+//   3 chunk_scan     diagonal blocks (orange) + output from the true initial
+//                    state (blue) + D skip
+// With bf16 I/O and a shape inside the tensor-core envelope (N = 128;
+// Q in {128, 256}; P = 64, or P = 128 with Q = 128) steps 1 and 3 run on
+// tcgen05 tensor cores; otherwise (fp32 I/O, other shapes) they run as
+// float32 CUDA-core kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/ssd.h"
+#include "ssd_kernels.cuh"
+#include "ssd_tc.cuh"
+
+namespace {
+
+using ssd::kTcN;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+  int64_t b, T, H, P, N, GB, GC;
+  int Q, nc;
+  bool bf16, softplus, tc;
+  size_t cs_off, S_off, Hin_off, total;
+};
+
+bool valid_dim(int64_t v) { return v >= 1 && v <= (int64_t(1) << 31) - 1; }
+
+// Shared shape checks of both calls.  Returns SSD_OK or the error to report.
+ssd_status check_dims(const ssd_dims *d) {
+  if (!d) return SSD_ERR_INVALID_ARG;
+  if (!valid_dim(d->batch) || !valid_dim(d->seqlen) || !valid_dim(d->nheads) ||
+      !valid_dim(d->headdim) || !valid_dim(d->dstate) || !valid_dim(d->ngroups_b) ||
+      !valid_dim(d->ngroups_c))
+    return SSD_ERR_INVALID_ARG;
+  if (d->io_dtype != SSD_F32 && d->io_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+  if (d->dt_softplus != 0 && d->dt_softplus != 1) return SSD_ERR_INVALID_ARG;
+  if (d->nheads % d->ngroups_b || d->nheads % d->ngroups_c) return SSD_ERR_INVALID_ARG;
+  if (d->headdim % 16 || d->dstate % 16 || d->headdim > 256 || d->dstate > 256)
+    return SSD_ERR_UNSUPPORTED;
+  return SSD_OK;
+}
+
+ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
+  ssd_status st = check_dims(d);
+  if (st != SSD_OK) return st;
+  if (chunk != 64 && chunk != 128 && chunk != 256) return SSD_ERR_UNSUPPORTED;
+  pl->b = d->batch;
+  pl->T = d->seqlen;
+  pl->H = d->nheads;
+  pl->P = d->headdim;
+  pl->N = d->dstate;
+  pl->GB = d->ngroups_b;
+  pl->GC = d->ngroups_c;
+  pl->Q = chunk;
+  pl->nc = static_cast<int>((d->seqlen + chunk - 1) / chunk);
+  pl->bf16 = d->io_dtype == SSD_BF16;
+  pl->softplus = d->dt_softplus != 0;
+  pl->tc = pl->bf16 && pl->N == kTcN &&
+           ((pl->Q == 256 && pl->P == 64) || (pl->Q == 128 && (pl->P == 64 || pl->P == 128)));
+  // grid limits: gridDim.y / gridDim.z <= 65535
+  if (pl->nc * ((pl->Q + 31) / 32) > 65535 || pl->b > 65535 || pl->H > 65535)
+    return SSD_ERR_UNSUPPORTED;
+  if (pl->b * pl->nc * pl->H > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
+  const size_t states = static_cast<size_t>(pl->b) * pl->nc * pl->H * pl->N * pl->P;
+  pl->cs_off = 0;
+  pl->S_off = align_up(static_cast<size_t>(pl->b) * pl->H * pl->nc * pl->Q * sizeof(float));
+  pl->Hin_off = pl->S_off + align_up(states * sizeof(float));
+  pl->total = pl->Hin_off + align_up(states * (pl->tc ? 2 : 4));
+  return SSD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors (driver entry point fetched through the runtime; no libcuda
+// link needed).
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor of rank r (dims innermost first, strides in bytes of dims 1..r-1),
+// box `box`, 128-byte swizzle, zero fill outside the tensor.
+bool encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                 const cuuint64_t *strides, const cuuint32_t *box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [b, T, G, W] bf16 tensor, tiles of [Q rows][64] at (w0, g, t0, b).
+bool encode_btgw(CUtensorMap *m, const void *base, int64_t b, int64_t T, int64_t G, int64_t W,
+                 int Q) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(G),
+                              static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(b)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W * 2), static_cast<cuuint64_t>(G * W * 2),
+                                 static_cast<cuuint64_t>(T * G * W * 2)};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(Q), 1};
+  return encode_bf16(m, base, 4, dims, strides, box);
+}
+
+template <typename K>
+bool set_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+         cudaSuccess;
+}
+
+ssd_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+void record(void *const *events, int i, cudaStream_t s) {
+  if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+}
+
+// ---------------------------------------------------------------------------
+// Stage launchers
+// ---------------------------------------------------------------------------
+ssd_status launch_cumsum(const Plan &pl, const float *dt, const float *A, float *cs,
+                         cudaStream_t s) {
+  dim3 grid(pl.nc, static_cast<unsigned>(pl.b));
+  switch (pl.Q) {
+    case 64: ssd::dt_cumsum_kernel<64><<<grid, 256, 0, s>>>(dt, A, cs, pl.T, pl.H, pl.nc, pl.softplus); break;
+    case 128: ssd::dt_cumsum_kernel<128><<<grid, 256, 0, s>>>(dt, A, cs, pl.T, pl.H, pl.nc, pl.softplus); break;
+    default: ssd::dt_cumsum_kernel<256><<<grid, 256, 0, s>>>(dt, A, cs, pl.T, pl.H, pl.nc, pl.softplus); break;
+  }
+  return launch_status();
+}
+
+template <typename HT>
+ssd_status launch_passing(const Plan &pl, const float *S, const float *cs, const float *h0,
+                          HT *Hin, float *h_final, cudaStream_t s) {
+  const int NP = static_cast<int>(pl.N * pl.P);
+  dim3 grid((NP / 4 + 255) / 256, static_cast<unsigned>(pl.H), static_cast<unsigned>(pl.b));
+  ssd::state_passing_kernel<HT><<<grid, 256, 0, s>>>(S, cs, h0, Hin, h_final, static_cast<int>(pl.H),
+                                                     pl.nc, pl.Q, NP);
+  return launch_status();
+}
+
+template <typename IO>
+ssd_status launch_state_simt(const Plan &pl, const void *x, const void *B, const float *cs,
+                             float *S, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
+  ssd::chunk_state_simt<IO><<<grid, 256, pl.Q * sizeof(float), s>>>(
+      static_cast<const IO *>(x), static_cast<const IO *>(B), cs, S, pl.T, static_cast<int>(pl.H),
+      static_cast<int>(pl.GB), static_cast<int>(pl.N), static_cast<int>(pl.P), pl.Q, pl.nc);
+  return launch_status();
+}
+
+template <typename IO, typename HT>
+ssd_status launch_scan_simt(const Plan &pl, const void *x, const void *B, const void *C,
+                            const float *cs, const HT *Hin, const float *D, void *y,
+                            cudaStream_t s) {
+  const int smem = static_cast<int>((pl.Q + 32 * pl.N + 32 * pl.Q) * sizeof(float));
+  auto k = ssd::chunk_scan_simt<IO, HT>;
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [&] { ok = set_smem(k, 32 * (256 + 256) * 4 + 256 * 4); });
+  if (!ok) return SSD_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(pl.H), pl.nc * ((pl.Q + 31) / 32), static_cast<unsigned>(pl.b));
+  k<<<grid, 256, smem, s>>>(static_cast<const IO *>(x), static_cast<const IO *>(B),
+                            static_cast<const IO *>(C), cs, Hin, D, static_cast<IO *>(y), pl.T,
+                            static_cast<int>(pl.H), static_cast<int>(pl.GB),
+                            static_cast<int>(pl.GC), static_cast<int>(pl.N),
+                            static_cast<int>(pl.P), pl.Q, pl.nc);
+  return launch_status();
+}
+
+template <int Q, int P>
+ssd_status launch_state_tc(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
+                           const float *cs, float *S, cudaStream_t s) {
+  using L = ssd::ChunkStateSmem<Q, P>;
+  auto k = ssd::chunk_state_tc<Q, P>;
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+  if (!ok) return SSD_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
+  k<<<grid, 128, L::kBytes, s>>>(mB, mX, cs, S, static_cast<int>(pl.H), static_cast<int>(pl.GB),
+                                 pl.nc);
+  return launch_status();
+}
+
+template <int Q, int P>
+ssd_status launch_scan_tc(const Plan &pl, const CUtensorMap &mC, const CUtensorMap &mB,
+                          const CUtensorMap &mX, const CUtensorMap &mH, const float *cs,
+                          const float *D, void *y, cudaStream_t s) {
+  using L = ssd::ChunkScanSmem<Q, P>;
+  auto k = ssd::chunk_scan_tc<Q, P>;
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+  if (!ok) return SSD_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
+  k<<<grid, 256, L::kBytes, s>>>(mC, mB, mX, mH, cs, D, static_cast<__nv_bfloat16 *>(y), pl.T,
+                                 static_cast<int>(pl.H), static_cast<int>(pl.GB),
+                                 static_cast<int>(pl.GC), pl.nc);
+  return launch_status();
+}
+
+constexpr int64_t kMultistepSmemMax = 200 * 1024;
+
+template <typename IO, int RPT>
+ssd_status launch_multistep(dim3 grid, int threads, int64_t smem, const ssd_dims *d,
+                            const void *x, const float *dt, const float *A, const void *B,
+                            const void *C, const float *D, const float *h_cache,
+                            const int32_t *j, void *y, float *h_j, float *h_K, int PS,
+                            cudaStream_t s) {
+  auto k = ssd::multistep_kernel<IO, RPT>;
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [&] { ok = set_smem(k, static_cast<int>(kMultistepSmemMax)); });
+  if (!ok) return SSD_ERR_CUDA;
+  k<<<grid, threads, static_cast<size_t>(smem), s>>>(
+      static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
+      D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
+      static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
+      static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus);
+  return launch_status();
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                    const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
+                    void *y, float *h_final, void *workspace, size_t ws_bytes, void *const *events,
+                    void *stream) {
+  Plan pl;
+  ssd_status st = make_plan(dims, chunk, &pl);
+  if (st != SSD_OK) return st;
+  if (!x || !dt || !A || !B || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, dt, A, B, C, D, h0, y, h_final, workspace};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if (ws_bytes < pl.total) return SSD_ERR_INVALID_ARG;
+  const size_t io = pl.bf16 ? 2 : 4;
+  const size_t nx = static_cast<size_t>(pl.b * pl.T * pl.H * pl.P) * io;
+  const size_t nB = static_cast<size_t>(pl.b * pl.T * pl.GB * pl.N) * io;
+  const size_t nC = static_cast<size_t>(pl.b * pl.T * pl.GC * pl.N) * io;
+  const size_t ndt = static_cast<size_t>(pl.b * pl.T * pl.H) * 4;
+  const size_t nst = static_cast<size_t>(pl.b * pl.H * pl.N * pl.P) * 4;
+  const size_t nh = static_cast<size_t>(pl.H) * 4;
+  struct Buf { const void *p; size_t n; };
+  const Buf ins[] = {{x, nx}, {dt, ndt}, {A, nh}, {B, nB}, {C, nC}, {D, nh}, {h0, nst}};
+  const Buf outs[] = {{y, nx}, {h_final, nst}, {workspace, pl.total}};
+  for (const Buf &o : outs) {
+    for (const Buf &i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return SSD_ERR_INVALID_ARG;
+  }
+  if (overlaps(y, nx, h_final, nst) || overlaps(y, nx, workspace, pl.total) ||
+      overlaps(h_final, nst, workspace, pl.total))
+    return SSD_ERR_INVALID_ARG;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *cs = reinterpret_cast<float *>(ws + pl.cs_off);
+  float *S = reinterpret_cast<float *>(ws + pl.S_off);
+  void *Hin = ws + pl.Hin_off;
+
+  if (pl.tc) {
+    CUtensorMap mX, mB, mC, mH;
+    const cuuint64_t hdims[3] = {static_cast<cuuint64_t>(pl.P), static_cast<cuuint64_t>(pl.N),
+                                 static_cast<cuuint64_t>(pl.b * pl.nc * pl.H)};
+    const cuuint64_t hstr[2] = {static_cast<cuuint64_t>(pl.P * 2),
+                                static_cast<cuuint64_t>(pl.N * pl.P * 2)};
+    const cuuint32_t hbox[3] = {64, static_cast<cuuint32_t>(pl.N), 1};
+    if (!encode_btgw(&mX, x, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
+        !encode_btgw(&mB, B, pl.b, pl.T, pl.GB, pl.N, pl.Q) ||
+        !encode_btgw(&mC, C, pl.b, pl.T, pl.GC, pl.N, pl.Q) ||
+        !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
+      return SSD_ERR_CUDA;
+    record(events, 0, s);
+    if ((st = launch_cumsum(pl, dt, A, cs, s)) != SSD_OK) return st;
+    record(events, 1, s);
+    if (pl.Q == 256) st = launch_state_tc<256, 64>(pl, mB, mX, cs, S, s);
+    else if (pl.P == 64) st = launch_state_tc<128, 64>(pl, mB, mX, cs, S, s);
+    else st = launch_state_tc<128, 128>(pl, mB, mX, cs, S, s);
+    if (st != SSD_OK) return st;
+    record(events, 2, s);
+    if ((st = launch_passing(pl, S, cs, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s)) != SSD_OK)
+      return st;
+    record(events, 3, s);
+    if (pl.Q == 256) st = launch_scan_tc<256, 64>(pl, mC, mB, mX, mH, cs, D, y, s);
+    else if (pl.P == 64) st = launch_scan_tc<128, 64>(pl, mC, mB, mX, mH, cs, D, y, s);
+    else st = launch_scan_tc<128, 128>(pl, mC, mB, mX, mH, cs, D, y, s);
+    if (st != SSD_OK) return st;
+    record(events, 4, s);
+    return SSD_OK;
+  }
+
+  float *Hf = static_cast<float *>(Hin);
+  record(events, 0, s);
+  if ((st = launch_cumsum(pl, dt, A, cs, s)) != SSD_OK) return st;
+  record(events, 1, s);
+  st = pl.bf16 ? launch_state_simt<__nv_bfloat16>(pl, x, B, cs, S, s)
+               : launch_state_simt<float>(pl, x, B, cs, S, s);
+  if (st != SSD_OK) return st;
+  record(events, 2, s);
+  if ((st = launch_passing(pl, S, cs, h0, Hf, h_final, s)) != SSD_OK) return st;
+  record(events, 3, s);
+  st = pl.bf16 ? launch_scan_simt<__nv_bfloat16, float>(pl, x, B, C, cs, Hf, D, y, s)
+               : launch_scan_simt<float, float>(pl, x, B, C, cs, Hf, D, y, s);
+  if (st != SSD_OK) return st;
+  record(events, 4, s);
+  return SSD_OK;
+}
+
+const char *const kStageNamesTc[] = {"dt_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"};
+const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
+                                       "chunk_scan_simt"};
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk) {
+  Plan pl;
+  return make_plan(dims, chunk, &pl) == SSD_OK ? pl.total : 0;
+}
+
+int32_t ssd_fwd_num_stages(const ssd_dims *dims, int32_t chunk) {
+  Plan pl;
+  return make_plan(dims, chunk, &pl) == SSD_OK ? 4 : 0;
+}
+
+const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
+  Plan pl;
+  if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= 4) return nullptr;
+  return pl.tc ? kStageNamesTc[i] : kStageNamesSimt[i];
+}
+
+ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                   const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
+                   void *y, float *h_final, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+  return fwd_impl(dims, x, dt, A, B, C, D, h0, chunk, y, h_final, workspace, workspace_bytes,
+                  nullptr, stream);
+}
+
+ssd_status ssd_fwd_profiled(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                            const void *B, const void *C, const float *D, const float *h0,
+                            int32_t chunk, void *y, float *h_final, void *workspace,
+                            size_t workspace_bytes, void *const *events, void *stream) {
+  if (!events) return SSD_ERR_INVALID_ARG;
+  return fwd_impl(dims, x, dt, A, B, C, D, h0, chunk, y, h_final, workspace, workspace_bytes,
+                  events, stream);
+}
+
+ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                         const void *B, const void *C, const float *D, const float *h_cache,
+                         const int32_t *j, void *y, float *h_j, float *h_K, void *stream) {
+  ssd_status st = check_dims(dims);
+  if (st != SSD_OK) return st;
+  const int64_t b = dims->batch, K = dims->seqlen, H = dims->nheads, P = dims->headdim,
+                N = dims->dstate, GB = dims->ngroups_b, GC = dims->ngroups_c;
+  if (K > 16) return SSD_ERR_UNSUPPORTED;
+  if (b > 65535 || H > 65535) return SSD_ERR_UNSUPPORTED;
+  if (!x || !dt || !A || !B || !C || !h_cache || !j || !y || !h_j || !h_K)
+    return SSD_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, dt, A, B, C, D, h_cache, j, y, h_j, h_K};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  const bool bf16 = dims->io_dtype == SSD_BF16;
+  const size_t io = bf16 ? 2 : 4;
+  const size_t nx = static_cast<size_t>(b * K * H * P) * io;
+  const size_t nst = static_cast<size_t>(b * H * N * P) * 4;
+  struct Buf { const void *p; size_t n; };
+  const Buf ins[] = {{x, nx},
+                     {dt, static_cast<size_t>(b * K * H) * 4},
+                     {A, static_cast<size_t>(H) * 4},
+                     {B, static_cast<size_t>(b * K * GB * N) * io},
+                     {C, static_cast<size_t>(b * K * GC * N) * io},
+                     {D, static_cast<size_t>(H) * 4},
+                     {h_cache, nst},
+                     {j, static_cast<size_t>(b) * 4}};
+  const Buf outs[] = {{y, nx}, {h_j, nst}, {h_K, nst}};
+  for (const Buf &o : outs)
+    for (const Buf &i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return SSD_ERR_INVALID_ARG;
+  if (overlaps(y, nx, h_j, nst) || overlaps(y, nx, h_K, nst) || overlaps(h_j, nst, h_K, nst))
+    return SSD_ERR_INVALID_ARG;
+
+  // column slice per block: the largest of 128, 64, 32, 16 that divides P
+  const int PS = P % 128 == 0 ? 128 : P % 64 == 0 ? 64 : P % 32 == 0 ? 32 : 16;
+  const int TP = PS / 4;
+  auto smem_for = [&](int rpt, int *threads_out) {
+    int threads = TP * (static_cast<int>(N) / rpt);
+    threads = threads < 32 ? 32 : (threads + 31) / 32 * 32;
+    *threads_out = threads;
+    return (2 * K * N + K * PS + 16 + K * static_cast<int64_t>(threads / 32) * PS) * 4;
+  };
+  int threads = 0;
+  int rpt = 8;
+  int64_t smem = smem_for(8, &threads);
+  if (smem > kMultistepSmemMax || threads > 512) {
+    rpt = 16;
+    smem = smem_for(16, &threads);
+  }
+  if (smem > kMultistepSmemMax || threads > 512) return SSD_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
+  if (bf16) {
+    st = rpt == 8 ? launch_multistep<__nv_bfloat16, 8>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
+                  : launch_multistep<__nv_bfloat16, 16>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
+  } else {
+    st = rpt == 8 ? launch_multistep<float, 8>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
+                  : launch_multistep<float, 16>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
+  }
+  return st;
+}
+
+ssd_status ssd_check_device_error(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
+  int code = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&code, ssd::g_device_error, sizeof(int)) != cudaSuccess ||
+      cudaMemcpyToSymbol(ssd::g_device_error, &zero, sizeof(int)) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  if (code == ssd::kDevTimeout) return SSD_ERR_TIMEOUT;
+  if (code == ssd::kDevBadJ) return SSD_ERR_INVALID_ARG;
+  return SSD_OK;
+}
+
+const char *ssd_status_string(ssd_status status) {
+  switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported shape or chunk length";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t ssd_version(void) { return SSD_VERSION; }
+
+}  // extern "C"

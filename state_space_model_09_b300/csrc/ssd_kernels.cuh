@@ -1,0 +1,313 @@
+// ssd_kernels.cuh -- CUDA-core kernels of libssd:
+//   dt_cumsum_kernel      softplus(dt) * A and its in-chunk inclusive running sum
+//   state_passing_kernel  the scan of chunk-final states across chunks
+//   chunk_state_simt / chunk_scan_simt
+//                         float32-accurate chunk kernels (the fp32 I/O path and
+//                         shapes outside the tensor-core kernels' envelope)
+//   multistep_kernel      K-token verification decode from a cached state
+#pragma once
+
+#include "ssd_device.cuh"
+
+namespace ssd {
+
+// ----------------------------------------------------------------------------
+// dt -> cs.  cs[b,h,c,i] = sum_{k<=i} softplus(dt[b, cQ+k, h]) * A_h, inclusive,
+// within chunk c (the in-chunk "segment sums" whose differences give the decay
+// mask L and whose last entry gives the chunk decay; Mamba-2 page, section
+// "SSD算法", the modified A factors of the state-passing step).  Positions past
+// T contribute 0, so a short last chunk keeps its last valid value.
+// grid (nc, batch), 256 threads; warp w handles heads w, w+8, ...
+// ----------------------------------------------------------------------------
+template <int Q>
+__global__ void __launch_bounds__(256) dt_cumsum_kernel(const float *__restrict__ dt,
+                                                         const float *__restrict__ A,
+                                                         float *__restrict__ cs, int64_t T, int H,
+                                                         int nc, int softplus) {
+  constexpr int PER = Q / 32;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
+  for (int h = warp; h < H; h += 8) {
+    const float Ah = A[h];
+    float v[PER];
+    float run = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int64_t t = t0 + k;
+      float d = 0.f;
+      if (t < T) {
+        const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
+        d = (softplus ? softplus_f32(z) : z) * Ah;
+      }
+      run += d;
+      v[k] = run;
+    }
+    float incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const float excl = incl - run;
+    float *out = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q + lane * PER;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) out[k] = v[k] + excl;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// State passing across chunks (Mamba-2 page, "SSD算法", the 1-semiseparable
+// scan): Hin[0] = h0 (or 0), Hin[c+1] = exp(cs_last(c)) * Hin[c] + S[c],
+// h_final = Hin[nc].  Every (b, h, n, p) element is an independent scan over
+// the nc chunks; each thread carries 4 consecutive elements.
+// S, Hin: [b, nc, H, N*P]; grid (ceil(NP/1024), H, batch), 256 threads.
+// ----------------------------------------------------------------------------
+template <typename HT>
+__device__ __forceinline__ void store4(HT *dst, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float *dst, float4 v) {
+  *reinterpret_cast<float4 *>(dst) = v;
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float4 v) {
+  uint2 u;
+  u.x = pack_bf16x2(v.x, v.y);
+  u.y = pack_bf16x2(v.z, v.w);
+  *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+template <typename HT>
+__global__ void __launch_bounds__(256) state_passing_kernel(
+    const float *__restrict__ S, const float *__restrict__ cs, const float *__restrict__ h0,
+    HT *__restrict__ Hin, float *__restrict__ h_final, int H, int nc, int Q, int NP) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (e >= NP) return;
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
+  float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (h0) st = *reinterpret_cast<const float4 *>(h0 + bh * NP + e);
+  const float *csl = cs + bh * nc * Q + (Q - 1);
+#pragma unroll 4
+  for (int c = 0; c < nc; ++c) {
+    const int64_t off = ((static_cast<int64_t>(b) * nc + c) * H + h) * NP + e;
+    const float4 s = __ldcs(reinterpret_cast<const float4 *>(S + off));
+    const float decay = expf(csl[static_cast<int64_t>(c) * Q]);
+    store4<HT>(Hin + off, st);
+    st.x = fmaf(decay, st.x, s.x);
+    st.y = fmaf(decay, st.y, s.y);
+    st.z = fmaf(decay, st.z, s.z);
+    st.w = fmaf(decay, st.w, s.w);
+  }
+  if (h_final) *reinterpret_cast<float4 *>(h_final + bh * NP + e) = st;
+}
+
+// ----------------------------------------------------------------------------
+// Chunk-final states from a zero initial state, on CUDA cores in float32
+// (Mamba-2 page, "SSD算法", the green step):
+//   S[b,c,h][n][p] = sum_j exp(cs_last - cs_j) B[cQ+j, n] x[cQ+j, p].
+// grid (H, nc, batch), 256 threads; dynamic smem: Q floats.
+// ----------------------------------------------------------------------------
+template <typename IO>
+__global__ void __launch_bounds__(256) chunk_state_simt(
+    const IO *__restrict__ x, const IO *__restrict__ Bm, const float *__restrict__ cs,
+    float *__restrict__ S, int64_t T, int H, int GB, int N, int P, int Q, int nc) {
+  extern __shared__ float w_s[];
+  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+  const int gb = h / (H / GB);
+  const int64_t t0 = static_cast<int64_t>(c) * Q;
+  const int L = static_cast<int>(T - t0 < Q ? T - t0 : static_cast<int64_t>(Q));
+  const float *csc = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q;
+  const float cl = csc[Q - 1];
+  for (int j = threadIdx.x; j < Q; j += blockDim.x) w_s[j] = j < L ? expf(cl - csc[j]) : 0.f;
+  __syncthreads();
+  float *Sc = S + ((static_cast<int64_t>(b) * nc + c) * H + h) * N * P;
+  for (int idx = threadIdx.x; idx < N * P; idx += blockDim.x) {
+    const int n = idx / P, p = idx % P;
+    float acc = 0.f;
+    for (int j = 0; j < L; ++j) {
+      const int64_t t = t0 + j;
+      acc = fmaf(w_s[j] * to_f32(Bm[((static_cast<int64_t>(b) * T + t) * GB + gb) * N + n]),
+                 to_f32(x[((static_cast<int64_t>(b) * T + t) * H + h) * P + p]), acc);
+    }
+    Sc[idx] = acc;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Chunk outputs on CUDA cores in float32 (Mamba-2 page, "SSD算法": the orange
+// diagonal block in quadratic form plus the blue term from the chunk's true
+// initial state, and the D skip):
+//   y_i = sum_{j<=i} exp(cs_i - cs_j) (C_i . B_j) x_j + exp(cs_i) C_i^T Hin + D x_i
+// grid (H, nc * ceil(Q/32), batch): 32 rows of one chunk per block, 256 threads.
+// dynamic smem: cs[Q] + C rows [32][N] + masked scores [32][Q] (floats).
+// ----------------------------------------------------------------------------
+template <typename IO, typename HT>
+__global__ void __launch_bounds__(256) chunk_scan_simt(
+    const IO *__restrict__ x, const IO *__restrict__ Bm, const IO *__restrict__ Cm,
+    const float *__restrict__ cs, const HT *__restrict__ Hin, const float *__restrict__ D,
+    IO *__restrict__ y, int64_t T, int H, int GB, int GC, int N, int P, int Q, int nc) {
+  extern __shared__ float sm_f[];
+  float *csq = sm_f;
+  float *Ct = csq + Q;
+  float *G = Ct + 32 * N;
+  const int h = blockIdx.x, b = blockIdx.z;
+  const int tiles = (Q + 31) / 32;
+  const int c = blockIdx.y / tiles, i0 = (blockIdx.y % tiles) * 32;
+  const int gb = h / (H / GB), gc = h / (H / GC);
+  const int64_t t0 = static_cast<int64_t>(c) * Q;
+  const int L = static_cast<int>(T - t0 < Q ? T - t0 : static_cast<int64_t>(Q));
+  const float *csc = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q;
+  for (int j = threadIdx.x; j < Q; j += blockDim.x) csq[j] = csc[j];
+  for (int idx = threadIdx.x; idx < 32 * N; idx += blockDim.x) {
+    const int ii = idx / N, n = idx % N, i = i0 + ii;
+    Ct[idx] = i < L ? to_f32(Cm[((static_cast<int64_t>(b) * T + t0 + i) * GC + gc) * N + n]) : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 32 * Q; idx += blockDim.x) {
+    const int ii = idx / Q, j = idx % Q, i = i0 + ii;
+    float g = 0.f;
+    if (j <= i && i < L) {
+      const IO *Bj = Bm + ((static_cast<int64_t>(b) * T + t0 + j) * GB + gb) * N;
+      float dot = 0.f;
+      for (int n = 0; n < N; ++n) dot = fmaf(Ct[ii * N + n], to_f32(Bj[n]), dot);
+      g = dot * expf(csq[i] - csq[j]);
+    }
+    G[idx] = g;
+  }
+  __syncthreads();
+  const float Dh = D ? D[h] : 0.f;
+  const HT *Hc = Hin + ((static_cast<int64_t>(b) * nc + c) * H + h) * N * P;
+  for (int idx = threadIdx.x; idx < 32 * P; idx += blockDim.x) {
+    const int ii = idx / P, p = idx % P, i = i0 + ii;
+    if (i >= L) continue;
+    float acc = 0.f;
+    for (int j = 0; j <= i; ++j)
+      acc = fmaf(G[ii * Q + j], to_f32(x[((static_cast<int64_t>(b) * T + t0 + j) * H + h) * P + p]),
+                 acc);
+    float off = 0.f;
+    for (int n = 0; n < N; ++n) off = fmaf(Ct[ii * N + n], to_f32(Hc[n * P + p]), off);
+    const int64_t xo = ((static_cast<int64_t>(b) * T + t0 + i) * H + h) * P + p;
+    y[xo] = from_f32<IO>(acc + expf(csq[i]) * off + Dh * to_f32(x[xo]));
+  }
+}
+
+// ----------------------------------------------------------------------------
+// K-token multi-step decode ("Mamba in the Llama", 推测解码, MultiStep).
+// One block per (h, b, p-slice of PS columns).  The block's slice of the state
+// (N x PS floats) lives in registers: thread (r, q) holds rows r, r+R, ...
+// (RPT of them) of the 4 columns 4q..4q+3, R = N / RPT row groups.
+// Per token: h = a h + B x^T, then y = C^T h + D x reduced over rows by warp
+// shuffles and shared memory.  h_j is stored when the step count reaches j.
+// dynamic smem: B[K][N], C[K][N], x[K][PS], a[16], partial y [K][warps][PS].
+// ----------------------------------------------------------------------------
+template <typename IO>
+__device__ __forceinline__ float4 load_io4(const IO *p);
+template <> __device__ __forceinline__ float4 load_io4<float>(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+template <> __device__ __forceinline__ float4 load_io4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  const float2 a = unpack_bf16x2(u.x), c = unpack_bf16x2(u.y);
+  return make_float4(a.x, a.y, c.x, c.y);
+}
+
+template <typename IO, int RPT>
+__global__ void __launch_bounds__(512) multistep_kernel(
+    const IO *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
+    const IO *__restrict__ Bm, const IO *__restrict__ Cm, const float *__restrict__ D,
+    const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
+    float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N, int P,
+    int PS, int softplus) {
+  extern __shared__ float sm_ms[];
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  float *sB = sm_ms;
+  float *sC = sB + K * N;
+  float *sx = sC + K * N;
+  float *sa = sx + K * PS;
+  float *red = sa + 16;
+  const int h = blockIdx.x, b = blockIdx.y, p0 = blockIdx.z * PS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gb = h / (H / GB), gc = h / (H / GC);
+  const int TP = PS / 4, R = N / RPT;
+  const int q = tid % TP, r = tid / TP;
+  const bool active = r < R;
+
+  for (int i = tid; i < K * N; i += nthreads) {
+    const int k = i / N, n = i % N;
+    sB[i] = to_f32(Bm[((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n]);
+    sC[i] = to_f32(Cm[((static_cast<int64_t>(b) * K + k) * GC + gc) * N + n]);
+  }
+  for (int i = tid; i < K * PS; i += nthreads) {
+    const int k = i / PS, p = i % PS;
+    sx[i] = to_f32(x[((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p]);
+  }
+  if (tid < K) {
+    const float z = dt[(static_cast<int64_t>(b) * K + tid) * H + h];
+    sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[h]);
+  }
+  int jb = jacc[b];
+  if (jb < 0 || jb > K) {
+    if (tid == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
+    jb = -1;
+  }
+
+  const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
+  float4 st[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    st[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) st[i] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + (r + R * i) * P));
+  }
+  if (jb == 0 && active) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4 *>(h_j + base + (r + R * i) * P) = st[i];
+  }
+  __syncthreads();
+
+  for (int k = 0; k < K; ++k) {
+    const float a = sa[k];
+    float4 yp = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
+      const float4 xv = *reinterpret_cast<const float4 *>(sx + k * PS + 4 * q);
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int n = r + R * i;
+        const float bn = sB[k * N + n], cn = sC[k * N + n];
+        st[i].x = fmaf(a, st[i].x, bn * xv.x);
+        st[i].y = fmaf(a, st[i].y, bn * xv.y);
+        st[i].z = fmaf(a, st[i].z, bn * xv.z);
+        st[i].w = fmaf(a, st[i].w, bn * xv.w);
+        yp.x = fmaf(cn, st[i].x, yp.x);
+        yp.y = fmaf(cn, st[i].y, yp.y);
+        yp.z = fmaf(cn, st[i].z, yp.z);
+        yp.w = fmaf(cn, st[i].w, yp.w);
+      }
+    }
+    // lanes q, q + TP, q + 2TP, ... of a warp hold the same 4 columns
+    for (int off = TP; off < 32; off <<= 1) {
+      yp.x += __shfl_xor_sync(0xffffffffu, yp.x, off);
+      yp.y += __shfl_xor_sync(0xffffffffu, yp.y, off);
+      yp.z += __shfl_xor_sync(0xffffffffu, yp.z, off);
+      yp.w += __shfl_xor_sync(0xffffffffu, yp.w, off);
+    }
+    if (lane < TP) *reinterpret_cast<float4 *>(red + (k * nwarps + warp) * PS + 4 * lane) = yp;
+    if (k + 1 == jb && active) {
+#pragma unroll
+      for (int i = 0; i < RPT; ++i)
+        *reinterpret_cast<float4 *>(h_j + base + (r + R * i) * P) = st[i];
+    }
+  }
+  __syncthreads();
+  const float Dh = D ? D[h] : 0.f;
+  for (int i = tid; i < K * PS; i += nthreads) {
+    const int k = i / PS, p = i % PS;
+    float acc = 0.f;
+    for (int w = 0; w < nwarps; ++w) acc += red[(k * nwarps + w) * PS + p];
+    y[((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p] = from_f32<IO>(acc + Dh * sx[i]);
+  }
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4 *>(h_K + base + (r + R * i) * P) = st[i];
+  }
+}
+
+}  // namespace ssd

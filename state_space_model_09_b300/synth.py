@@ -31,14 +31,20 @@ BF16 = 1
 
 
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bfloat16 (ties to even), as float32."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    # NaN never occurs in the generated data; rounding adds 0x7FFF plus the
-    # lowest kept bit, then truncates the low 16 bits.
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16) << 16
-    return r.astype(np.uint32).view(np.float32).reshape(a.shape)
+    """Round float32 values to the nearest bfloat16 (ties to even), as float32.
+
+    Works on the bit pattern: add 0x7FFF plus the lowest kept bit, then clear
+    the low 16 bits.  Finite inputs cannot overflow 32 bits this way."""
+    out = np.array(a, dtype=np.float32, copy=True, order="C")
+    u = out.view(np.uint32)
+    step = 1 << 24
+    flat = u.reshape(-1)
+    for s in range(0, flat.size, step):
+        blk = flat[s:s + step]
+        lsb = (blk >> 16) & 1
+        blk += np.uint32(0x7FFF) + lsb
+        blk &= np.uint32(0xFFFF0000)
+    return out
 
 
 @dataclasses.dataclass(frozen=True)

@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, reports sizes and stage names, and rejects bad arguments on
+the host before any CUDA call."""
+import ctypes
+
+import pytest
+
+from state_space_model_09_b300 import ssd as S
+
+
+def test_exports_every_declared_function():
+    names = S.header_functions()
+    assert {"ssd_fwd", "ssd_multistep", "ssd_fwd_workspace_size", "ssd_status_string",
+            "ssd_version", "ssd_fwd_profiled", "ssd_check_device_error"} <= set(names)
+    lib = S.library_handle()
+    for n in names:
+        assert getattr(lib, n) is not None, n
+
+
+def test_version_and_status_strings():
+    assert S.ssd_version() == 10000
+    for st in range(5):
+        assert S.ssd_status_string(st)
+    assert S.ssd_status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups_b=1,
+                ngroups_c=1, io_dtype=S.SSD_BF16, dt_softplus=True)
+    base.update(kw)
+    return S.make_dims(**base)
+
+
+def test_workspace_size_layout():
+    d = _dims()
+    nc = 8
+    cs = 8 * 80 * nc * 256 * 4
+    st = 8 * nc * 80 * 128 * 64
+    assert S.ssd_fwd_workspace_size(d, 256) == cs + st * 4 + st * 2
+    # float32 I/O keeps the chunk initial states in float32
+    d32 = _dims(io_dtype=S.SSD_F32)
+    assert S.ssd_fwd_workspace_size(d32, 256) == cs + st * 4 + st * 4
+    # ragged T: ceil(T / Q) chunks
+    d2 = _dims(seqlen=2049)
+    assert S.ssd_fwd_workspace_size(d2, 256) > S.ssd_fwd_workspace_size(d, 256)
+
+
+def test_stage_names_follow_the_path():
+    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(4)] == \
+        ["dt_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"]
+    assert S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, 1) == "chunk_state_simt"
+    assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 3) == "chunk_scan_tc"
+    assert S.ssd_fwd_stage_name(_dims(), 256, 4) is None
+    assert S.ssd_fwd_num_stages(_dims(), 256) == 4
+
+
+@pytest.mark.parametrize("kw,chunk,status", [
+    (dict(headdim=24), 256, S.SSD_ERR_UNSUPPORTED),
+    (dict(dstate=272), 256, S.SSD_ERR_UNSUPPORTED),
+    (dict(ngroups_b=3), 256, S.SSD_ERR_INVALID_ARG),
+    (dict(batch=0), 256, S.SSD_ERR_INVALID_ARG),
+    (dict(io_dtype=7), 256, S.SSD_ERR_INVALID_ARG),
+    (dict(), 96, S.SSD_ERR_UNSUPPORTED),
+])
+def test_bad_dims_rejected_on_host(kw, chunk, status):
+    d = _dims(**kw)
+    assert S.ssd_fwd_workspace_size(d, chunk) == 0
+    lib = S.library_handle()
+    # fake, aligned, non-null "device" pointers: validation fails before any use
+    p = ctypes.c_void_p(1 << 20)
+    r = lib.ssd_fwd(ctypes.byref(d), p, p, p, p, p, None, None, chunk, ctypes.c_void_p(2 << 20),
+                    None, ctypes.c_void_p(3 << 20), 1 << 40, None)
+    assert r == status
+
+
+def test_null_and_misaligned_pointers_rejected():
+    d = _dims()
+    lib = S.library_handle()
+    good = [ctypes.c_void_p((k + 1) << 32) for k in range(5)]
+    y, ws = ctypes.c_void_p(9 << 32), ctypes.c_void_p(10 << 32)
+    args = lambda ins, yy: [ctypes.byref(d)] + ins + [None, None, 256, yy, None, ws, 1 << 40, None]
+    assert lib.ssd_fwd(*args([None] + good[1:], y)) == S.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fwd(*args(good, ctypes.c_void_p((9 << 32) + 8))) == S.SSD_ERR_INVALID_ARG
+    # short workspace
+    r = lib.ssd_fwd(ctypes.byref(d), *good, None, None, 256, y, None, ws, 1024, None)
+    assert r == S.SSD_ERR_INVALID_ARG
+    # output aliasing an input
+    r = lib.ssd_fwd(ctypes.byref(d), *good, None, None, 256, good[0], None, ws, 1 << 40, None)
+    assert r == S.SSD_ERR_INVALID_ARG
+
+
+def test_multistep_validation():
+    lib = S.library_handle()
+    d = _dims(seqlen=17)
+    p = [ctypes.c_void_p((k + 1) << 32) for k in range(11)]
+    assert lib.ssd_multistep(ctypes.byref(d), *p, None) == S.SSD_ERR_UNSUPPORTED
+    d = _dims(seqlen=8)
+    q = list(p)
+    q[7] = None  # j
+    assert lib.ssd_multistep(ctypes.byref(d), *q, None) == S.SSD_ERR_INVALID_ARG
+    q = list(p)
+    q[9] = q[6]  # h_j aliases h_cache
+    assert lib.ssd_multistep(ctypes.byref(d), *q, None) == S.SSD_ERR_INVALID_ARG

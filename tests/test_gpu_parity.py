@@ -1,0 +1,311 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerance (the layer's stated bar): max|y - y_ref| / max|y_ref| <= 1e-2 with
+bf16 inputs and float32 state, <= 1e-4 with float32 inputs; the same bound on
+every returned state.  Small shapes are compared element by element over the
+whole output; the full-size workloads are compared on sampled (b, h) pairs,
+which the oracle computes independently of the others.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_model_09_b300 import ssd as S
+from state_space_model_09_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {synth.F32: 1e-4, synth.BF16: 1e-2}
+
+
+def rel_err(got, ref):
+    return float(np.abs(got - ref).max() / np.abs(ref).max())
+
+
+def to_dev(inp, io):
+    dt_io = torch.bfloat16 if io == synth.BF16 else torch.float32
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif k in ("x", "B", "C"):
+            out[k] = torch.from_numpy(v).to(dt_io).cuda()
+        elif k == "j":
+            out[k] = torch.from_numpy(v).cuda()
+        else:
+            out[k] = torch.from_numpy(v).cuda()
+    return out
+
+
+def run_fwd(d, chunk, dt_softplus=True, with_final=True):
+    y = torch.full_like(d["x"], float("nan"))
+    b, T, H, P = d["x"].shape
+    N = d["B"].shape[3]
+    hf = torch.full((b, H, N, P), float("nan"), device="cuda") if with_final else None
+    dims = S.dims_of(d["x"], d["B"], d["C"], dt_softplus)
+    ws = S.workspace_for(dims, chunk)
+    ws.fill_(0xFF)  # NaN-poison the scratch
+    S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk, y, hf, ws,
+              dt_softplus)
+    S.ssd_check_device_error()
+    return y, hf
+
+
+def y_pairs(y, pairs, H):
+    """y [b,T,H,P] (torch) -> [len(pairs), T, P] float64 numpy."""
+    yy = y.float().cpu().numpy().astype(np.float64)
+    return np.stack([yy[p // H, :, p % H, :] for p in pairs])
+
+
+def h_pairs(h, pairs, H):
+    hh = h.cpu().numpy().astype(np.float64)
+    return np.stack([hh[p // H, p % H] for p in pairs])
+
+
+def check_fwd(shape, seed, pairs=None, dt_softplus=True, D_none=False):
+    inp = synth.make_fwd_inputs(shape, seed)
+    if D_none:
+        inp["D"] = None
+    if not dt_softplus:
+        inp["dt"] = np.abs(inp["dt"]) * np.float32(0.05)
+    d = to_dev(inp, shape.io)
+    y, hf = run_fwd(d, shape.chunk, dt_softplus)
+    H = shape.nheads
+    if pairs is None:
+        pairs = list(range(shape.batch * H))
+    y_ref, h_ref = oracle.ssd_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["h0"], dt_softplus=dt_softplus, pairs=pairs)
+    ey = rel_err(y_pairs(y, pairs, H), y_ref)
+    eh = rel_err(h_pairs(hf, pairs, H), h_ref)
+    tol = TOL[shape.io]
+    assert np.isfinite(ey) and np.isfinite(eh)
+    assert ey <= tol, "y rel err %.3g > %.1g" % (ey, tol)
+    assert eh <= tol, "h_final rel err %.3g > %.1g" % (eh, tol)
+    return ey, eh
+
+
+F = synth.FwdShape
+
+SMALL = {
+    # float32 I/O (CUDA-core float32 kernels)
+    "tiny_f32": (synth.WORKLOADS["tiny_f32"], 1000),
+    "f32_ragged_groups": (F(2, 200, 4, 48, 32, 2, 4, 64, synth.F32, "all"), 11),
+    "f32_T1": (F(1, 1, 2, 16, 16, 1, 1, 64, synth.F32, "all"), 12),
+    "f32_q128_short": (F(1, 100, 2, 32, 64, 1, 2, 128, synth.F32, "zero"), 13),
+    # bf16 I/O on the tensor-core kernels
+    "tc_q256_p64": (F(2, 600, 4, 64, 128, 1, 1, 256, synth.BF16, "all"), 21),
+    "tc_q256_exact": (F(1, 512, 3, 64, 128, 1, 1, 256, synth.BF16, "zero"), 22),
+    "tc_q128_p128_groups": (F(2, 300, 8, 128, 128, 2, 8, 128, synth.BF16, "half"), 23),
+    "tc_q128_p64": (F(1, 384, 4, 64, 128, 1, 4, 128, synth.BF16, "all"), 24),
+    "tc_T1": (F(1, 1, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 25),
+    "tc_T_short": (F(2, 77, 2, 64, 128, 1, 2, 256, synth.BF16, "all"), 26),
+    # bf16 I/O outside the tensor-core envelope (float32 CUDA-core kernels)
+    "bf16_q64_n64": (F(2, 160, 4, 64, 64, 1, 1, 64, synth.BF16, "all"), 31),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_fwd_small(name):
+    shape, seed = SMALL[name]
+    check_fwd(shape, seed)
+
+
+def test_fwd_tc_without_softplus_and_D():
+    check_fwd(F(1, 300, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 41, dt_softplus=False,
+              D_none=True)
+
+
+def test_fwd_f32_without_softplus_and_D():
+    check_fwd(F(1, 130, 2, 32, 32, 1, 1, 64, synth.F32, "all"), 42, dt_softplus=False,
+              D_none=True)
+
+
+def test_fwd_stage_path_matches_dtype():
+    d = S.make_dims(8, 2048, 80, 64, 128)
+    assert S.ssd_fwd_stage_name(d, 256, 3) == "chunk_scan_tc"
+
+
+# ---------------------------------------------------------------- full sizes
+@pytest.mark.parametrize("name", ["mamba2_2p7b", "long_16k", "hybrid_llama3_8b"])
+def test_fwd_full_size(name):
+    """The full workloads, in the launch configuration the benchmark times,
+    element by element over every (b, h) pair."""
+    shape = synth.WORKLOADS[name]
+    check_fwd(shape, synth.WORKLOAD_SEEDS[name])
+
+
+def test_fwd_split_with_carried_state_matches_whole():
+    """A prompt processed in two calls, the second starting from the first's
+    final state, gives the one-call result (sequential prefill)."""
+    shape = F(2, 1000, 4, 64, 128, 1, 1, 256, synth.BF16, "all")
+    inp = synth.make_fwd_inputs(shape, 51)
+    d = to_dev(inp, shape.io)
+    y, hf = run_fwd(d, 256)
+    T1 = 512
+    part = lambda k, sl: d[k][:, sl].contiguous()
+    d1 = dict(d, x=part("x", slice(0, T1)), dt=part("dt", slice(0, T1)), B=part("B", slice(0, T1)),
+              C=part("C", slice(0, T1)))
+    y1, h1 = run_fwd(d1, 256)
+    d2 = dict(d, x=part("x", slice(T1, None)), dt=part("dt", slice(T1, None)),
+              B=part("B", slice(T1, None)), C=part("C", slice(T1, None)), h0=h1)
+    y2, h2 = run_fwd(d2, 256)
+    ycat = torch.cat([y1, y2], dim=1).float()
+    assert (ycat - y.float()).abs().max() / y.float().abs().max() < 1e-2
+    assert (h2 - hf).abs().max() / hf.abs().max() < 1e-2
+
+
+def test_fwd_deterministic():
+    shape = F(1, 700, 4, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = to_dev(synth.make_fwd_inputs(shape, 52), shape.io)
+    y1, h1 = run_fwd(d, 256)
+    y2, h2 = run_fwd(d, 256)
+    assert torch.equal(y1, y2) and torch.equal(h1, h2)
+
+
+def test_fwd_profiled_events():
+    shape = synth.WORKLOADS["tiny_f32"]
+    d = to_dev(synth.make_fwd_inputs(shape, 1000), shape.io)
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    ws = S.workspace_for(dims, 64)
+    y = torch.empty_like(d["x"])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    S.ssd_fwd_profiled(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], None, 64, y, None, ws, ev)
+    torch.cuda.synchronize()
+    for a, b in zip(ev[:-1], ev[1:]):
+        assert a.elapsed_time(b) >= 0.0
+    y2, _ = run_fwd(d, 64, with_final=False)
+    assert torch.equal(y, y2)
+
+
+# ---------------------------------------------------------------- multistep
+def ms_device(inp, io, s):
+    dt_io = torch.bfloat16 if io == synth.BF16 else torch.float32
+    return dict(x=torch.from_numpy(inp["x"][s]).to(dt_io).cuda(),
+                dt=torch.from_numpy(inp["dt"][s]).cuda(),
+                B=torch.from_numpy(inp["B"][s]).to(dt_io).cuda(),
+                C=torch.from_numpy(inp["C"][s]).to(dt_io).cuda(),
+                j=torch.from_numpy(inp["j"][s]).cuda())
+
+
+M = synth.MultistepShape
+
+
+@pytest.mark.parametrize("shape,seed", [
+    (M(3, 5, 4, 64, 128, 2, 4, synth.BF16, 1), 61),
+    (M(2, 8, 4, 64, 128, 1, 1, synth.F32, 1), 62),
+    (M(2, 1, 2, 32, 48, 1, 2, synth.F32, 1), 63),
+    (M(2, 16, 2, 128, 256, 1, 1, synth.BF16, 1), 64),
+    (M(1, 3, 3, 48, 16, 1, 3, synth.F32, 1), 65),
+])
+def test_multistep_small(shape, seed):
+    inp = synth.make_multistep_inputs(shape, seed)
+    d = ms_device(inp, shape.io, 0)
+    A, D = torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["D"]).cuda()
+    hc = torch.from_numpy(inp["h_cache"]).cuda()
+    y, hj, hK = S.multistep(d["x"], d["dt"], A, d["B"], d["C"], D, hc, d["j"])
+    S.ssd_check_device_error()
+    yr, hjr, hKr = oracle.ssd_multistep(inp["x"][0], inp["dt"][0], inp["A"], inp["B"][0],
+                                        inp["C"][0], inp["D"], inp["h_cache"], inp["j"][0])
+    b, K, H, P = inp["x"][0].shape
+    pairs = list(range(b * H))
+    tol = TOL[shape.io]
+    assert rel_err(y_pairs(y, pairs, H), yr) <= tol
+    assert rel_err(h_pairs(hj, pairs, H), hjr) <= tol
+    assert rel_err(h_pairs(hK, pairs, H), hKr) <= tol
+
+
+def test_multistep_j_extremes_bit_exact():
+    shape = M(4, 8, 4, 64, 128, 1, 1, synth.BF16, 1)
+    inp = synth.make_multistep_inputs(shape, 66)
+    d = ms_device(inp, shape.io, 0)
+    A, D = torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["D"]).cuda()
+    hc = torch.from_numpy(inp["h_cache"]).cuda()
+    j = torch.tensor([0, 8, 0, 8], dtype=torch.int32, device="cuda")
+    y, hj, hK = S.multistep(d["x"], d["dt"], A, d["B"], d["C"], D, hc, j)
+    assert torch.equal(hj[0], hc[0]) and torch.equal(hj[2], hc[2])
+    assert torch.equal(hj[1], hK[1]) and torch.equal(hj[3], hK[3])
+
+
+def test_multistep_bad_j_reported():
+    shape = M(2, 4, 2, 64, 128, 1, 1, synth.BF16, 1)
+    inp = synth.make_multistep_inputs(shape, 67)
+    d = ms_device(inp, shape.io, 0)
+    A, D = torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["D"]).cuda()
+    hc = torch.from_numpy(inp["h_cache"]).cuda()
+    j = torch.tensor([1, 5], dtype=torch.int32, device="cuda")
+    S.multistep(d["x"], d["dt"], A, d["B"], d["C"], D, hc, j)
+    with pytest.raises(S.SsdError) as e:
+        S.ssd_check_device_error()
+    assert e.value.status == S.SSD_ERR_INVALID_ARG
+    S.ssd_check_device_error()  # the word was cleared
+
+
+def _chain(shape, inp, steps, graph: bool):
+    """Speculative chain: each step continues from h_j (ping-pong buffers)."""
+    dt_io = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
+    X = torch.from_numpy(inp["x"][:steps]).to(dt_io).cuda()
+    DT = torch.from_numpy(inp["dt"][:steps]).cuda()
+    BB = torch.from_numpy(inp["B"][:steps]).to(dt_io).cuda()
+    CC = torch.from_numpy(inp["C"][:steps]).to(dt_io).cuda()
+    J = torch.from_numpy(inp["j"][:steps]).cuda()
+    A, D = torch.from_numpy(inp["A"]).cuda(), torch.from_numpy(inp["D"]).cuda()
+    h0 = torch.from_numpy(inp["h_cache"]).cuda()
+    bufs = [torch.empty_like(h0), torch.empty_like(h0)]
+    hK = torch.empty_like(h0)
+    Y = torch.empty_like(X)
+    dims = S.dims_of(X[0], BB[0], CC[0])
+
+    def run():
+        cur = h0
+        for s in range(steps):
+            nxt = bufs[s % 2]
+            S.ssd_multistep(X[s], DT[s], A, BB[s], CC[s], D, cur, J[s], Y[s], nxt, hK, dims=dims)
+            cur = nxt
+        return cur
+
+    out = run()
+    torch.cuda.synchronize()
+    if not graph:
+        return Y, out
+    Y.fill_(float("nan"))
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        out = run()
+    g.replay()
+    torch.cuda.synchronize()
+    return Y, out
+
+
+def test_multistep_chain_full_size_sampled():
+    """The 1000-step speculative chain at the full decode shape; sampled
+    (b, h) pairs follow the oracle's chain step by step."""
+    shape = synth.WORKLOADS["multistep_k8"]
+    steps = shape.steps
+    inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"])
+    Y, h_last = _chain(shape, inp, steps, graph=True)
+    S.ssd_check_device_error()
+    b, K, H, P = inp["x"][0].shape
+    N = inp["B"].shape[-1]
+    pairs = list(range(0, b * H, 20))
+    cache = inp["h_cache"].copy()
+    worst = 0.0
+    for s in range(steps):
+        yr, hjr, _ = oracle.ssd_multistep(inp["x"][s], inp["dt"][s], inp["A"], inp["B"][s],
+                                          inp["C"][s], inp["D"], cache, inp["j"][s], pairs=pairs)
+        # the oracle continues from its own states (float32-rounded like the GPU's)
+        for q, p in enumerate(pairs):
+            cache[p // H, p % H] = hjr[q].astype(np.float32)
+        if s % 100 == 0 or s == steps - 1:
+            worst = max(worst, rel_err(y_pairs(Y[s], pairs, H), yr))
+    assert worst <= 1e-2
+    assert rel_err(h_pairs(h_last, pairs, H), np.stack([cache[p // H, p % H] for p in pairs])) <= 1e-2
+
+
+def test_multistep_graph_equals_eager():
+    shape = M(4, 8, 8, 64, 128, 1, 1, synth.BF16, 20)
+    inp = synth.make_multistep_inputs(shape, 68)
+    Y1, h1 = _chain(shape, inp, 20, graph=False)
+    Y2, h2 = _chain(shape, inp, 20, graph=True)
+    assert torch.equal(Y1, Y2) and torch.equal(h1, h2)
