@@ -137,6 +137,33 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
                          const void *B, const void *C, const float *D, const float *h_cache,
                          const int32_t *j, void *y, float *h_j, float *h_K, void *stream);
 
+/* Allocation-free variant of ssd_fwd.  The pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc at the point
+ * where they run the layer -- code working under a fixed device-memory plan
+ * that forbids allocation after start-up, code inside a framework whose
+ * caching allocator already owns the device memory (a raw cudaMalloc there
+ * sits outside its accounting, or fails once the pool holds everything), and
+ * latency-critical paths where cudaMalloc's implicit device synchronisation
+ * is not acceptable.
+ * Same arguments and results as ssd_fwd, without the workspace: the scratch
+ * lives in a static device array of SSD_NOALLOC_SCRATCH_BYTES bytes inside
+ * this library, which every GPU that loads the library holds until the
+ * process exits.  Shapes whose ssd_fwd_workspace_size() exceeds that return
+ * SSD_ERR_UNSUPPORTED before anything is launched.  The call allocates and
+ * frees nothing.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents; nothing in it needs to start at zero (every byte the
+ *     kernels read is written earlier in the same call).  Calls that overlap
+ *     on the GPU (different streams, or different host threads) race on the
+ *     array: serialise them. */
+#define SSD_NOALLOC_SCRATCH_BYTES (64ull << 20)
+ssd_status ssd_fwd_noalloc(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                           const void *B, const void *C, const float *D, const float *h0,
+                           int32_t chunk, void *y, float *h_final, void *stream);
+
 /* Synchronises `stream`, then reads and clears the library's device error
  * word: SSD_OK, or SSD_ERR_TIMEOUT if a kernel gave up a bounded wait since
  * the last check (its outputs are then invalid).  Diagnostic call; the only

@@ -342,6 +342,37 @@ const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_p
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Allocation-free prefill: the scratch of ssd_fwd_noalloc lives in this
+// static device array (SSD_NOALLOC_SCRATCH_BYTES), looked up once per device.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name only stands in for the symbol, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+ssd_status noalloc_scratch(void **addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSD_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SSD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return SSD_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk) {
@@ -375,6 +406,19 @@ ssd_status ssd_fwd_profiled(const ssd_dims *dims, const void *x, const float *dt
   if (!events) return SSD_ERR_INVALID_ARG;
   return fwd_impl(dims, x, dt, A, B, C, D, h0, chunk, y, h_final, workspace, workspace_bytes,
                   events, stream);
+}
+
+ssd_status ssd_fwd_noalloc(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                           const void *B, const void *C, const float *D, const float *h0,
+                           int32_t chunk, void *y, float *h_final, void *stream) {
+  Plan pl;
+  ssd_status st = make_plan(dims, chunk, &pl);
+  if (st != SSD_OK) return st;
+  if (pl.total > SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != SSD_OK) return st;
+  return fwd_impl(dims, x, dt, A, B, C, D, h0, chunk, y, h_final, scratch,
+                  SSD_NOALLOC_SCRATCH_BYTES, nullptr, stream);
 }
 
 ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, const float *A,

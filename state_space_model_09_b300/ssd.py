@@ -54,6 +54,8 @@ _lib.ssd_fwd.argtypes = _fwd_args + [_vp]
 _lib.ssd_fwd.restype = ctypes.c_int
 _lib.ssd_fwd_profiled.argtypes = _fwd_args + [_vp, _vp]
 _lib.ssd_fwd_profiled.restype = ctypes.c_int
+_lib.ssd_fwd_noalloc.argtypes = [_P] + [_vp] * 7 + [ctypes.c_int32, _vp, _vp, _vp]
+_lib.ssd_fwd_noalloc.restype = ctypes.c_int
 _lib.ssd_multistep.argtypes = [_P] + [_vp] * 11 + [_vp]
 _lib.ssd_multistep.restype = ctypes.c_int
 _lib.ssd_check_device_error.argtypes = [_vp]
@@ -171,6 +173,20 @@ def ssd_fwd_profiled(x, dt, A, B, C, D, h0, chunk: int, y, h_final, workspace,
     st = _lib.ssd_fwd_profiled(ctypes.byref(dims), *ins, int(chunk), outs[0], outs[1], outs[2],
                                ws_bytes, arr, _stream(stream))
     _check(st, "ssd_fwd_profiled")
+
+
+def ssd_fwd_noalloc(x, dt, A, B, C, D, h0, chunk: int, y, h_final, dt_softplus: bool = True,
+                    stream=None, dims: Optional[ssd_dims] = None) -> None:
+    """ssd_fwd without a caller workspace: for callers that cannot allocate
+    device memory where they run the layer (a fixed memory plan, a framework's
+    caching allocator owning the device, or a path that must not pay
+    cudaMalloc's implicit synchronisation).  The library's static scratch
+    array (SSD_NOALLOC_SCRATCH_BYTES) is used instead; larger shapes raise.
+    Calls on one device share that array, so they must not overlap."""
+    dims = dims or dims_of(x, B, C, dt_softplus)
+    st = _lib.ssd_fwd_noalloc(ctypes.byref(dims), *[_ptr(t) for t in (x, dt, A, B, C, D, h0)],
+                              int(chunk), _ptr(y), _ptr(h_final), _stream(stream))
+    _check(st, "ssd_fwd_noalloc")
 
 
 def ssd_multistep(x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, dt_softplus: bool = True,
