@@ -58,7 +58,7 @@ def fwd_work(s: synth.FwdShape):
     h_final (f32).  Flops count causal work only: P*Q(Q+1) (masked scores times
     x), 2QNP (chunk state), 2QNP (output from the initial state) per
     (b, chunk, head), plus N*Q(Q+1) per (b, chunk, distinct B/C group pair) for
-    C B^T.  Stage bytes count each stage's own inputs/outputs once."""
+    C B^T.  Stage bytes count each stage's own inputs and outputs once."""
     io = 2 if s.io == synth.BF16 else 4
     b, T, H, P, N, Q = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.chunk
     nc = math.ceil(T / Q)
@@ -72,16 +72,19 @@ def fwd_work(s: synth.FwdShape):
     flops = b * nc * H * (P * Q * (Q + 1) + 4 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)
     layer_bytes = 2 * x + Bb + Cb + dt + h0 + st
     cs = b * H * nc * Q * 4
-    S = b * nc * H * N * P * 4
-    hin = b * nc * H * N * P * (2 if s.io == synth.BF16 else 4)
-    stage_bytes = [dt + cs, x + Bb + cs + S, S + b * H * nc * 4 + h0 + hin + st,
-                   x + Bb + Cb + cs + hin + x]
-    stage_flops = [0, 2 * b * nc * H * Q * N * P,
-                   2 * b * nc * H * N * P,
-                   b * nc * H * (P * Q * (Q + 1) + 2 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)]
-    return dict(layer_bytes=layer_bytes, flops=flops, stage_bytes=stage_bytes,
-                stage_flops=stage_flops, tok_heads=b * T * H,
-                h2d=x + Bb + Cb + dt + h0 + 2 * H * 4, d2h=x + st)
+    S32 = b * nc * H * N * P * 4
+    hin16 = b * nc * H * N * P * 2
+    f_state = 2 * b * nc * H * Q * N * P
+    f_scan = b * nc * H * (P * Q * (Q + 1) + 2 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)
+    stages = {
+        "chunk_state_pass_tc": (x + Bb + dt + h0 + hin16 + st, f_state),
+        "chunk_scan_hl": (x + Bb + Cb + dt + hin16 + x, f_scan),
+        "dt_cumsum": (dt + cs, 0),
+        "chunk_state_simt": (x + Bb + cs + S32, f_state),
+        "state_passing": (S32 + b * H * nc * 4 + h0 + S32 + st, 2 * b * nc * H * N * P),
+        "chunk_scan_simt": (x + Bb + Cb + cs + S32 + x, f_scan),
+    }
+    return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -339,8 +342,7 @@ def run_ours(args, shape, work, world, rank, local):
     t_hbm = work["layer_bytes"] / (pk["hbm"] * 1e9)
     t_tc = work["flops"] / (pk["bf16"] * 1e12)
     dom = int(np.argmax(stage_ms))
-    dom_bytes = work["stage_bytes"][dom]
-    dom_flops = work["stage_flops"][dom]
+    dom_bytes, dom_flops = work["stages"][names[dom]]
     dom_s = stage_ms[dom] * 1e-3
     if dom_flops / (pk["bf16"] * 1e12) > dom_bytes / (pk["hbm"] * 1e9):
         roof = {"bound": "tensor", "achieved": round(dom_flops / dom_s / 1e12, 2),

@@ -21,6 +21,8 @@
 
 #include "../../include/ssd.h"
 #include "ssd_kernels.cuh"
+#include "ssd_scan.cuh"
+#include "ssd_state.cuh"
 #include "ssd_tc.cuh"
 
 namespace {
@@ -78,10 +80,17 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     return SSD_ERR_UNSUPPORTED;
   if (pl->b * pl->nc * pl->H > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
   const size_t states = static_cast<size_t>(pl->b) * pl->nc * pl->H * pl->N * pl->P;
-  pl->cs_off = 0;
-  pl->S_off = align_up(static_cast<size_t>(pl->b) * pl->H * pl->nc * pl->Q * sizeof(float));
-  pl->Hin_off = pl->S_off + align_up(states * sizeof(float));
-  pl->total = pl->Hin_off + align_up(states * (pl->tc ? 2 : 4));
+  if (pl->tc) {
+    // tensor-core path: only the chunk initial states (bf16) go through HBM
+    pl->cs_off = pl->S_off = 0;
+    pl->Hin_off = 0;
+    pl->total = align_up(states * 2);
+  } else {
+    pl->cs_off = 0;
+    pl->S_off = align_up(static_cast<size_t>(pl->b) * pl->H * pl->nc * pl->Q * sizeof(float));
+    pl->Hin_off = pl->S_off + align_up(states * sizeof(float));
+    pl->total = pl->Hin_off + align_up(states * sizeof(float));
+  }
   return SSD_OK;
 }
 
@@ -145,7 +154,7 @@ void record(void *const *events, int i, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 ssd_status launch_cumsum(const Plan &pl, const float *dt, const float *A, float *cs,
                          cudaStream_t s) {
-  dim3 grid(pl.nc, static_cast<unsigned>(pl.b));
+  dim3 grid(pl.nc, static_cast<unsigned>(pl.b), static_cast<unsigned>((pl.H + 31) / 32));
   switch (pl.Q) {
     case 64: ssd::dt_cumsum_kernel<64><<<grid, 256, 0, s>>>(dt, A, cs, pl.T, pl.H, pl.nc, pl.softplus); break;
     case 128: ssd::dt_cumsum_kernel<128><<<grid, 256, 0, s>>>(dt, A, cs, pl.T, pl.H, pl.nc, pl.softplus); break;
@@ -193,35 +202,33 @@ ssd_status launch_scan_simt(const Plan &pl, const void *x, const void *B, const 
   return launch_status();
 }
 
-template <int Q, int P>
-ssd_status launch_state_tc(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
-                           const float *cs, float *S, cudaStream_t s) {
-  using L = ssd::ChunkStateSmem<Q, P>;
-  auto k = ssd::chunk_state_tc<Q, P>;
+int num_sms() {
+  static int n = 0;
   static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
-  if (!ok) return SSD_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
-  k<<<grid, 128, L::kBytes, s>>>(mB, mX, cs, S, static_cast<int>(pl.H), static_cast<int>(pl.GB),
-                                 pl.nc);
-  return launch_status();
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  });
+  return n;
 }
 
-template <int Q, int P>
-ssd_status launch_scan_tc(const Plan &pl, const CUtensorMap &mC, const CUtensorMap &mB,
-                          const CUtensorMap &mX, const CUtensorMap &mH, const float *cs,
-                          const float *D, void *y, cudaStream_t s) {
-  using L = ssd::ChunkScanSmem<Q, P>;
-  auto k = ssd::chunk_scan_tc<Q, P>;
+template <int Q>
+ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
+                             const float *dt, const float *A, const float *h0, __nv_bfloat16 *Hin,
+                             float *h_final, cudaStream_t s) {
+  using L = ssd::StatePass<Q>;
+  auto k = ssd::chunk_state_pass_tc<Q>;
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
   if (!ok) return SSD_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
-  k<<<grid, 256, L::kBytes, s>>>(mC, mB, mX, mH, cs, D, static_cast<__nv_bfloat16 *>(y), pl.T,
-                                 static_cast<int>(pl.H), static_cast<int>(pl.GB),
-                                 static_cast<int>(pl.GC), pl.nc);
+  dim3 grid(static_cast<unsigned>(pl.P / L::PS), static_cast<unsigned>(pl.H),
+            static_cast<unsigned>(pl.b));
+  k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
+                                         static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
+                                         static_cast<int>(pl.P), pl.softplus);
   return launch_status();
 }
 
@@ -243,6 +250,44 @@ ssd_status launch_multistep(dim3 grid, int threads, int64_t smem, const ssd_dims
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
       static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus);
+  return launch_status();
+}
+
+// Heads per CTA of chunk_scan_hl: trades the per-group C B^T product (paid
+// once per CTA) against wave quantisation over the SMs.
+int scan_heads_per_cta(const Plan &pl, int num_sms) {
+  const bool shared = pl.GB == 1 && pl.GC == 1;
+  const double t_head = 1.0, t_group = shared ? 1.5 : 0.0;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int hp = 1; hp <= ssd::ScanHL<128, 64>::kMaxHeads && hp <= pl.H; ++hp) {
+    const int64_t ctas = ((pl.H + hp - 1) / hp) * pl.nc * pl.b;
+    const double waves = static_cast<double>((ctas + num_sms - 1) / num_sms);
+    const double groups = shared ? 1.0 : static_cast<double>(hp);
+    const double cost = waves * (hp * t_head + groups * (shared ? t_group : 0.5));
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = hp;
+    }
+  }
+  return best;
+}
+
+template <int Q, int P>
+ssd_status launch_scan_hl(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
+                          const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
+                          const float *dt, const float *A, const float *D, cudaStream_t s) {
+  using L = ssd::ScanHL<Q, P>;
+  auto k = ssd::chunk_scan_hl<Q, P>;
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+  if (!ok) return SSD_ERR_CUDA;
+  const int hpc = scan_heads_per_cta(pl, num_sms());
+  dim3 grid(static_cast<unsigned>((pl.H + hpc - 1) / hpc), pl.nc, static_cast<unsigned>(pl.b));
+  k<<<grid, L::kThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, pl.T,
+                                         static_cast<int>(pl.H), static_cast<int>(pl.GB),
+                                         static_cast<int>(pl.GC), pl.nc, hpc, pl.softplus);
   return launch_status();
 }
 
@@ -289,7 +334,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   void *Hin = ws + pl.Hin_off;
 
   if (pl.tc) {
-    CUtensorMap mX, mB, mC, mH;
+    CUtensorMap mX, mB, mC32, mH, mY;
     const cuuint64_t hdims[3] = {static_cast<cuuint64_t>(pl.P), static_cast<cuuint64_t>(pl.N),
                                  static_cast<cuuint64_t>(pl.b * pl.nc * pl.H)};
     const cuuint64_t hstr[2] = {static_cast<cuuint64_t>(pl.P * 2),
@@ -297,25 +342,20 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     const cuuint32_t hbox[3] = {64, static_cast<cuuint32_t>(pl.N), 1};
     if (!encode_btgw(&mX, x, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
         !encode_btgw(&mB, B, pl.b, pl.T, pl.GB, pl.N, pl.Q) ||
-        !encode_btgw(&mC, C, pl.b, pl.T, pl.GC, pl.N, pl.Q) ||
+        !encode_btgw(&mC32, C, pl.b, pl.T, pl.GC, pl.N, 32) ||
+        !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
         !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
       return SSD_ERR_CUDA;
     record(events, 0, s);
-    if ((st = launch_cumsum(pl, dt, A, cs, s)) != SSD_OK) return st;
+    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s)
+                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s);
+    if (st != SSD_OK) return st;
     record(events, 1, s);
-    if (pl.Q == 256) st = launch_state_tc<256, 64>(pl, mB, mX, cs, S, s);
-    else if (pl.P == 64) st = launch_state_tc<128, 64>(pl, mB, mX, cs, S, s);
-    else st = launch_state_tc<128, 128>(pl, mB, mX, cs, S, s);
+    if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
+    else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
+    else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     if (st != SSD_OK) return st;
     record(events, 2, s);
-    if ((st = launch_passing(pl, S, cs, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s)) != SSD_OK)
-      return st;
-    record(events, 3, s);
-    if (pl.Q == 256) st = launch_scan_tc<256, 64>(pl, mC, mB, mX, mH, cs, D, y, s);
-    else if (pl.P == 64) st = launch_scan_tc<128, 64>(pl, mC, mB, mX, mH, cs, D, y, s);
-    else st = launch_scan_tc<128, 128>(pl, mC, mB, mX, mH, cs, D, y, s);
-    if (st != SSD_OK) return st;
-    record(events, 4, s);
     return SSD_OK;
   }
 
@@ -336,7 +376,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   return SSD_OK;
 }
 
-const char *const kStageNamesTc[] = {"dt_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"};
+const char *const kStageNamesTc[] = {"chunk_state_pass_tc", "chunk_scan_hl"};
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
 
@@ -382,12 +422,13 @@ size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk) {
 
 int32_t ssd_fwd_num_stages(const ssd_dims *dims, int32_t chunk) {
   Plan pl;
-  return make_plan(dims, chunk, &pl) == SSD_OK ? 4 : 0;
+  if (make_plan(dims, chunk, &pl) != SSD_OK) return 0;
+  return pl.tc ? 2 : 4;
 }
 
 const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
-  if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= 4) return nullptr;
+  if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= (pl.tc ? 2 : 4)) return nullptr;
   return pl.tc ? kStageNamesTc[i] : kStageNamesSimt[i];
 }
 

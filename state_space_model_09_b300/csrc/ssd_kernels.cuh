@@ -17,7 +17,8 @@ namespace ssd {
 // mask L and whose last entry gives the chunk decay; Mamba-2 page, section
 // "SSD算法", the modified A factors of the state-passing step).  Positions past
 // T contribute 0, so a short last chunk keeps its last valid value.
-// grid (nc, batch), 256 threads; warp w handles heads w, w+8, ...
+// grid (nc, batch, ceil(H/32)), 256 threads: the block stages the chunk's
+// dt rows for 32 heads (coalesced), then warp w scans heads w, w+8, ...
 // ----------------------------------------------------------------------------
 template <int Q>
 __global__ void __launch_bounds__(256) dt_cumsum_kernel(const float *__restrict__ dt,
@@ -25,22 +26,27 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(const float *__restrict_
                                                          float *__restrict__ cs, int64_t T, int H,
                                                          int nc, int softplus) {
   constexpr int PER = Q / 32;
-  const int c = blockIdx.x, b = blockIdx.y;
+  __shared__ float tile[Q][33];
+  const int c = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * 32;
+  const int nh = min(32, H - h0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
-  for (int h = warp; h < H; h += 8) {
-    const float Ah = A[h];
+  const int64_t tc = static_cast<int64_t>(c) * Q;
+  for (int idx = threadIdx.x; idx < Q * 32; idx += 256) {
+    const int t = idx >> 5, hh = idx & 31;
+    float d = 0.f;
+    if (hh < nh && tc + t < T) {
+      const float z = dt[(static_cast<int64_t>(b) * T + tc + t) * H + h0 + hh];
+      d = (softplus ? softplus_f32(z) : z) * A[h0 + hh];
+    }
+    tile[t][hh] = d;
+  }
+  __syncthreads();
+  for (int hh = warp; hh < nh; hh += 8) {
     float v[PER];
     float run = 0.f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const int64_t t = t0 + k;
-      float d = 0.f;
-      if (t < T) {
-        const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
-        d = (softplus ? softplus_f32(z) : z) * Ah;
-      }
-      run += d;
+      run += tile[lane * PER + k][hh];
       v[k] = run;
     }
     float incl = run;
@@ -50,7 +56,7 @@ __global__ void __launch_bounds__(256) dt_cumsum_kernel(const float *__restrict_
       if (lane >= off) incl += o;
     }
     const float excl = incl - run;
-    float *out = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q + lane * PER;
+    float *out = cs + ((static_cast<int64_t>(b) * H + h0 + hh) * nc + c) * Q + lane * PER;
 #pragma unroll
     for (int k = 0; k < PER; ++k) out[k] = v[k] + excl;
   }

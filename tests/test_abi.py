@@ -36,8 +36,9 @@ def test_workspace_size_layout():
     nc = 8
     cs = 8 * 80 * nc * 256 * 4
     st = 8 * nc * 80 * 128 * 64
-    assert S.ssd_fwd_workspace_size(d, 256) == cs + st * 4 + st * 2
-    # float32 I/O keeps the chunk initial states in float32
+    # tensor-core path: only the bf16 chunk initial states
+    assert S.ssd_fwd_workspace_size(d, 256) == st * 2
+    # float32 path: cumsums, chunk states and chunk initial states in float32
     d32 = _dims(io_dtype=S.SSD_F32)
     assert S.ssd_fwd_workspace_size(d32, 256) == cs + st * 4 + st * 4
     # ragged T: ceil(T / Q) chunks
@@ -46,12 +47,14 @@ def test_workspace_size_layout():
 
 
 def test_stage_names_follow_the_path():
-    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(4)] == \
-        ["dt_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"]
-    assert S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, 1) == "chunk_state_simt"
-    assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 3) == "chunk_scan_tc"
-    assert S.ssd_fwd_stage_name(_dims(), 256, 4) is None
-    assert S.ssd_fwd_num_stages(_dims(), 256) == 4
+    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(2)] == \
+        ["chunk_state_pass_tc", "chunk_scan_hl"]
+    assert [S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, i) for i in range(4)] == \
+        ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
+    assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"
+    assert S.ssd_fwd_stage_name(_dims(), 256, 2) is None
+    assert S.ssd_fwd_num_stages(_dims(), 256) == 2
+    assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
 
 
 @pytest.mark.parametrize("kw,chunk,status", [

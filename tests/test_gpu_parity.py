@@ -123,7 +123,7 @@ def test_fwd_f32_without_softplus_and_D():
 
 def test_fwd_stage_path_matches_dtype():
     d = S.make_dims(8, 2048, 80, 64, 128)
-    assert S.ssd_fwd_stage_name(d, 256, 3) == "chunk_scan_tc"
+    assert S.ssd_fwd_stage_name(d, 256, 1) == "chunk_scan_hl"
 
 
 # ---------------------------------------------------------------- full sizes
@@ -169,7 +169,7 @@ def test_fwd_profiled_events():
     dims = S.dims_of(d["x"], d["B"], d["C"])
     ws = S.workspace_for(dims, 64)
     y = torch.empty_like(d["x"])
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(S.ssd_fwd_num_stages(dims, 64) + 1)]
     S.ssd_fwd_profiled(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], None, 64, y, None, ws, ev)
     torch.cuda.synchronize()
     for a, b in zip(ev[:-1], ev[1:]):
