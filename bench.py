@@ -380,18 +380,122 @@ def run_ours(args, shape, work, world, rank, local):
     print(json.dumps(line, ensure_ascii=False))
 
 
+# ----------------------------------------------------------------------------- multistep arm
+def multistep_work(s: synth.MultistepShape):
+    """Bytes of one multi-step call: h_cache in, h_j and h_K out (f32), x and y
+    (io), B, C (io), dt (f32), j (int32)."""
+    io = 2 if s.io == synth.BF16 else 4
+    st = s.batch * s.nheads * s.dstate * s.headdim * 4
+    x = s.batch * s.K * s.nheads * s.headdim * io
+    bc = s.batch * s.K * (s.ngroups_b + s.ngroups_c) * s.dstate * io
+    return dict(bytes=3 * st + 2 * x + bc + s.batch * s.K * s.nheads * 4 + s.batch * 4,
+                tok_heads=s.batch * s.K * s.nheads)
+
+
+def run_multistep(args, world, rank, local):
+    """One step = one ssd_multistep call of the speculative chain (each step
+    continues from h_j).  The chain of `shape.steps` calls is captured in a
+    CUDA graph and replayed; the time per call is the replay time / steps."""
+    import torch
+    from state_space_model_09_b300 import ssd as S
+
+    shape = synth.WORKLOADS["multistep_k8"]
+    work = multistep_work(shape)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"] + 17 * rank)
+    bf = torch.bfloat16
+    X = torch.from_numpy(inp["x"]).to(bf).to(dev)
+    DT = torch.from_numpy(inp["dt"]).to(dev)
+    BB = torch.from_numpy(inp["B"]).to(bf).to(dev)
+    CC = torch.from_numpy(inp["C"]).to(bf).to(dev)
+    J = torch.from_numpy(inp["j"]).to(dev)
+    A = torch.from_numpy(inp["A"]).to(dev)
+    D = torch.from_numpy(inp["D"]).to(dev)
+    h0 = torch.from_numpy(inp["h_cache"]).to(dev)
+    bufs = [torch.empty_like(h0), torch.empty_like(h0)]
+    hK = torch.empty_like(h0)
+    Y = torch.empty_like(X)
+    dims = S.dims_of(X[0], BB[0], CC[0])
+    steps = shape.steps
+    stream = torch.cuda.Stream(dev)
+
+    def chain():
+        cur = h0
+        for i in range(steps):
+            nxt = bufs[i % 2]
+            S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur, J[i], Y[i], nxt, hK,
+                            stream=stream, dims=dims)
+            cur = nxt
+
+    with torch.cuda.stream(stream):
+        chain()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain()
+    reps = max(1, args.steps // steps) if args.steps >= steps else 1
+    with torch.cuda.stream(stream):  # replays run on the current stream
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        S.ssd_check_device_error(stream)
+        clocks = ClockSampler(gpu_id_for(dev))
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / (reps * steps), world, dev)
+    if rank != 0:
+        return
+    pk = peaks()
+    gbs = work["bytes"] / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)",
+        "value": round(world * work["tok_heads"] / (ms_step * 1e-3) / 1e6, 2), "unit": UNIT,
+        "n_gpus": world, "steps": reps * steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": "multistep_k8", "batch": shape.batch, "K": shape.K,
+                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                   "chain": steps, "graph": True,
+                   "l2": "states 3 x 42 MB per step (h_cache, h_j, h_K) ~ L2 size; no flush"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm"], 4), "traffic": None, "kernel": "multistep_kernel",
+                     "algorithmic_bytes": work["bytes"], "peak_source": pk["source"] + " (burst)"},
+        "gpu_launches": reps * steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line, ensure_ascii=False))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mamba2_2p7b",
-                    choices=[k for k, v in synth.WORKLOADS.items() if isinstance(v, synth.FwdShape)])
+    ap.add_argument("--workload", default="mamba2_2p7b", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload == "multistep_k8":
+        if args.impl == "reference":
+            if int(os.environ.get("RANK", "0")) == 0:
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the oracle arm is timed on the prefill workloads only"}))
+            return
+        world, rank, local = dist_setup()
+        run_multistep(args, world, rank, local)
+        return
     shape = synth.WORKLOADS[args.workload]
     work = fwd_work(shape)
     if args.impl == "reference":

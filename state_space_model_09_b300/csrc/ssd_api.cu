@@ -232,20 +232,17 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   return launch_status();
 }
 
-constexpr int64_t kMultistepSmemMax = 200 * 1024;
-
-template <typename IO, int RPT>
-ssd_status launch_multistep(dim3 grid, int threads, int64_t smem, const ssd_dims *d,
-                            const void *x, const float *dt, const float *A, const void *B,
-                            const void *C, const float *D, const float *h_cache,
-                            const int32_t *j, void *y, float *h_j, float *h_K, int PS,
-                            cudaStream_t s) {
-  auto k = ssd::multistep_kernel<IO, RPT>;
+template <typename IO, int KT>
+ssd_status launch_multistep(dim3 grid, int64_t smem, const ssd_dims *d, const void *x,
+                            const float *dt, const float *A, const void *B, const void *C,
+                            const float *D, const float *h_cache, const int32_t *j, void *y,
+                            float *h_j, float *h_K, int PS, cudaStream_t s) {
+  auto k = ssd::multistep_kernel<IO, KT>;
   static std::once_flag once;
   static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, static_cast<int>(kMultistepSmemMax)); });
+  std::call_once(once, [&] { ok = set_smem(k, 227 * 1024); });
   if (!ok) return SSD_ERR_CUDA;
-  k<<<grid, threads, static_cast<size_t>(smem), s>>>(
+  k<<<grid, ssd::kMsThreads, static_cast<size_t>(smem), s>>>(
       static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
@@ -498,29 +495,18 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
 
   // column slice per block: the largest of 128, 64, 32, 16 that divides P
   const int PS = P % 128 == 0 ? 128 : P % 64 == 0 ? 64 : P % 32 == 0 ? 32 : 16;
-  const int TP = PS / 4;
-  auto smem_for = [&](int rpt, int *threads_out) {
-    int threads = TP * (static_cast<int>(N) / rpt);
-    threads = threads < 32 ? 32 : (threads + 31) / 32 * 32;
-    *threads_out = threads;
-    return (2 * K * N + K * PS + 16 + K * static_cast<int64_t>(threads / 32) * PS) * 4;
-  };
-  int threads = 0;
-  int rpt = 8;
-  int64_t smem = smem_for(8, &threads);
-  if (smem > kMultistepSmemMax || threads > 512) {
-    rpt = 16;
-    smem = smem_for(16, &threads);
-  }
-  if (smem > kMultistepSmemMax || threads > 512) return SSD_ERR_UNSUPPORTED;
+  const int R = ssd::kMsItemThreads / (PS / 4);
+  if (N % R) return SSD_ERR_UNSUPPORTED;
+  const int64_t smem = 2 * (2 * K * N + K * PS + ssd::kMsMaxK + K * 2 * PS) * 4;
+  if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
+  dim3 grid(static_cast<unsigned>((H + 1) / 2), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
   if (bf16) {
-    st = rpt == 8 ? launch_multistep<__nv_bfloat16, 8>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
-                  : launch_multistep<__nv_bfloat16, 16>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
+    st = K <= 8 ? launch_multistep<__nv_bfloat16, 8>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
+                : launch_multistep<__nv_bfloat16, 16>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
   } else {
-    st = rpt == 8 ? launch_multistep<float, 8>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
-                  : launch_multistep<float, 16>(grid, threads, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
+    st = K <= 8 ? launch_multistep<float, 8>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
+                : launch_multistep<float, 16>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
   }
   return st;
 }

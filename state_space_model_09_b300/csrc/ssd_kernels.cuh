@@ -198,121 +198,132 @@ __global__ void __launch_bounds__(256) chunk_scan_simt(
 
 // ----------------------------------------------------------------------------
 // K-token multi-step decode ("Mamba in the Llama", 推测解码, MultiStep).
-// One block per (h, b, p-slice of PS columns).  The block's slice of the state
-// (N x PS floats) lives in registers: thread (r, q) holds rows r, r+R, ...
-// (RPT of them) of the 4 columns 4q..4q+3, R = N / RPT row groups.
-// Per token: h = a h + B x^T, then y = C^T h + D x reduced over rows by warp
-// shuffles and shared memory.  h_j is stored when the step count reaches j.
-// dynamic smem: B[K][N], C[K][N], x[K][PS], a[16], partial y [K][warps][PS].
+// A block of 128 threads serves two items (heads 2 blockIdx.x and +1 of batch
+// row b, p-slice of PS columns); 64 threads per item.  Thread (r, q) of an item
+// handles the 4 columns 4q..4q+3 of state rows r, r + R, r + 2R, ...
+// (R = 64 / (PS/4) row groups) and streams them: a row's 4 values are
+// advanced through the K tokens (h = a h + B x^T; written to h_j after j
+// tokens and to h_K after K) and add C_k[n] h to the thread's y partials,
+// which stay in registers; loads run four rows ahead.  y = sum over rows
+// (warp shuffles + shared memory) + D x.  The state is never held whole
+// (42 MB of state would not fit the register file), so the whole grid is
+// resident at once.
+// dynamic smem per item: B[K][N], C[K][N], x[K][PS], a[16], y partials [K][2][PS].
 // ----------------------------------------------------------------------------
-template <typename IO>
-__device__ __forceinline__ float4 load_io4(const IO *p);
-template <> __device__ __forceinline__ float4 load_io4<float>(const float *p) {
-  return *reinterpret_cast<const float4 *>(p);
-}
-template <> __device__ __forceinline__ float4 load_io4<__nv_bfloat16>(const __nv_bfloat16 *p) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(p);
-  const float2 a = unpack_bf16x2(u.x), c = unpack_bf16x2(u.y);
-  return make_float4(a.x, a.y, c.x, c.y);
-}
+constexpr int kMsThreads = 128;
+constexpr int kMsItemThreads = 64;
+constexpr int kMsMaxK = 16;
 
-template <typename IO, int RPT>
-__global__ void __launch_bounds__(512) multistep_kernel(
+template <typename IO, int KT>
+__global__ void __launch_bounds__(128, 5) multistep_kernel(
     const IO *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const IO *__restrict__ Bm, const IO *__restrict__ Cm, const float *__restrict__ D,
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
     float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N, int P,
     int PS, int softplus) {
+  // KT: compile-time bound on K (8 or 16); K <= KT
   extern __shared__ float sm_ms[];
-  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-  float *sB = sm_ms;
+  const int item = threadIdx.x / kMsItemThreads;  // 0 or 1
+  const int h = 2 * blockIdx.x + item, b = blockIdx.y, p0 = blockIdx.z * PS;
+  const int tid = threadIdx.x % kMsItemThreads, lane = threadIdx.x & 31;
+  const int warp = tid >> 5;  // warp within the item: 0 or 1
+  const int item_floats = 2 * K * N + K * PS + kMsMaxK + K * 2 * PS;
+  float *sB = sm_ms + item * item_floats;
   float *sC = sB + K * N;
   float *sx = sC + K * N;
   float *sa = sx + K * PS;
-  float *red = sa + 16;
-  const int h = blockIdx.x, b = blockIdx.y, p0 = blockIdx.z * PS;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gb = h / (H / GB), gc = h / (H / GC);
-  const int TP = PS / 4, R = N / RPT;
+  float *red = sa + kMsMaxK;
+  const bool live = h < H;
+  const int hh = live ? h : H - 1;
+  const int gb = hh / (H / GB), gc = hh / (H / GC);
+  const int TP = PS / 4, R = kMsItemThreads / TP;
   const int q = tid % TP, r = tid / TP;
-  const bool active = r < R;
 
-  for (int i = tid; i < K * N; i += nthreads) {
+  for (int i = tid; i < K * N; i += kMsItemThreads) {
     const int k = i / N, n = i % N;
     sB[i] = to_f32(Bm[((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n]);
     sC[i] = to_f32(Cm[((static_cast<int64_t>(b) * K + k) * GC + gc) * N + n]);
   }
-  for (int i = tid; i < K * PS; i += nthreads) {
+  for (int i = tid; i < K * PS; i += kMsItemThreads) {
     const int k = i / PS, p = i % PS;
-    sx[i] = to_f32(x[((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p]);
+    sx[i] = to_f32(x[((static_cast<int64_t>(b) * K + k) * H + hh) * P + p0 + p]);
   }
   if (tid < K) {
-    const float z = dt[(static_cast<int64_t>(b) * K + tid) * H + h];
-    sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[h]);
+    const float z = dt[(static_cast<int64_t>(b) * K + tid) * H + hh];
+    sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
   }
   int jb = jacc[b];
   if (jb < 0 || jb > K) {
     if (tid == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
     jb = -1;
   }
-
-  const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
-  float4 st[RPT];
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    st[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) st[i] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + (r + R * i) * P));
-  }
-  if (jb == 0 && active) {
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4 *>(h_j + base + (r + R * i) * P) = st[i];
-  }
   __syncthreads();
 
-  for (int k = 0; k < K; ++k) {
-    const float a = sa[k];
-    float4 yp = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) {
-      const float4 xv = *reinterpret_cast<const float4 *>(sx + k * PS + 4 * q);
+  float4 yp[KT];
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const int n = r + R * i;
-        const float bn = sB[k * N + n], cn = sC[k * N + n];
-        st[i].x = fmaf(a, st[i].x, bn * xv.x);
-        st[i].y = fmaf(a, st[i].y, bn * xv.y);
-        st[i].z = fmaf(a, st[i].z, bn * xv.z);
-        st[i].w = fmaf(a, st[i].w, bn * xv.w);
-        yp.x = fmaf(cn, st[i].x, yp.x);
-        yp.y = fmaf(cn, st[i].y, yp.y);
-        yp.z = fmaf(cn, st[i].z, yp.z);
-        yp.w = fmaf(cn, st[i].w, yp.w);
+  for (int k = 0; k < KT; ++k) yp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (live) {
+    const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
+    const int rows = N / R;
+    constexpr int PF = 4;  // rows in flight
+    float4 buf[PF];
+#pragma unroll
+    for (int u = 0; u < PF; ++u)
+      if (u < rows) buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(r + R * u) * P));
+    for (int i0 = 0; i0 < rows; i0 += PF) {
+#pragma unroll
+      for (int u = 0; u < PF; ++u) {
+        const int i = i0 + u;
+        if (i < rows) {
+          const int n = r + R * i;
+          float4 st = buf[u];
+          if (i + PF < rows)
+            buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(n + R * PF) * P));
+          const int64_t off = base + static_cast<int64_t>(n) * P;
+          if (jb == 0) __stcs(reinterpret_cast<float4 *>(h_j + off), st);
+#pragma unroll
+          for (int k = 0; k < KT; ++k) {
+            if (k < K) {
+              const float bn = sB[k * N + n], cn = sC[k * N + n], a = sa[k];
+              const float4 xk = *reinterpret_cast<const float4 *>(sx + k * PS + 4 * q);
+              st.x = fmaf(a, st.x, bn * xk.x);
+              st.y = fmaf(a, st.y, bn * xk.y);
+              st.z = fmaf(a, st.z, bn * xk.z);
+              st.w = fmaf(a, st.w, bn * xk.w);
+              yp[k].x = fmaf(cn, st.x, yp[k].x);
+              yp[k].y = fmaf(cn, st.y, yp[k].y);
+              yp[k].z = fmaf(cn, st.z, yp[k].z);
+              yp[k].w = fmaf(cn, st.w, yp[k].w);
+              if (k + 1 == jb) __stcs(reinterpret_cast<float4 *>(h_j + off), st);
+            }
+          }
+          __stcs(reinterpret_cast<float4 *>(h_K + off), st);
+        }
       }
     }
-    // lanes q, q + TP, q + 2TP, ... of a warp hold the same 4 columns
-    for (int off = TP; off < 32; off <<= 1) {
-      yp.x += __shfl_xor_sync(0xffffffffu, yp.x, off);
-      yp.y += __shfl_xor_sync(0xffffffffu, yp.y, off);
-      yp.z += __shfl_xor_sync(0xffffffffu, yp.z, off);
-      yp.w += __shfl_xor_sync(0xffffffffu, yp.w, off);
-    }
-    if (lane < TP) *reinterpret_cast<float4 *>(red + (k * nwarps + warp) * PS + 4 * lane) = yp;
-    if (k + 1 == jb && active) {
+  }
+  // reduce the y partials over row groups: lanes q, q + TP, ... of a warp, then 2 warps
 #pragma unroll
-      for (int i = 0; i < RPT; ++i)
-        *reinterpret_cast<float4 *>(h_j + base + (r + R * i) * P) = st[i];
+  for (int k = 0; k < KT; ++k) {
+    if (k < K) {
+      float4 v = yp[k];
+      for (int off = TP; off < 32; off <<= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, off);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, off);
+      }
+      if (lane < TP) *reinterpret_cast<float4 *>(red + (k * 2 + warp) * PS + 4 * lane) = v;
     }
   }
   __syncthreads();
+  if (!live) return;
   const float Dh = D ? D[h] : 0.f;
-  for (int i = tid; i < K * PS; i += nthreads) {
+  for (int i = tid; i < K * PS; i += kMsItemThreads) {
     const int k = i / PS, p = i % PS;
-    float acc = 0.f;
-    for (int w = 0; w < nwarps; ++w) acc += red[(k * nwarps + w) * PS + p];
+    const float acc = red[(k * 2) * PS + p] + red[(k * 2 + 1) * PS + p];
     y[((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p] = from_f32<IO>(acc + Dh * sx[i]);
-  }
-  if (active) {
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) *reinterpret_cast<float4 *>(h_K + base + (r + R * i) * P) = st[i];
   }
 }
 
