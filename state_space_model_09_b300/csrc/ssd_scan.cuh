@@ -15,7 +15,7 @@
 //   mask:  A2 = bf16(L o S + D I)           (TMEM -> registers -> swizzled smem)
 //   scale: Y *= exp(cs_i) row by row        (tcgen05.ld / tcgen05.st)
 //   MMA2:  Y += A2 x                        (K = causal columns)
-//   out:   y = bf16(Y), staged in smem, written by a TMA tile store
+//   out:   y = bf16(Y), staged in smem, written by TMA tile stores
 // L is never formed in memory.  It is factorised per 32-column band: for a row
 // i below band k (reference column r_k = 32k + 31),
 //   L[i,j] = exp(cs_i - cs_rk) * exp(cs_rk - cs_j),
@@ -28,9 +28,9 @@
 // quarter q holds rows 32q.. of the first tile and rows 224 - 32q.. of the
 // second: every quarter then has nine non-zero 32-column bands.
 //
-// Warp roles: warps 0-7 (256 threads) do the cumsum, mask, scaling and output;
-// warp 8 (one elected lane) issues every TMA load and MMA.  Every wait is
-// bounded in time.
+// Warp roles: warps 0-15 (512 threads; four per TMEM lane quarter) do the
+// cumsum, mask, scaling and output; warp 16 (one elected lane) issues every
+// TMA load and MMA.  Every wait is bounded in time.
 #pragma once
 
 #include "ssd_device.cuh"
@@ -56,8 +56,16 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// barrier among the 256 compute threads only (warps 0-7)
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// waits until at most one committed bulk store group of this thread is still
+// reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+constexpr int kScanComputeWarps = 16;
+constexpr int kScanThreads = 32 * (kScanComputeWarps + 1);
+// barrier among the compute threads only (warps 0-15)
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 template <int Q, int P>
 struct ScanHL {
@@ -69,10 +77,10 @@ struct ScanHL {
   static constexpr int kU = kB > kA2 ? kB : kA2;
   static constexpr int kX = P * Q * 2;
   static constexpr int kH = P * N * 2;
-  static constexpr int kStage = P * Q * 2;  // y staging, inside the first A2 block
-  static constexpr int kMaxHeads = 12;        // most heads per CTA
-  // cs*log2e, exp(cs), band factors, warp sums, A, D, dt [Q][kMaxHeads]
-  static constexpr int kFloats = 3 * Q + 16 + 2 * kMaxHeads + Q * kMaxHeads;
+  static constexpr int kStageTile = P * 128 * 2;  // y staging of one 128-row tile
+  static constexpr int kMaxHeads = 12;            // most heads per CTA
+  // cs*log2e, exp(cs), band factors, warp sums, D, softplus(dt)*A [Q][kMaxHeads]
+  static constexpr int kFloats = 3 * Q + 32 + kMaxHeads + Q * kMaxHeads;
   static constexpr int kBars = 12;
   static constexpr int kBytes = kC + kU + kX + kH + kFloats * 4 + kBars * 8 + 16 + 1024;
   static constexpr int kSCols = 128 * MT * (MT + 1) / 2;
@@ -80,8 +88,9 @@ struct ScanHL {
   static constexpr uint32_t kAlloc = kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM columns exceeded");
   static_assert(kBytes <= 227 * 1024, "shared memory exceeded");
-  static_assert(kStage <= 128 * 128 * 2, "y staging must fit the first A2 block");
-  static constexpr int kThreads = 288;
+  // tile 0 is staged in the first A2 block, tile 1 in the second
+  static_assert(kStageTile <= 128 * 128 * 2, "y staging must fit an A2 block");
+  static constexpr int kThreads = kScanThreads;
 };
 
 enum : int {
@@ -95,30 +104,83 @@ __device__ __forceinline__ int scan_row(int s) {
   return 128 + 32 * (3 - ((s - 128) >> 5)) + (s & 31);
 }
 
+// Masked scores of one 32-column band kb of row tile mt for the calling warp's
+// 32 rows: A2 = bf16(L o S + D I) written into the swizzled A2 block.  Kept out
+// of line: one copy serves every band, which keeps the kernel's code small.
+template <int MT>
+__device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const float *cs2,
+                                            const float *cf, int q, int lane, int mt, int kb,
+                                            float Dh) {
+  const int r = 32 * q + lane;               // TMEM lane / A2 row
+  const int i = scan_row<MT>(128 * mt + r);  // chunk row
+  const int diag_band = i >> 5;              // uniform over the warp
+  uint8_t *blk = Bt + 128 * 128 * 2 * (mt * (mt + 1) / 2) + (kb >> 1) * (128 * 128);
+  const int col0 = (kb & 1) * 32;
+  uint32_t pk[16];
+  if (kb > diag_band) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+  } else {
+    float v[32];
+    tmem_ld32(tlane + 128 * mt * (mt + 1) / 2 + 32 * kb, v);
+    const float ci = cs2[i];
+    const float4 *c4 = reinterpret_cast<const float4 *>((kb < diag_band ? cf : cs2) + 32 * kb);
+    if (kb < diag_band) {
+      const float rf = ex2_approx(ci - cs2[32 * kb + 31]);
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = c4[e >> 2];
+        pk[e >> 1] = pack_bf16x2(v[e] * rf * f.x, v[e + 1] * rf * f.y);
+        pk[(e >> 1) + 1] = pack_bf16x2(v[e + 2] * rf * f.z, v[e + 3] * rf * f.w);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = c4[e >> 2];
+        const int j = 32 * kb + e;
+        float l0 = j <= i ? v[e] * ex2_approx(ci - f.x) : 0.f;
+        float l1 = j + 1 <= i ? v[e + 1] * ex2_approx(ci - f.y) : 0.f;
+        float l2 = j + 2 <= i ? v[e + 2] * ex2_approx(ci - f.z) : 0.f;
+        float l3 = j + 3 <= i ? v[e + 3] * ex2_approx(ci - f.w) : 0.f;
+        if (j == i) l0 += Dh;
+        if (j + 1 == i) l1 += Dh;
+        if (j + 2 == i) l2 += Dh;
+        if (j + 3 == i) l3 += Dh;
+        pk[e >> 1] = pack_bf16x2(l0, l1);
+        pk[(e >> 1) + 1] = pack_bf16x2(l2, l3);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    *reinterpret_cast<uint4 *>(blk + sw128_offset(r, col0 + 8 * e)) =
+        make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+}
+
 template <int Q, int P>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_hl(const __grid_constant__ CUtensorMap mapC32, const __grid_constant__ CUtensorMap mapB,
                   const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapH,
-                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                  const __grid_constant__ CUtensorMap mapY128, const float *__restrict__ dt,
                   const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
                   int GB, int GC, int nc, int heads_per_cta, int softplus) {
   using L = ScanHL<Q, P>;
-  constexpr int N = L::N, MT = L::MT;
+  constexpr int N = L::N, MT = L::MT, KMAX = L::kMaxHeads;
+  constexpr int CW = kScanComputeWarps;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *Ct = smem;
-  uint8_t *Bt = Ct + L::kC;  // B tile, then the A2 blocks; y staging in the first A2 block
+  uint8_t *Bt = Ct + L::kC;  // B tile, then the A2 blocks (and the y staging)
   uint8_t *Xt = Bt + L::kU;
   uint8_t *Ht = Xt + L::kX;
   float *cs2 = reinterpret_cast<float *>(Ht + L::kH);  // cs * log2(e)
   float *ecs = cs2 + Q;                                // exp(cs)
   float *cf = ecs + Q;                                 // exp(cs_{j|31} - cs_j)
   float *wsum = cf + Q;                                // per-warp scan totals
-  float *A_s = wsum + 16;                              // A of this CTA's heads
-  float *D_s = A_s + L::kMaxHeads;                     // D of this CTA's heads
-  float *dt_s = D_s + L::kMaxHeads;                    // raw dt [Q][kMaxHeads]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(dt_s + Q * L::kMaxHeads);
+  float *D_s = wsum + 32;                              // D of this CTA's heads
+  float *dA_s = D_s + KMAX;                            // softplus(dt) * A  [Q][KMAX]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(dA_s + Q * KMAX);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
@@ -135,23 +197,24 @@ __global__ void __launch_bounds__(288, 1)
   if (tid == 0) {
     for (int i = 0; i < L::kBars; ++i) {
       const bool per_warp = i == kBarA2a || i == kBarA2b || i == kBarYFree;
-      mbar_init(&bars[i], per_warp ? 8 : 1);
+      mbar_init(&bars[i], per_warp ? CW : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) tmem_alloc(tslot, L::kAlloc);
-  if (warp < 8) {
-    // this CTA's per-head scalars and its chunk of dt, staged once
-    if (tid < nh) {
-      A_s[tid] = A[h_begin + tid];
-      D_s[tid] = D ? D[h_begin + tid] : 0.f;
-    }
+  if (warp == CW) tmem_alloc(tslot, L::kAlloc);
+  if (warp < CW) {
+    // this CTA's D and softplus(dt) * A for its heads and chunk, staged once
+    if (tid < nh) D_s[tid] = D ? D[h_begin + tid] : 0.f;
     const int64_t t_row0 = static_cast<int64_t>(c) * Q;
-    for (int idx = tid; idx < Q * nh; idx += 256) {
-      const int t = idx / nh, hh = idx % nh;
-      dt_s[t * L::kMaxHeads + hh] =
-          t_row0 + t < T ? dt[(static_cast<int64_t>(b) * T + t_row0 + t) * H + h_begin + hh] : 0.f;
+    for (int idx = tid; idx < Q * nh; idx += 32 * CW) {
+      const int t = idx / nh, k = idx % nh;
+      float v = 0.f;
+      if (t_row0 + t < T) {
+        const float z = dt[(static_cast<int64_t>(b) * T + t_row0 + t) * H + h_begin + k];
+        v = (softplus ? softplus_f32(z) : z) * A[h_begin + k];
+      }
+      dA_s[t * KMAX + k] = v;
     }
   }
   tc_fence_before_sync();
@@ -159,7 +222,7 @@ __global__ void __launch_bounds__(288, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  if (warp == 8) {
+  if (warp == CW) {
     // ================================================================ control
     if (lane == 0) {
       prefetch_tensormap(&mapC32);
@@ -195,7 +258,7 @@ __global__ void __launch_bounds__(288, 1)
         }
         if (new_group_at(k)) {
           ++group;
-          // the previous head's y store must have left the staging area (B/A2 region)
+          // the previous head's y stores must have left the B/A2 region
           if (k > 0 && !mbar_wait(&bars[kBarStore], (k - 1) & 1, abort_flag)) break;
           mbar_arrive_expect_tx(&bars[kBarCB], L::kC + L::kB);
 #pragma unroll
@@ -263,16 +326,11 @@ __global__ void __launch_bounds__(288, 1)
     __syncwarp();
   } else {
     // ================================================================ compute
-    const int q = warp & 3, hf = warp >> 2;
+    const int q = warp & 3, hs = warp >> 2;  // TMEM lane quarter, sub-warp of the quarter
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    const int64_t t_row0 = static_cast<int64_t>(c) * Q;
-    // in-chunk inclusive cumsum of softplus(dt) * A_h -> cs2, ecs, cf (k = head index)
+    // in-chunk inclusive cumsum of dA for head index k -> cs2, ecs, cf
     auto cumsum = [&](int k) {
-      float v = 0.f;
-      if (tid < Q && t_row0 + tid < T) {
-        const float z = dt_s[tid * L::kMaxHeads + k];
-        v = (softplus ? softplus_f32(z) : z) * A_s[k];
-      }
+      float v = tid < Q ? dA_s[tid * KMAX + k] : 0.f;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_up_sync(0xffffffffu, v, off);
@@ -280,10 +338,10 @@ __global__ void __launch_bounds__(288, 1)
       }
       if (lane == 31) wsum[warp] = v;
       compute_sync();
-      float base = 0.f;
-      for (int w = 0; w < warp; ++w) base += wsum[w];
-      v += base;
       if (tid < Q) {
+        float base = 0.f;
+        for (int w = 0; w < warp; ++w) base += wsum[w];
+        v += base;
         cs2[tid] = v * kLog2e;
         ecs[tid] = ex2_approx(v * kLog2e);
       }
@@ -291,6 +349,13 @@ __global__ void __launch_bounds__(288, 1)
       if (tid < Q) cf[tid] = ex2_approx(cs2[tid | 31] - cs2[tid]);
       compute_sync();
     };
+    auto mask_band = [&](int mt, int kb, float Dh) {
+      scan_mask_band<MT>(Bt, tmem + lane_base, cs2, cf, q, lane, mt, kb, Dh);
+    };
+    constexpr int CPW = P / 4;  // Y columns per warp of a quarter
+    // y staging of row tile mt: the first A2 block for tile 0, the second for tile 1
+    auto stage_of = [&](int mt) { return Bt + 128 * 128 * 2 * (mt * (mt + 1) / 2); };
+
     cumsum(0);
     int group = -1;
     for (int k = 0; k < nh; ++k) {
@@ -298,10 +363,19 @@ __global__ void __launch_bounds__(288, 1)
       const bool more = k + 1 < nh;
       const bool new_group = new_group_at(k);
       if (new_group) ++group;
-      if (k > 0) {  // the previous head's y store has left the staging area
+      // The previous head's y stores must have read their staging before the
+      // A2 blocks are rewritten.  kBarStore is arrived once per head k >= 1
+      // when both have; a new group (whose B tile overwrites the whole region)
+      // waits for that before its C B^T product.
+      const bool full_wait = MT == 1 || new_group;
+      if (k > 0) {
         if (tid == 0) {
-          bulk_wait_read0();
-          mbar_arrive(&bars[kBarStore]);
+          if (full_wait) {
+            bulk_wait_read0();
+            mbar_arrive(&bars[kBarStore]);
+          } else {
+            bulk_wait_read1();  // tile 0's staging only
+          }
         }
         compute_sync();
       }
@@ -309,64 +383,7 @@ __global__ void __launch_bounds__(288, 1)
       const bool ok = __all_sync(0xffffffffu, ok_s) && !*abort_flag;
       tc_fence_after_sync();
       const float Dh = D_s[k];
-
-      // ---- mask of row tile mt: A2_mt = bf16(L o S_mt + D I)
-      auto mask_tile = [&](int mt) {
-        const int r = 32 * q + lane;             // TMEM lane / A2 row
-        const int i = scan_row<MT>(128 * mt + r);  // chunk row
-        const float ci = cs2[i];
-        const int diag_band = i >> 5;            // uniform over the warp
-        uint8_t *a2 = Bt + 128 * 128 * 2 * (mt * (mt + 1) / 2);
-        const uint32_t scol = 128 * mt * (mt + 1) / 2;
-        const int nb = 4 * (mt + 1);
-        // this warp's bands: hf, hf + 2, ...; those at or below the diagonal are
-        // loaded two at a time
-#pragma unroll
-        for (int kb0 = hf; kb0 < nb; kb0 += 4) {
-          const int kb1 = kb0 + 2;
-          const bool z0 = kb0 > diag_band, z1 = kb1 >= nb || kb1 > diag_band;
-          float v[64];
-          if (!z0 && !z1) {
-            tmem_ld32x2(tmem + lane_base + scol + 32 * kb0, tmem + lane_base + scol + 32 * kb1, v);
-          } else if (!z0) {
-            tmem_ld32(tmem + lane_base + scol + 32 * kb0, *reinterpret_cast<float(*)[32]>(v));
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int kb = half ? kb1 : kb0;
-            if (kb >= nb) continue;
-            const float *vv = v + 32 * half;
-            uint32_t pk[16];
-            if (kb > diag_band) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            } else if (kb < diag_band) {
-              const float rf = ex2_approx(ci - cs2[32 * kb + 31]);
-#pragma unroll
-              for (int e = 0; e < 32; e += 2)
-                pk[e >> 1] = pack_bf16x2(vv[e] * rf * cf[32 * kb + e], vv[e + 1] * rf * cf[32 * kb + e + 1]);
-            } else {
-              float l[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int j = 32 * kb + e;
-                l[e] = j <= i ? vv[e] * ex2_approx(ci - cs2[j]) : 0.f;
-                if (j == i) l[e] += Dh;
-              }
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(l[e], l[e + 1]);
-            }
-            uint8_t *blk = a2 + (kb >> 1) * (128 * 128);
-            const int col0 = (kb & 1) * 32;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4 *>(blk + sw128_offset(r, col0 + 8 * e)) =
-                  make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
-        }
-      };
-
-      if (ok) mask_tile(0);
+      if (ok) mask_band(0, hs, Dh);
       // ---- Y *= exp(cs_i) once MMA3 (Y = C Hin) is done
       bool ok3 = ok && mbar_wait(&bars[kBarM3], k & 1, abort_flag);
       ok3 = __all_sync(0xffffffffu, ok3);
@@ -375,9 +392,9 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const float e_i = ecs[scan_row<MT>(128 * mt + 32 * q + lane)];
-          const uint32_t dcol = L::kSCols + mt * P;
+          const uint32_t dcol = L::kSCols + mt * P + CPW * hs;
 #pragma unroll
-          for (int cc = hf * (P / 2); cc < (hf + 1) * (P / 2); cc += 16) {
+          for (int cc = 0; cc < CPW; cc += 16) {
             float v[16];
             tmem_ld16(tmem + lane_base + dcol + cc, v);
 #pragma unroll
@@ -392,35 +409,44 @@ __global__ void __launch_bounds__(288, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[MT == 2 ? kBarA2a : kBarA2b]);
       if (MT == 2) {
-        if (ok3) mask_tile(1);
+        if (k > 0 && !full_wait) {  // the previous head's tile-1 store has read its staging
+          if (tid == 0) {
+            bulk_wait_read0();
+            mbar_arrive(&bars[kBarStore]);
+          }
+          compute_sync();
+        }
+        if (ok3) {
+          mask_band(1, hs, Dh);
+          mask_band(1, hs + 4, Dh);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarA2b]);
       }
       // ---- next head's cumsum overlaps the last MMA2
       if (more) cumsum(k + 1);
-      // ---- output: Y -> bf16 -> staging (first A2 block) per row tile
-      uint8_t *stage = Bt;
+      // ---- output: Y -> bf16 -> staging per row tile, then TMA stores
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         bool ok2 = ok3 && mbar_wait(mt + 1 < MT ? &bars[kBarM2a] : &bars[kBarM2b], k & 1, abort_flag);
         ok2 = __all_sync(0xffffffffu, ok2);
         tc_fence_after_sync();
         if (!ok2) continue;
-        const int i = scan_row<MT>(128 * mt + 32 * q + lane);
-        const uint32_t dcol = L::kSCols + mt * P;
-        float v[64];
-        if (P / 2 == 64) {
-          tmem_ld32x2(tmem + lane_base + dcol + hf * 64, tmem + lane_base + dcol + hf * 64 + 32, v);
-        } else {
-          tmem_ld32(tmem + lane_base + dcol + hf * 32, *reinterpret_cast<float(*)[32]>(v));
-        }
+        const int r = 32 * q + lane;
+        const int row = scan_row<MT>(128 * mt + r) - 128 * mt;  // row within the tile
+        uint8_t *stage = stage_of(mt);
 #pragma unroll
-        for (int e = 0; e < P / 2; e += 8) {
-          const int col = hf * (P / 2) + e;
-          *reinterpret_cast<uint4 *>(stage + (col >> 6) * Q * 128 + sw128_offset(i, col & 63)) =
-              make_uint4(pack_bf16x2(v[e], v[e + 1]), pack_bf16x2(v[e + 2], v[e + 3]),
-                         pack_bf16x2(v[e + 4], v[e + 5]), pack_bf16x2(v[e + 6], v[e + 7]));
+        for (int cc = 0; cc < CPW; cc += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_base + L::kSCols + mt * P + CPW * hs + cc, v);
+          const int col = CPW * hs + cc;
+#pragma unroll
+          for (int e = 0; e < 16; e += 8)
+            *reinterpret_cast<uint4 *>(stage + ((col + e) >> 6) * (128 * 128) +
+                                       sw128_offset(row, (col + e) & 63)) =
+                make_uint4(pack_bf16x2(v[e], v[e + 1]), pack_bf16x2(v[e + 2], v[e + 3]),
+                           pack_bf16x2(v[e + 4], v[e + 5]), pack_bf16x2(v[e + 6], v[e + 7]));
         }
       }
       tc_fence_before_sync();
@@ -430,15 +456,19 @@ __global__ void __launch_bounds__(288, 1)
       compute_sync();
       if (tid == 0 && !*abort_flag) {
 #pragma unroll
-        for (int s = 0; s < P / 64; ++s) tma_store_4d(&mapY, stage + s * Q * 128, 64 * s, h, c * Q, b);
-        bulk_commit();
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int s = 0; s < P / 64; ++s)
+            tma_store_4d(&mapY128, stage_of(mt) + s * (128 * 128), 64 * s, h, c * Q + 128 * mt, b);
+          bulk_commit();
+        }
       }
     }
     if (tid == 0) bulk_wait_all();
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 8) tmem_dealloc(tmem, L::kAlloc);
+  if (warp == CW) tmem_dealloc(tmem, L::kAlloc);
 }
 
 }  // namespace ssd
