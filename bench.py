@@ -40,6 +40,35 @@ UNIT = "Mtok·heads/s"
 L2_BYTES = 126 * 1024 * 1024
 
 
+# DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) of
+# the dominant kernels, with the sha1 of the kernel's source at capture time;
+# the summaries are in profiles/.  A changed source reports null.
+MEASURED_TRAFFIC = {
+    ("chunk_scan_hl", "mamba2_2p7b"):
+        (402_307_840, "state_space_model_09_b300/csrc/ssd_scan.cuh",
+         "6996da878264a60752719f0e7e274250cb8cbcf9"),
+    ("chunk_state_pass_tc", "mamba2_2p7b"):
+        (269_110_016, "state_space_model_09_b300/csrc/ssd_state.cuh",
+         "29ed2098fdf5e3ddfaf3a3e895d752697edba400"),
+    ("multistep_kernel", "multistep_k8"):
+        (71_916_800, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
+         "85902be059783d58d40ec7e108370cad7b25bc17"),
+}
+
+
+def measured_traffic(kernel: str, workload: str):
+    import hashlib
+    ent = MEASURED_TRAFFIC.get((kernel, workload))
+    if not ent:
+        return None
+    nbytes, src, sha = ent
+    try:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            return nbytes if hashlib.sha1(f.read()).hexdigest() == sha else None
+    except OSError:
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -351,7 +380,7 @@ def run_ours(args, shape, work, world, rank, local):
         roof = {"bound": "hbm", "achieved": round(dom_bytes / dom_s / 1e9, 1), "peak": pk["hbm"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(names[dom], args.workload)
     roof["kernel"] = names[dom]
     roof["algorithmic_bytes"] = dom_bytes
     roof["algorithmic_flops"] = dom_flops
@@ -468,7 +497,9 @@ def run_multistep(args, world, rank, local):
                    "chain": steps, "graph": True,
                    "l2": "states 3 x 42 MB per step (h_cache, h_j, h_K) ~ L2 size; no flush"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm"], 4), "traffic": None, "kernel": "multistep_kernel",
+                     "frac": round(gbs / pk["hbm"], 4),
+                     "traffic": measured_traffic("multistep_kernel", "multistep_k8"),
+                     "kernel": "multistep_kernel",
                      "algorithmic_bytes": work["bytes"], "peak_source": pk["source"] + " (burst)"},
         "gpu_launches": reps * steps,
         "clocks": clk,
