@@ -340,7 +340,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     if (!encode_btgw(&mX, x, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
         !encode_btgw(&mB, B, pl.b, pl.T, pl.GB, pl.N, pl.Q) ||
         !encode_btgw(&mC32, C, pl.b, pl.T, pl.GC, pl.N, 32) ||
-        !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, 128) ||
+        !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
         !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
       return SSD_ERR_CUDA;
     record(events, 0, s);

@@ -15,7 +15,7 @@
 //   mask:  A2 = bf16(L o S + D I)           (TMEM -> registers -> swizzled smem)
 //   scale: Y *= exp(cs_i) row by row        (tcgen05.ld / tcgen05.st)
 //   MMA2:  Y += A2 x                        (K = causal columns)
-//   out:   y = bf16(Y), staged in smem, written by TMA tile stores
+//   out:   y = bf16(Y), staged in the (then dead) x tile, written by TMA tile stores
 // L is never formed in memory.  It is factorised per 32-column band: for a row
 // i below band k (reference column r_k = 32k + 31),
 //   L[i,j] = exp(cs_i - cs_rk) * exp(cs_rk - cs_j),
@@ -29,8 +29,9 @@
 // second: every quarter then has nine non-zero 32-column bands.
 //
 // Warp roles: warps 0-15 (512 threads; four per TMEM lane quarter) do the
-// cumsum, mask, scaling and output; warp 16 (one elected lane) issues every
-// TMA load and MMA.  Every wait is bounded in time.
+// mask, scaling and output; warp 16 (one elected lane) issues every TMA load
+// and MMA; warp 17 computes each head's in-chunk cumsum and decay tables one
+// head ahead into a double buffer.  Every wait is bounded in time.
 #pragma once
 
 #include "ssd_device.cuh"
@@ -63,7 +64,9 @@ __device__ __forceinline__ void bulk_wait_read1() {
 }
 
 constexpr int kScanComputeWarps = 16;
-constexpr int kScanThreads = 32 * (kScanComputeWarps + 1);
+constexpr int kScanControlWarp = kScanComputeWarps;      // TMA + MMA issue
+constexpr int kScanAuxWarp = kScanComputeWarps + 1;      // per-head decay tables
+constexpr int kScanThreads = 32 * (kScanComputeWarps + 2);
 // barrier among the compute threads only (warps 0-15)
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
@@ -77,25 +80,29 @@ struct ScanHL {
   static constexpr int kU = kB > kA2 ? kB : kA2;
   static constexpr int kX = P * Q * 2;
   static constexpr int kH = P * N * 2;
-  static constexpr int kStageTile = P * 128 * 2;  // y staging of one 128-row tile
-  static constexpr int kMaxHeads = 12;            // most heads per CTA
-  // cs*log2e, exp(cs), band factors, warp sums, D, softplus(dt)*A [Q][kMaxHeads]
-  static constexpr int kFloats = 3 * Q + 32 + kMaxHeads + Q * kMaxHeads;
-  static constexpr int kBars = 12;
+  static constexpr int kMaxHeads = 16;            // most heads per CTA
+  // per-head decay tables, double-buffered: cs*log2e, exp(cs), the factors
+  // 2^(a_{j|31} - a_j) and 2^(a_{j&~31} - a_j); plus D of the CTA's heads
+  static constexpr int kTables = 4;
+  static constexpr int kFloats = 2 * kTables * Q + kMaxHeads;
+  static constexpr int kBars = 16;
   static constexpr int kBytes = kC + kU + kX + kH + kFloats * 4 + kBars * 8 + 16 + 1024;
   static constexpr int kSCols = 128 * MT * (MT + 1) / 2;
   static constexpr int kCols = kSCols + MT * P;
   static constexpr uint32_t kAlloc = kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM columns exceeded");
   static_assert(kBytes <= 227 * 1024, "shared memory exceeded");
-  // tile 0 is staged in the first A2 block, tile 1 in the second
-  static_assert(kStageTile <= 128 * 128 * 2, "y staging must fit an A2 block");
   static constexpr int kThreads = kScanThreads;
 };
 
+// kBarM2: every MMA2 of the head done (x tile and A2 blocks free);
+// kBarYStaged: the compute warps wrote the head's bf16 y into the x tile;
+// kBarXFree: the head's y store has read the x tile (the next x may land).
 enum : int {
-  kBarCB = 0, kBarX, kBarH, kBarS, kBarM3, kBarM2a, kBarM2b, kBarA2a, kBarA2b, kBarYFree, kBarStore
+  kBarCB = 0, kBarX, kBarH, kBarS, kBarM3, kBarM2a, kBarM2, kBarA2a, kBarA2b, kBarYFree, kBarXFree,
+  kBarTabFull0, kBarTabFull1, kBarTabEmpty0, kBarTabEmpty1, kBarYStaged, kNumScanBars
 };
+static_assert(kNumScanBars <= ScanHL<128, 64>::kBars, "barrier slots");
 
 // Chunk row held by smem/TMEM row s of the C tile (see "Row order" above).
 template <int MT>
@@ -105,12 +112,19 @@ __device__ __forceinline__ int scan_row(int s) {
 }
 
 // Masked scores of one 32-column band kb of row tile mt for the calling warp's
-// 32 rows: A2 = bf16(L o S + D I) written into the swizzled A2 block.  Kept out
-// of line: one copy serves every band, which keeps the kernel's code small.
+// 32 rows: A2 = bf16(L o S + D I) written into the swizzled A2 block.  With
+// a = cs * log2(e) (non-increasing):
+//   band left of the row's band : L = 2^(a_i - a_ref) * 2^(a_ref - a_j), ref = band end
+//                                 (both factors <= 1);
+//   the row's own band          : L = 2^(a_i - a_r) * 2^(a_r - a_j), r = band start,
+//                                 when the band's range a_r - a_{r+31} < 100 (so the
+//                                 second factor cannot overflow); otherwise one
+//                                 exponential per element.
+// Kept out of line: one copy serves every band, which keeps the code small.
 template <int MT>
-__device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const float *cs2,
-                                            const float *cf, int q, int lane, int mt, int kb,
-                                            float Dh) {
+__device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const float *a,
+                                            const float *cf, const float *ce, int q, int lane,
+                                            int mt, int kb, float Dh) {
   const int r = 32 * q + lane;               // TMEM lane / A2 row
   const int i = scan_row<MT>(128 * mt + r);  // chunk row
   const int diag_band = i >> 5;              // uniform over the warp
@@ -123,25 +137,45 @@ __device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const f
   } else {
     float v[32];
     tmem_ld32(tlane + 128 * mt * (mt + 1) / 2 + 32 * kb, v);
-    const float ci = cs2[i];
-    const float4 *c4 = reinterpret_cast<const float4 *>((kb < diag_band ? cf : cs2) + 32 * kb);
+    const float ai = a[i];
+    const int j0 = 32 * kb;
     if (kb < diag_band) {
-      const float rf = ex2_approx(ci - cs2[32 * kb + 31]);
+      const float rf = ex2_approx(ai - a[j0 + 31]);
+      const float4 *c4 = reinterpret_cast<const float4 *>(cf + j0);
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         const float4 f = c4[e >> 2];
         pk[e >> 1] = pack_bf16x2(v[e] * rf * f.x, v[e + 1] * rf * f.y);
         pk[(e >> 1) + 1] = pack_bf16x2(v[e + 2] * rf * f.z, v[e + 3] * rf * f.w);
       }
-    } else {
+    } else if (a[j0] - a[j0 + 31] < 100.f) {
+      const float g = ex2_approx(ai - a[j0]);
+      const float4 *e4 = reinterpret_cast<const float4 *>(ce + j0);
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        const float4 f = c4[e >> 2];
-        const int j = 32 * kb + e;
-        float l0 = j <= i ? v[e] * ex2_approx(ci - f.x) : 0.f;
-        float l1 = j + 1 <= i ? v[e + 1] * ex2_approx(ci - f.y) : 0.f;
-        float l2 = j + 2 <= i ? v[e + 2] * ex2_approx(ci - f.z) : 0.f;
-        float l3 = j + 3 <= i ? v[e + 3] * ex2_approx(ci - f.w) : 0.f;
+        const float4 f = e4[e >> 2];
+        const int j = j0 + e;
+        float l0 = j <= i ? v[e] * g * f.x : 0.f;
+        float l1 = j + 1 <= i ? v[e + 1] * g * f.y : 0.f;
+        float l2 = j + 2 <= i ? v[e + 2] * g * f.z : 0.f;
+        float l3 = j + 3 <= i ? v[e + 3] * g * f.w : 0.f;
+        if (j == i) l0 += Dh;
+        if (j + 1 == i) l1 += Dh;
+        if (j + 2 == i) l2 += Dh;
+        if (j + 3 == i) l3 += Dh;
+        pk[e >> 1] = pack_bf16x2(l0, l1);
+        pk[(e >> 1) + 1] = pack_bf16x2(l2, l3);
+      }
+    } else {
+      const float4 *a4 = reinterpret_cast<const float4 *>(a + j0);
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = a4[e >> 2];
+        const int j = j0 + e;
+        float l0 = j <= i ? v[e] * ex2_approx(ai - f.x) : 0.f;
+        float l1 = j + 1 <= i ? v[e + 1] * ex2_approx(ai - f.y) : 0.f;
+        float l2 = j + 2 <= i ? v[e + 2] * ex2_approx(ai - f.z) : 0.f;
+        float l3 = j + 3 <= i ? v[e + 3] * ex2_approx(ai - f.w) : 0.f;
         if (j == i) l0 += Dh;
         if (j + 1 == i) l1 += Dh;
         if (j + 2 == i) l2 += Dh;
@@ -161,7 +195,7 @@ template <int Q, int P>
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_hl(const __grid_constant__ CUtensorMap mapC32, const __grid_constant__ CUtensorMap mapB,
                   const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapH,
-                  const __grid_constant__ CUtensorMap mapY128, const float *__restrict__ dt,
+                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
                   const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
                   int GB, int GC, int nc, int heads_per_cta, int softplus) {
   using L = ScanHL<Q, P>;
@@ -174,13 +208,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   uint8_t *Bt = Ct + L::kC;  // B tile, then the A2 blocks (and the y staging)
   uint8_t *Xt = Bt + L::kU;
   uint8_t *Ht = Xt + L::kX;
-  float *cs2 = reinterpret_cast<float *>(Ht + L::kH);  // cs * log2(e)
-  float *ecs = cs2 + Q;                                // exp(cs)
-  float *cf = ecs + Q;                                 // exp(cs_{j|31} - cs_j)
-  float *wsum = cf + Q;                                // per-warp scan totals
-  float *D_s = wsum + 32;                              // D of this CTA's heads
-  float *dA_s = D_s + KMAX;                            // softplus(dt) * A  [Q][KMAX]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(dA_s + Q * KMAX);
+  // tables[buf][t][Q]: t = 0 a = cs*log2(e), 1 exp(cs), 2 2^(a_{j|31}-a_j), 3 2^(a_{j&~31}-a_j)
+  float *tables = reinterpret_cast<float *>(Ht + L::kH);
+  float *D_s = tables + 2 * L::kTables * Q;            // D of this CTA's heads
+  uint64_t *bars = reinterpret_cast<uint64_t *>(D_s + KMAX);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
@@ -196,33 +227,89 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < L::kBars; ++i) {
-      const bool per_warp = i == kBarA2a || i == kBarA2b || i == kBarYFree;
+      const bool per_warp = i == kBarA2a || i == kBarA2b || i == kBarYFree ||
+                            i == kBarTabEmpty0 || i == kBarTabEmpty1 || i == kBarYStaged;
       mbar_init(&bars[i], per_warp ? CW : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == CW) tmem_alloc(tslot, L::kAlloc);
-  if (warp < CW) {
-    // this CTA's D and softplus(dt) * A for its heads and chunk, staged once
-    if (tid < nh) D_s[tid] = D ? D[h_begin + tid] : 0.f;
-    const int64_t t_row0 = static_cast<int64_t>(c) * Q;
-    for (int idx = tid; idx < Q * nh; idx += 32 * CW) {
-      const int t = idx / nh, k = idx % nh;
-      float v = 0.f;
-      if (t_row0 + t < T) {
-        const float z = dt[(static_cast<int64_t>(b) * T + t_row0 + t) * H + h_begin + k];
-        v = (softplus ? softplus_f32(z) : z) * A[h_begin + k];
-      }
-      dA_s[t * KMAX + k] = v;
-    }
-  }
+  if (warp == kScanControlWarp) tmem_alloc(tslot, L::kAlloc);
+  if (tid < nh) D_s[tid] = D ? D[h_begin + tid] : 0.f;
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  if (warp == CW) {
+  if (warp == kScanAuxWarp) {
+    // ================================================================ aux
+    // Decay tables of head k into buffer k & 1, one head ahead of the compute
+    // warps: lane owns Q/32 consecutive tokens; running sum, then a warp scan.
+    // It also writes each head's y: once the compute warps have staged it in
+    // the x tile, one TMA store per 64 columns, and it frees the x tile for
+    // the next head as soon as the store has read it.
+    constexpr int PER = Q / 32;
+    const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
+    for (int k = 0; k <= nh; ++k) {
+      if (k < nh) {
+        const int h = h_begin + k, s = k & 1;
+        float z[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          z[e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
+        const float Ah = A[h];
+        if (k >= 2 && !mbar_wait(&bars[kBarTabEmpty0 + s], ((k - 2) >> 1) & 1, abort_flag)) break;
+        float v[PER];
+        float run = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          if (t0 + e < T) run += (softplus ? softplus_f32(z[e]) : z[e]) * Ah;
+          v[e] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        const float base = incl - run;
+        float *ta = tables + s * L::kTables * Q;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          const float av = (v[e] + base) * kLog2e;
+          ta[lane * PER + e] = av;
+          ta[Q + lane * PER + e] = ex2_approx(av);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          const int j = lane * PER + e;
+          const float av = ta[j];
+          ta[2 * Q + j] = ex2_approx(ta[j | 31] - av);
+          ta[3 * Q + j] = ex2_approx(ta[j & ~31] - av);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarTabFull0 + s]);
+      }
+      if (k >= 1) {
+        const int kp = k - 1;
+        const bool ok = mbar_wait(&bars[kBarYStaged], kp & 1, abort_flag);
+        if (lane == 0) {
+          if (ok && !*abort_flag) {
+#pragma unroll
+            for (int s = 0; s < P / 64; ++s)
+              tma_store_4d(&mapY, Xt + s * Q * 128, 64 * s, h_begin + kp, c * Q, b);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          mbar_arrive(&bars[kBarXFree]);
+        }
+        __syncwarp();
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  } else if (warp == kScanControlWarp) {
     // ================================================================ control
     if (lane == 0) {
       prefetch_tensormap(&mapC32);
@@ -249,17 +336,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       for (int k = 0; k < nh && !*abort_flag; ++k) {
         const int h = h_begin + k;
         const bool more = k + 1 < nh;
-        if (more) {  // warm L2 with the next head's tiles
-#pragma unroll
-          for (int s = 0; s < P / 64; ++s) {
-            tma_prefetch_4d(&mapX, 64 * s, h + 1, c * Q, b);
-            tma_prefetch_3d(&mapH, 64 * s, 0, hrow + h + 1);
-          }
-        }
         if (new_group_at(k)) {
           ++group;
-          // the previous head's y stores must have left the B/A2 region
-          if (k > 0 && !mbar_wait(&bars[kBarStore], (k - 1) & 1, abort_flag)) break;
+          // every earlier reader of C, B/A2 and S has finished (MMA2 of k - 1 waited below)
           mbar_arrive_expect_tx(&bars[kBarCB], L::kC + L::kB);
 #pragma unroll
           for (int s = 0; s < N / 64; ++s) {
@@ -302,12 +381,16 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mma_commit(&bars[kBarM3]);
         if (!mbar_wait(&bars[kBarM3], k & 1, abort_flag)) break;
         if (more) load_h(h + 1);
-        // MMA2: Y_mt += A2_mt x, each row tile as soon as its A2 block is written
+        // MMA2: Y_mt += A2_mt x, the last row tile first (its mask is written first)
         if (!mbar_wait(&bars[kBarX], k & 1, abort_flag)) break;
+        bool failed = false;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const bool last = mt + 1 == MT;
-          if (!mbar_wait(&bars[last ? kBarA2b : kBarA2a], k & 1, abort_flag)) break;
+        for (int mi = 0; mi < MT; ++mi) {
+          const int mt = MT - 1 - mi;
+          if (!mbar_wait(&bars[mt == MT - 1 ? kBarA2b : kBarA2a], k & 1, abort_flag)) {
+            failed = true;
+            break;
+          }
           tc_fence_after_sync();
           const uint32_t a2 = bt + 128 * 128 * 2 * (mt * (mt + 1) / 2);
 #pragma unroll
@@ -316,11 +399,16 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mma_bf16(tmem + L::kSCols + mt * P, ad, sdesc_sw128(xt + ks * 2048, Q * 128, 1024),
                      idesc_y, 1u);
           }
-          mma_commit(&bars[last ? kBarM2b : kBarM2a]);
+          if (mi + 1 < MT) mma_commit(&bars[kBarM2a]);
         }
-        if (*abort_flag) break;
-        if (!mbar_wait(&bars[kBarM2b], k & 1, abort_flag)) break;
-        if (more) load_x(h + 1);
+        if (failed) break;
+        mma_commit(&bars[kBarM2]);
+        if (!mbar_wait(&bars[kBarM2], k & 1, abort_flag)) break;
+        // the x tile now holds this head's y until its store has read it
+        if (more) {
+          if (!mbar_wait(&bars[kBarXFree], k & 1, abort_flag)) break;
+          load_x(h + 1);
+        }
       }
     }
     __syncwarp();
@@ -328,62 +416,33 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // ================================================================ compute
     const int q = warp & 3, hs = warp >> 2;  // TMEM lane quarter, sub-warp of the quarter
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    // in-chunk inclusive cumsum of dA for head index k -> cs2, ecs, cf
-    auto cumsum = [&](int k) {
-      float v = tid < Q ? dA_s[tid * KMAX + k] : 0.f;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += o;
-      }
-      if (lane == 31) wsum[warp] = v;
-      compute_sync();
-      if (tid < Q) {
-        float base = 0.f;
-        for (int w = 0; w < warp; ++w) base += wsum[w];
-        v += base;
-        cs2[tid] = v * kLog2e;
-        ecs[tid] = ex2_approx(v * kLog2e);
-      }
-      compute_sync();
-      if (tid < Q) cf[tid] = ex2_approx(cs2[tid | 31] - cs2[tid]);
-      compute_sync();
-    };
+    float *a_tab = tables, *e_tab = tables + Q, *cf_tab = tables + 2 * Q, *ce_tab = tables + 3 * Q;
     auto mask_band = [&](int mt, int kb, float Dh) {
-      scan_mask_band<MT>(Bt, tmem + lane_base, cs2, cf, q, lane, mt, kb, Dh);
+      scan_mask_band<MT>(Bt, tmem + lane_base, a_tab, cf_tab, ce_tab, q, lane, mt, kb, Dh);
     };
     constexpr int CPW = P / 4;  // Y columns per warp of a quarter
-    // y staging of row tile mt: the first A2 block for tile 0, the second for tile 1
-    auto stage_of = [&](int mt) { return Bt + 128 * 128 * 2 * (mt * (mt + 1) / 2); };
 
-    cumsum(0);
     int group = -1;
     for (int k = 0; k < nh; ++k) {
       const int h = h_begin + k;
-      const bool more = k + 1 < nh;
+      const int tb = k & 1;  // this head's table buffer
+      a_tab = tables + tb * L::kTables * Q;
+      e_tab = a_tab + Q;
+      cf_tab = a_tab + 2 * Q;
+      ce_tab = a_tab + 3 * Q;
       const bool new_group = new_group_at(k);
       if (new_group) ++group;
-      // The previous head's y stores must have read their staging before the
-      // A2 blocks are rewritten.  kBarStore is arrived once per head k >= 1
-      // when both have; a new group (whose B tile overwrites the whole region)
-      // waits for that before its C B^T product.
-      const bool full_wait = MT == 1 || new_group;
-      if (k > 0) {
-        if (tid == 0) {
-          if (full_wait) {
-            bulk_wait_read0();
-            mbar_arrive(&bars[kBarStore]);
-          } else {
-            bulk_wait_read1();  // tile 0's staging only
-          }
-        }
-        compute_sync();
-      }
-      const bool ok_s = !new_group || mbar_wait(&bars[kBarS], group & 1, abort_flag);
+      bool ok_s = !new_group || mbar_wait(&bars[kBarS], group & 1, abort_flag);
+      ok_s = ok_s && mbar_wait(&bars[kBarTabFull0 + tb], (k >> 1) & 1, abort_flag);
       const bool ok = __all_sync(0xffffffffu, ok_s) && !*abort_flag;
       tc_fence_after_sync();
       const float Dh = D_s[k];
-      if (ok) mask_band(0, hs, Dh);
+      // ---- last row tile's mask first: its MMA2 then overlaps the other tile's mask
+      if (ok && MT == 2) {
+        mask_band(1, hs, Dh);
+        mask_band(1, hs + 4, Dh);
+      }
+      if (ok && MT == 1) mask_band(0, hs, Dh);
       // ---- Y *= exp(cs_i) once MMA3 (Y = C Hin) is done
       bool ok3 = ok && mbar_wait(&bars[kBarM3], k & 1, abort_flag);
       ok3 = __all_sync(0xffffffffu, ok3);
@@ -391,7 +450,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       if (ok3) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const float e_i = ecs[scan_row<MT>(128 * mt + 32 * q + lane)];
+          const float e_i = e_tab[scan_row<MT>(128 * mt + 32 * q + lane)];
           const uint32_t dcol = L::kSCols + mt * P + CPW * hs;
 #pragma unroll
           for (int cc = 0; cc < CPW; cc += 16) {
@@ -407,68 +466,50 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[MT == 2 ? kBarA2a : kBarA2b]);
+      if (lane == 0) mbar_arrive(&bars[kBarA2b]);
       if (MT == 2) {
-        if (k > 0 && !full_wait) {  // the previous head's tile-1 store has read its staging
-          if (tid == 0) {
-            bulk_wait_read0();
-            mbar_arrive(&bars[kBarStore]);
-          }
-          compute_sync();
-        }
-        if (ok3) {
-          mask_band(1, hs, Dh);
-          mask_band(1, hs + 4, Dh);
-        }
+        if (ok3) mask_band(0, hs, Dh);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kBarA2b]);
+        if (lane == 0) mbar_arrive(&bars[kBarA2a]);
       }
-      // ---- next head's cumsum overlaps the last MMA2
-      if (more) cumsum(k + 1);
-      // ---- output: Y -> bf16 -> staging per row tile, then TMA stores
+      // ---- this head's decay tables are no longer needed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarTabEmpty0 + tb]);
+      // ---- output: after every MMA2 (the x tile is then free), Y -> bf16 -> x tile
+      bool ok2 = ok3 && mbar_wait(&bars[kBarM2], k & 1, abort_flag);
+      ok2 = __all_sync(0xffffffffu, ok2);
+      tc_fence_after_sync();
+      if (ok2) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        bool ok2 = ok3 && mbar_wait(mt + 1 < MT ? &bars[kBarM2a] : &bars[kBarM2b], k & 1, abort_flag);
-        ok2 = __all_sync(0xffffffffu, ok2);
-        tc_fence_after_sync();
-        if (!ok2) continue;
-        const int r = 32 * q + lane;
-        const int row = scan_row<MT>(128 * mt + r) - 128 * mt;  // row within the tile
-        uint8_t *stage = stage_of(mt);
+        for (int mt = 0; mt < MT; ++mt) {
+          const int row = scan_row<MT>(128 * mt + 32 * q + lane);  // chunk row
 #pragma unroll
-        for (int cc = 0; cc < CPW; cc += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + L::kSCols + mt * P + CPW * hs + cc, v);
-          const int col = CPW * hs + cc;
+          for (int cc = 0; cc < CPW; cc += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + L::kSCols + mt * P + CPW * hs + cc, v);
+            const int col = CPW * hs + cc;
 #pragma unroll
-          for (int e = 0; e < 16; e += 8)
-            *reinterpret_cast<uint4 *>(stage + ((col + e) >> 6) * (128 * 128) +
-                                       sw128_offset(row, (col + e) & 63)) =
-                make_uint4(pack_bf16x2(v[e], v[e + 1]), pack_bf16x2(v[e + 2], v[e + 3]),
-                           pack_bf16x2(v[e + 4], v[e + 5]), pack_bf16x2(v[e + 6], v[e + 7]));
+            for (int e = 0; e < 16; e += 8)
+              *reinterpret_cast<uint4 *>(Xt + ((col + e) >> 6) * Q * 128 +
+                                         sw128_offset(row, (col + e) & 63)) =
+                  make_uint4(pack_bf16x2(v[e], v[e + 1]), pack_bf16x2(v[e + 2], v[e + 3]),
+                             pack_bf16x2(v[e + 4], v[e + 5]), pack_bf16x2(v[e + 6], v[e + 7]));
+          }
         }
       }
       tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarYFree]);
       fence_proxy_async_smem();
-      compute_sync();
-      if (tid == 0 && !*abort_flag) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-          for (int s = 0; s < P / 64; ++s)
-            tma_store_4d(&mapY128, stage_of(mt) + s * (128 * 128), 64 * s, h, c * Q + 128 * mt, b);
-          bulk_commit();
-        }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kBarYFree]);
+        mbar_arrive(&bars[kBarYStaged]);
       }
     }
-    if (tid == 0) bulk_wait_all();
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == CW) tmem_dealloc(tmem, L::kAlloc);
+  if (warp == kScanControlWarp) tmem_dealloc(tmem, L::kAlloc);
 }
 
 }  // namespace ssd
