@@ -281,7 +281,9 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
           if (i + PF < rows)
             buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(n + R * PF) * P));
           const int64_t off = base + static_cast<int64_t>(n) * P;
-          if (jb == 0) __stcs(reinterpret_cast<float4 *>(h_j + off), st);
+          // h_j with ordinary (L2-resident) stores: a speculative decode step
+          // usually continues from it, so the next call finds it in L2
+          if (jb == 0) *reinterpret_cast<float4 *>(h_j + off) = st;
 #pragma unroll
           for (int k = 0; k < KT; ++k) {
             if (k < K) {
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
               yp[k].y = fmaf(cn, st.y, yp[k].y);
               yp[k].z = fmaf(cn, st.z, yp[k].z);
               yp[k].w = fmaf(cn, st.w, yp[k].w);
-              if (k + 1 == jb) __stcs(reinterpret_cast<float4 *>(h_j + off), st);
+              if (k + 1 == jb) *reinterpret_cast<float4 *>(h_j + off) = st;
             }
           }
           __stcs(reinterpret_cast<float4 *>(h_K + off), st);
