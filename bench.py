@@ -51,8 +51,8 @@ MEASURED_TRAFFIC = {
         (269_513_728, "state_space_model_09_b300/csrc/ssd_state.cuh",
          "29ed2098fdf5e3ddfaf3a3e895d752697edba400"),
     ("multistep_kernel", "multistep_k8"):
-        (70_077_184, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
-         "ac940821858ca3b25e94b37f272887008939e39b"),
+        (70_245_120, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
+         "f575ddfdbe1e709db11955094bcca465e1547ba7"),
 }
 
 

@@ -232,12 +232,12 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   return launch_status();
 }
 
-template <typename IO, int KT>
+template <typename IO, int KT, int NC = 0, int PSC = 0>
 ssd_status launch_multistep(dim3 grid, int64_t smem, const ssd_dims *d, const void *x,
                             const float *dt, const float *A, const void *B, const void *C,
                             const float *D, const float *h_cache, const int32_t *j, void *y,
                             float *h_j, float *h_K, int PS, cudaStream_t s) {
-  auto k = ssd::multistep_kernel<IO, KT>;
+  auto k = ssd::multistep_kernel<IO, KT, NC, PSC>;
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [&] { ok = set_smem(k, 227 * 1024); });
@@ -501,7 +501,10 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
   if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid(static_cast<unsigned>((H + 1) / 2), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
-  if (bf16) {
+  if (bf16 && K <= 8 && N == 128 && PS == 64) {
+    // the decode shape of the Mamba-2 layers: compile-time N and column slice
+    st = launch_multistep<__nv_bfloat16, 8, 128, 64>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
+  } else if (bf16) {
     st = K <= 8 ? launch_multistep<__nv_bfloat16, 8>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
                 : launch_multistep<__nv_bfloat16, 16>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
   } else {

@@ -214,14 +214,19 @@ constexpr int kMsThreads = 128;
 constexpr int kMsItemThreads = 64;
 constexpr int kMsMaxK = 16;
 
-template <typename IO, int KT>
+// KT: compile-time bound on K (8 or 16), K <= KT.  NC / PSC: the state size N
+// and the column slice PS when fixed at compile time (0: taken from the
+// arguments); with both fixed every shared-memory index of the row loop is a
+// constant offset, which removes most of its integer work.
+template <typename IO, int KT, int NC = 0, int PSC = 0>
 __global__ void __launch_bounds__(128, 5) multistep_kernel(
     const IO *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const IO *__restrict__ Bm, const IO *__restrict__ Cm, const float *__restrict__ D,
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
-    float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N, int P,
-    int PS, int softplus) {
-  // KT: compile-time bound on K (8 or 16); K <= KT
+    float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N_arg,
+    int P, int PS_arg, int softplus) {
+  const int N = NC ? NC : N_arg;
+  const int PS = PSC ? PSC : PS_arg;
   extern __shared__ float sm_ms[];
   const int item = threadIdx.x / kMsItemThreads;  // 0 or 1
   const int h = 2 * blockIdx.x + item, b = blockIdx.y, p0 = blockIdx.z * PS;
