@@ -176,8 +176,9 @@ ssd_status launch_passing(const Plan &pl, const float *S, const float *cs, const
 template <typename IO>
 ssd_status launch_state_simt(const Plan &pl, const void *x, const void *B, const float *cs,
                              float *S, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(pl.H), pl.nc, static_cast<unsigned>(pl.b));
-  ssd::chunk_state_simt<IO><<<grid, 256, pl.Q * sizeof(float), s>>>(
+  const int64_t tiles = ((pl.N + 63) / 64) * ((pl.P + 63) / 64) * pl.nc;
+  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(pl.H), static_cast<unsigned>(pl.b));
+  ssd::chunk_state_simt<IO><<<grid, 256, 0, s>>>(
       static_cast<const IO *>(x), static_cast<const IO *>(B), cs, S, pl.T, static_cast<int>(pl.H),
       static_cast<int>(pl.GB), static_cast<int>(pl.N), static_cast<int>(pl.P), pl.Q, pl.nc);
   return launch_status();
@@ -187,13 +188,14 @@ template <typename IO, typename HT>
 ssd_status launch_scan_simt(const Plan &pl, const void *x, const void *B, const void *C,
                             const float *cs, const HT *Hin, const float *D, void *y,
                             cudaStream_t s) {
-  const int smem = static_cast<int>((pl.Q + 32 * pl.N + 32 * pl.Q) * sizeof(float));
+  const int smem = ssd::scan_simt_smem_floats(pl.Q, static_cast<int>(pl.N)) * 4;
   auto k = ssd::chunk_scan_simt<IO, HT>;
   static std::once_flag once;
   static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, 32 * (256 + 256) * 4 + 256 * 4); });
+  std::call_once(once, [&] { ok = set_smem(k, ssd::scan_simt_smem_floats(256, 256) * 4); });
   if (!ok) return SSD_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>(pl.H), pl.nc * ((pl.Q + 31) / 32), static_cast<unsigned>(pl.b));
+  const int64_t blocks = ((pl.Q + 31) / 32) * ((pl.P + 63) / 64) * pl.nc;
+  dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.H), static_cast<unsigned>(pl.b));
   k<<<grid, 256, smem, s>>>(static_cast<const IO *>(x), static_cast<const IO *>(B),
                             static_cast<const IO *>(C), cs, Hin, D, static_cast<IO *>(y), pl.T,
                             static_cast<int>(pl.H), static_cast<int>(pl.GB),

@@ -110,31 +110,68 @@ __global__ void __launch_bounds__(256) state_passing_kernel(
 // Chunk-final states from a zero initial state, on CUDA cores in float32
 // (Mamba-2 page, "SSD算法", the green step):
 //   S[b,c,h][n][p] = sum_j exp(cs_last - cs_j) B[cQ+j, n] x[cQ+j, p].
-// grid (H, nc, batch), 256 threads; dynamic smem: Q floats.
+// One block computes a 64 x 64 tile of S (rows n0.., columns p0..) of one
+// (batch, chunk, head); grid (ceil(N/64) * ceil(P/64) * nc, H, batch), 256
+// threads, each a 4 x 4 register tile.  Tokens go through shared memory 32 at
+// a time as float32: w_j B_j (the weight folded into B) and x_j.
 // ----------------------------------------------------------------------------
+constexpr int kSimtTok = 32;  // tokens per shared-memory block
+
 template <typename IO>
 __global__ void __launch_bounds__(256) chunk_state_simt(
     const IO *__restrict__ x, const IO *__restrict__ Bm, const float *__restrict__ cs,
     float *__restrict__ S, int64_t T, int H, int GB, int N, int P, int Q, int nc) {
-  extern __shared__ float w_s[];
-  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+  __shared__ float w_s[256];
+  __shared__ __align__(16) float Bw[kSimtTok][64];
+  __shared__ __align__(16) float Xs[kSimtTok][64];
+  const int tilesP = (P + 63) / 64, tilesN = (N + 63) / 64;
+  const int tile = blockIdx.x % (tilesN * tilesP), c = blockIdx.x / (tilesN * tilesP);
+  const int n0 = 64 * (tile / tilesP), p0 = 64 * (tile % tilesP);
+  const int h = blockIdx.y, b = blockIdx.z;
   const int gb = h / (H / GB);
+  const int tid = threadIdx.x, tn = tid >> 4, tp = tid & 15;
   const int64_t t0 = static_cast<int64_t>(c) * Q;
   const int L = static_cast<int>(T - t0 < Q ? T - t0 : static_cast<int64_t>(Q));
   const float *csc = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q;
   const float cl = csc[Q - 1];
-  for (int j = threadIdx.x; j < Q; j += blockDim.x) w_s[j] = j < L ? expf(cl - csc[j]) : 0.f;
-  __syncthreads();
-  float *Sc = S + ((static_cast<int64_t>(b) * nc + c) * H + h) * N * P;
-  for (int idx = threadIdx.x; idx < N * P; idx += blockDim.x) {
-    const int n = idx / P, p = idx % P;
-    float acc = 0.f;
-    for (int j = 0; j < L; ++j) {
+  for (int j = tid; j < Q; j += 256) w_s[j] = j < L ? expf(cl - csc[j]) : 0.f;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += kSimtTok) {
+    __syncthreads();  // w_s written; previous block consumed
+    for (int idx = tid; idx < kSimtTok * 64; idx += 256) {
+      const int jj = idx >> 6, cc = idx & 63, j = j0 + jj;
+      const bool in_t = j < L;
       const int64_t t = t0 + j;
-      acc = fmaf(w_s[j] * to_f32(Bm[((static_cast<int64_t>(b) * T + t) * GB + gb) * N + n]),
-                 to_f32(x[((static_cast<int64_t>(b) * T + t) * H + h) * P + p]), acc);
+      Bw[jj][cc] = in_t && n0 + cc < N
+                       ? w_s[j] * to_f32(Bm[((static_cast<int64_t>(b) * T + t) * GB + gb) * N + n0 + cc])
+                       : 0.f;
+      Xs[jj][cc] = in_t && p0 + cc < P
+                       ? to_f32(x[((static_cast<int64_t>(b) * T + t) * H + h) * P + p0 + cc])
+                       : 0.f;
     }
-    Sc[idx] = acc;
+    __syncthreads();
+#pragma unroll 4
+    for (int jj = 0; jj < kSimtTok; ++jj) {
+      const float4 bv = *reinterpret_cast<const float4 *>(&Bw[jj][4 * tn]);
+      const float4 xv = *reinterpret_cast<const float4 *>(&Xs[jj][4 * tp]);
+      const float bn[4] = {bv.x, bv.y, bv.z, bv.w}, xp[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = fmaf(bn[r], xp[e], acc[r][e]);
+    }
+  }
+  float *Sc = S + ((static_cast<int64_t>(b) * nc + c) * H + h) * N * P;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int n = n0 + 4 * tn + r, p = p0 + 4 * tp;
+    if (n < N && p < P)
+      *reinterpret_cast<float4 *>(Sc + static_cast<int64_t>(n) * P + p) =
+          make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
   }
 }
 
@@ -143,56 +180,119 @@ __global__ void __launch_bounds__(256) chunk_state_simt(
 // diagonal block in quadratic form plus the blue term from the chunk's true
 // initial state, and the D skip):
 //   y_i = sum_{j<=i} exp(cs_i - cs_j) (C_i . B_j) x_j + exp(cs_i) C_i^T Hin + D x_i
-// grid (H, nc * ceil(Q/32), batch): 32 rows of one chunk per block, 256 threads.
-// dynamic smem: cs[Q] + C rows [32][N] + masked scores [32][Q] (floats).
+// One block computes 32 rows i0.. x 64 columns p0.. of one (batch, chunk,
+// head); grid (ceil(Q/32) * ceil(P/64) * nc, H, batch), 256 threads, thread
+// (row ri, column group pg) owns 8 columns of one row.  Shared memory (floats):
+// cs[Q], C rows [32][Np] (zero-padded to Np = N rounded up to 32), then per
+// 32-token block the B rows [32][Np + 1] (odd stride: the score loop reads a
+// column of it across the lanes), the masked scores G[32][33] and x (or, for
+// the C Hin term, Hin rows) [32][64].
 // ----------------------------------------------------------------------------
+__host__ __device__ constexpr int scan_simt_smem_floats(int Q, int N) {
+  return Q + 32 * ((N + 31) / 32 * 32) + 32 * ((N + 31) / 32 * 32 + 1) + 32 * 33 + kSimtTok * 64;
+}
+
 template <typename IO, typename HT>
 __global__ void __launch_bounds__(256) chunk_scan_simt(
     const IO *__restrict__ x, const IO *__restrict__ Bm, const IO *__restrict__ Cm,
     const float *__restrict__ cs, const HT *__restrict__ Hin, const float *__restrict__ D,
     IO *__restrict__ y, int64_t T, int H, int GB, int GC, int N, int P, int Q, int nc) {
-  extern __shared__ float sm_f[];
-  float *csq = sm_f;
-  float *Ct = csq + Q;
-  float *G = Ct + 32 * N;
-  const int h = blockIdx.x, b = blockIdx.z;
-  const int tiles = (Q + 31) / 32;
-  const int c = blockIdx.y / tiles, i0 = (blockIdx.y % tiles) * 32;
+  extern __shared__ __align__(16) float sm_f[];
+  const int Np = (N + 31) / 32 * 32;
+  float *csq = sm_f;            // [Q]
+  float *Ct = csq + Q;          // [32][Np]
+  const int Bst = Np + 1;
+  float *Bs = Ct + 32 * Np;     // [32][Bst]
+  float *G = Bs + 32 * Bst;     // [32][33]
+  float *Ws = G + 32 * 33;      // [32][64]: x block or Hin block (offset a multiple of 4 floats)
+  const int rowT = (Q + 31) / 32, tilesP = (P + 63) / 64;
+  const int per_c = rowT * tilesP;
+  const int c = blockIdx.x / per_c, rem = blockIdx.x % per_c;
+  const int i0 = 32 * (rem / tilesP), p0 = 64 * (rem % tilesP);
+  const int h = blockIdx.y, b = blockIdx.z;
   const int gb = h / (H / GB), gc = h / (H / GC);
+  const int tid = threadIdx.x, ri = tid >> 3, pg = tid & 7;
+  const int i = i0 + ri;
   const int64_t t0 = static_cast<int64_t>(c) * Q;
   const int L = static_cast<int>(T - t0 < Q ? T - t0 : static_cast<int64_t>(Q));
   const float *csc = cs + ((static_cast<int64_t>(b) * H + h) * nc + c) * Q;
-  for (int j = threadIdx.x; j < Q; j += blockDim.x) csq[j] = csc[j];
-  for (int idx = threadIdx.x; idx < 32 * N; idx += blockDim.x) {
-    const int ii = idx / N, n = idx % N, i = i0 + ii;
-    Ct[idx] = i < L ? to_f32(Cm[((static_cast<int64_t>(b) * T + t0 + i) * GC + gc) * N + n]) : 0.f;
+  for (int j = tid; j < Q; j += 256) csq[j] = csc[j];
+  for (int idx = tid; idx < 32 * Np; idx += 256) {
+    const int ii = idx / Np, n = idx % Np;
+    Ct[idx] = i0 + ii < L && n < N
+                  ? to_f32(Cm[((static_cast<int64_t>(b) * T + t0 + i0 + ii) * GC + gc) * N + n])
+                  : 0.f;
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < 32 * Q; idx += blockDim.x) {
-    const int ii = idx / Q, j = idx % Q, i = i0 + ii;
-    float g = 0.f;
-    if (j <= i && i < L) {
-      const IO *Bj = Bm + ((static_cast<int64_t>(b) * T + t0 + j) * GB + gb) * N;
-      float dot = 0.f;
-      for (int n = 0; n < N; ++n) dot = fmaf(Ct[ii * N + n], to_f32(Bj[n]), dot);
-      g = dot * expf(csq[i] - csq[j]);
+  float accd[8], acco[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) accd[e] = acco[e] = 0.f;
+  auto accumulate = [&](const float *coef, int coef_stride, float (&acc)[8]) {
+    // acc[e] += sum_k coef[k] * Ws[k][8 pg + e], k over the 32-row block
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+      const float g = coef[k * coef_stride];
+      const float4 w0 = *reinterpret_cast<const float4 *>(&Ws[k * 64 + 8 * pg]);
+      const float4 w1 = *reinterpret_cast<const float4 *>(&Ws[k * 64 + 8 * pg + 4]);
+      acc[0] = fmaf(g, w0.x, acc[0]); acc[1] = fmaf(g, w0.y, acc[1]);
+      acc[2] = fmaf(g, w0.z, acc[2]); acc[3] = fmaf(g, w0.w, acc[3]);
+      acc[4] = fmaf(g, w1.x, acc[4]); acc[5] = fmaf(g, w1.y, acc[5]);
+      acc[6] = fmaf(g, w1.z, acc[6]); acc[7] = fmaf(g, w1.w, acc[7]);
     }
-    G[idx] = g;
-  }
-  __syncthreads();
-  const float Dh = D ? D[h] : 0.f;
+  };
+  // ---- C Hin, 32 state rows at a time
   const HT *Hc = Hin + ((static_cast<int64_t>(b) * nc + c) * H + h) * N * P;
-  for (int idx = threadIdx.x; idx < 32 * P; idx += blockDim.x) {
-    const int ii = idx / P, p = idx % P, i = i0 + ii;
-    if (i >= L) continue;
-    float acc = 0.f;
-    for (int j = 0; j <= i; ++j)
-      acc = fmaf(G[ii * Q + j], to_f32(x[((static_cast<int64_t>(b) * T + t0 + j) * H + h) * P + p]),
-                 acc);
-    float off = 0.f;
-    for (int n = 0; n < N; ++n) off = fmaf(Ct[ii * N + n], to_f32(Hc[n * P + p]), off);
-    const int64_t xo = ((static_cast<int64_t>(b) * T + t0 + i) * H + h) * P + p;
-    y[xo] = from_f32<IO>(acc + expf(csq[i]) * off + Dh * to_f32(x[xo]));
+  for (int nb = 0; nb < N; nb += 32) {
+    __syncthreads();
+    for (int idx = tid; idx < 32 * 64; idx += 256) {
+      const int k = idx >> 6, cc = idx & 63;
+      Ws[idx] = nb + k < N && p0 + cc < P ? to_f32(Hc[static_cast<int64_t>(nb + k) * P + p0 + cc]) : 0.f;
+    }
+    __syncthreads();
+    accumulate(Ct + ri * Np + nb, 1, acco);
+  }
+  // ---- diagonal block, 32 tokens at a time (causal: tokens j <= i0 + 31)
+  const int jmax = min(i0 + 32, L);
+  for (int j0 = 0; j0 < jmax; j0 += kSimtTok) {
+    __syncthreads();
+    for (int idx = tid; idx < 32 * Np; idx += 256) {
+      const int jj = idx / Np, n = idx % Np, j = j0 + jj;
+      Bs[jj * Bst + n] = j < L && n < N
+                    ? to_f32(Bm[((static_cast<int64_t>(b) * T + t0 + j) * GB + gb) * N + n])
+                    : 0.f;
+    }
+    for (int idx = tid; idx < 32 * 64; idx += 256) {
+      const int k = idx >> 6, cc = idx & 63, j = j0 + k;
+      Ws[idx] = j < L && p0 + cc < P
+                    ? to_f32(x[((static_cast<int64_t>(b) * T + t0 + j) * H + h) * P + p0 + cc])
+                    : 0.f;
+    }
+    __syncthreads();
+    // masked scores G[ii][jj] = exp(cs_i - cs_j) C_i . B_j for j <= i (4 per thread)
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int e = tid + 256 * q4, ii = e >> 5, jj = e & 31;
+      const int gi = i0 + ii, gj = j0 + jj;
+      float g = 0.f;
+      if (gj <= gi && gi < L && gj < L) {
+        float dot = 0.f;
+        for (int n = 0; n < N; ++n) dot = fmaf(Ct[ii * Np + n], Bs[jj * Bst + n], dot);
+        g = dot * expf(csq[gi] - csq[gj]);
+      }
+      G[ii * 33 + jj] = g;
+    }
+    __syncthreads();
+    accumulate(G + ri * 33, 1, accd);
+  }
+  // ---- y = diagonal + exp(cs_i) C Hin + D x
+  if (i < L) {
+    const float ei = expf(csq[i]);
+    const float Dh = D ? D[h] : 0.f;
+    const int64_t row = ((static_cast<int64_t>(b) * T + t0 + i) * H + h) * P;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int p = p0 + 8 * pg + e;
+      if (p < P) y[row + p] = from_f32<IO>(accd[e] + ei * acco[e] + Dh * to_f32(x[row + p]));
+    }
   }
 }
 
