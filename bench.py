@@ -108,6 +108,7 @@ def fwd_work(s: synth.FwdShape):
     stages = {
         "chunk_state_pass_tc": (x + Bb + dt + h0 + hin16 + st, f_state),
         "chunk_scan_hl": (x + Bb + Cb + dt + hin16 + x, f_scan),
+        "state_fixup": (2 * hin16 + st, 0),
         "dt_cumsum": (dt + cs, 0),
         "chunk_state_simt": (x + Bb + cs + S32, f_state),
         "state_passing": (S32 + b * H * nc * 4 + h0 + S32 + st, 2 * b * nc * H * N * P),

@@ -39,7 +39,27 @@ struct Plan {
   int Q, nc;
   bool bf16, softplus, tc;
   size_t cs_off, S_off, Hin_off, total;
+  // tensor-core path: sequence segments of the state pass (1: none) and the
+  // workspace of their hand-off (segment final states, decay products)
+  int nseg = 1, cps = 0;
+  size_t Fseg_off = 0, Lseg_off = 0, Dc_off = 0;
 };
+
+int num_sms();
+
+// Segments of the tensor-core state pass.  Its CTAs walk their chunks one after
+// another, two per SM; when the (batch, head, slice) items leave SM slots idle
+// the sequence is split so that every slot works on a segment of at least four
+// chunks.
+void plan_segments(Plan *pl) {
+  const int64_t items = pl->b * pl->H * (pl->P / 64);
+  const int64_t slots = 2 * static_cast<int64_t>(num_sms());
+  int64_t nseg = items >= slots ? 1 : slots / items;
+  nseg = std::min<int64_t>(nseg, pl->nc / 4);
+  nseg = std::max<int64_t>(nseg, 1);
+  pl->cps = static_cast<int>((pl->nc + nseg - 1) / nseg);
+  pl->nseg = (pl->nc + pl->cps - 1) / pl->cps;
+}
 
 bool valid_dim(int64_t v) { return v >= 1 && v <= (int64_t(1) << 31) - 1; }
 
@@ -81,10 +101,20 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
   if (pl->b * pl->nc * pl->H > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
   const size_t states = static_cast<size_t>(pl->b) * pl->nc * pl->H * pl->N * pl->P;
   if (pl->tc) {
-    // tensor-core path: only the chunk initial states (bf16) go through HBM
+    // tensor-core path: the chunk initial states (bf16) go through HBM, plus,
+    // for a segmented state pass, each segment's final state and decays
     pl->cs_off = pl->S_off = 0;
     pl->Hin_off = 0;
     pl->total = align_up(states * 2);
+    plan_segments(pl);
+    if (pl->nseg > 1) {
+      if (pl->b * pl->nseg > 65535) return SSD_ERR_UNSUPPORTED;
+      const size_t bh = static_cast<size_t>(pl->b) * pl->H;
+      pl->Fseg_off = pl->total;
+      pl->Lseg_off = pl->Fseg_off + align_up(bh * pl->nseg * pl->N * pl->P * sizeof(float));
+      pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
+      pl->total = pl->Dc_off + align_up(bh * pl->nc * sizeof(float));
+    }
   } else {
     pl->cs_off = 0;
     pl->S_off = align_up(static_cast<size_t>(pl->b) * pl->H * pl->nc * pl->Q * sizeof(float));
@@ -219,7 +249,8 @@ int num_sms() {
 template <int Q>
 ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
                              const float *dt, const float *A, const float *h0, __nv_bfloat16 *Hin,
-                             float *h_final, cudaStream_t s) {
+                             float *h_final, float *Fseg, float *Lseg, float *Dc,
+                             void *const *events, cudaStream_t s) {
   using L = ssd::StatePass<Q>;
   auto k = ssd::chunk_state_pass_tc<Q>;
   static std::once_flag once;
@@ -227,10 +258,18 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
   if (!ok) return SSD_ERR_CUDA;
   dim3 grid(static_cast<unsigned>(pl.P / L::PS), static_cast<unsigned>(pl.H),
-            static_cast<unsigned>(pl.b));
+            static_cast<unsigned>(pl.b * pl.nseg));
   k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
                                          static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
-                                         static_cast<int>(pl.P), pl.softplus);
+                                         static_cast<int>(pl.P), pl.softplus, pl.nseg, pl.cps,
+                                         Fseg, Lseg, Dc);
+  if (launch_status() != SSD_OK || pl.nseg == 1) return launch_status();
+  record(events, 1, s);
+  const int NP = static_cast<int>(pl.N * pl.P);
+  dim3 g2(static_cast<unsigned>((NP / 4 + 255) / 256), static_cast<unsigned>(pl.H),
+          static_cast<unsigned>(pl.b));
+  ssd::state_fixup_kernel<<<g2, 256, 0, s>>>(Fseg, Lseg, Dc, Hin, h_final,
+                                             static_cast<int>(pl.H), pl.nc, pl.cps, pl.nseg, NP);
   return launch_status();
 }
 
@@ -346,15 +385,19 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
         !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
       return SSD_ERR_CUDA;
     record(events, 0, s);
-    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s)
-                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, s);
+    float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
+    float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
+    float *Dc = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Dc_off) : nullptr;
+    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, events, s)
+                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, events, s);
     if (st != SSD_OK) return st;
-    record(events, 1, s);
+    const int se = pl.nseg > 1 ? 2 : 1;  // events index after the state stages
+    record(events, se, s);
     if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     if (st != SSD_OK) return st;
-    record(events, 2, s);
+    record(events, se + 1, s);
     return SSD_OK;
   }
 
@@ -376,6 +419,8 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
 }
 
 const char *const kStageNamesTc[] = {"chunk_state_pass_tc", "chunk_scan_hl"};
+const char *const kStageNamesTcSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hl"};
+int num_stages(const Plan &pl) { return pl.tc ? (pl.nseg > 1 ? 3 : 2) : 4; }
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
 
@@ -422,13 +467,14 @@ size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk) {
 int32_t ssd_fwd_num_stages(const ssd_dims *dims, int32_t chunk) {
   Plan pl;
   if (make_plan(dims, chunk, &pl) != SSD_OK) return 0;
-  return pl.tc ? 2 : 4;
+  return num_stages(pl);
 }
 
 const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
-  if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= (pl.tc ? 2 : 4)) return nullptr;
-  return pl.tc ? kStageNamesTc[i] : kStageNamesSimt[i];
+  if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= num_stages(pl)) return nullptr;
+  if (!pl.tc) return kStageNamesSimt[i];
+  return pl.nseg > 1 ? kStageNamesTcSeg[i] : kStageNamesTc[i];
 }
 
 ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,

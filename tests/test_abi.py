@@ -55,6 +55,12 @@ def test_stage_names_follow_the_path():
     assert S.ssd_fwd_stage_name(_dims(), 256, 2) is None
     assert S.ssd_fwd_num_stages(_dims(), 256) == 2
     assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
+    # one long sequence over 80 heads: the state pass is split into sequence
+    # segments, joined by a fix-up stage
+    long = _dims(batch=1, seqlen=16384)
+    assert [S.ssd_fwd_stage_name(long, 256, i) for i in range(S.ssd_fwd_num_stages(long, 256))] == \
+        ["chunk_state_pass_tc", "state_fixup", "chunk_scan_hl"]
+    assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
 
 
 @pytest.mark.parametrize("kw,chunk,status", [

@@ -100,6 +100,10 @@ SMALL = {
     "tc_q128_p64": (F(1, 384, 4, 64, 128, 1, 4, 128, synth.BF16, "all"), 24),
     "tc_T1": (F(1, 1, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 25),
     "tc_T_short": (F(2, 77, 2, 64, 128, 1, 2, 256, synth.BF16, "all"), 26),
+    # few (batch, head) pairs and many chunks: the state pass runs in sequence
+    # segments joined by state_fixup (ragged last chunk, random h0)
+    "tc_segments_q128": (F(1, 2000, 2, 64, 128, 1, 1, 128, synth.BF16, "all"), 27),
+    "tc_segments_q256": (F(1, 3000, 3, 64, 128, 1, 1, 256, synth.BF16, "all"), 28),
     # bf16 I/O outside the tensor-core envelope (float32 CUDA-core kernels)
     "bf16_q64_n64": (F(2, 160, 4, 64, 64, 1, 1, 64, synth.BF16, "all"), 31),
 }
