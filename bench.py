@@ -48,8 +48,8 @@ MEASURED_TRAFFIC = {
         (406_627_840, "state_space_model_09_b300/csrc/ssd_scan.cuh",
          "4fb9995bf87887d2f10a730a63c27b4c9c93ad75"),
     ("chunk_state_pass_tc", "mamba2_2p7b"):
-        (269_513_728, "state_space_model_09_b300/csrc/ssd_state.cuh",
-         "29ed2098fdf5e3ddfaf3a3e895d752697edba400"),
+        (269_728_768, "state_space_model_09_b300/csrc/ssd_state.cuh",
+         "03036be1fc4d80f9f3f82cc70eb68c769eafd0b1"),
     ("multistep_kernel", "multistep_k8"):
         (70_245_120, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
          "f575ddfdbe1e709db11955094bcca465e1547ba7"),

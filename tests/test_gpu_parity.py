@@ -167,6 +167,39 @@ def test_fwd_deterministic():
     assert torch.equal(y1, y2) and torch.equal(h1, h2)
 
 
+@pytest.mark.parametrize("shape,seed", [
+    (F(2, 700, 4, 64, 128, 1, 1, 256, synth.BF16, "all"), 53),     # two tensor-core kernels
+    (F(1, 2000, 2, 64, 128, 1, 1, 128, synth.BF16, "all"), 54),    # segmented state pass (3 kernels)
+    (F(1, 300, 4, 64, 64, 1, 1, 64, synth.F32, "all"), 55),        # float32 path (4 kernels)
+])
+def test_fwd_graph_replay_equals_eager(shape, seed):
+    """ssd_fwd captured in a CUDA graph and replayed twice gives the eager result
+    bit for bit: every step of the call is enqueued on the caller's stream."""
+    d = to_dev(synth.make_fwd_inputs(shape, seed), shape.io)
+    y_ref, h_ref = run_fwd(d, shape.chunk)
+    b, T, H, P = d["x"].shape
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    ws = S.workspace_for(dims, shape.chunk)
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((b, H, d["B"].shape[3], P), device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], shape.chunk, y, hf, ws,
+                  stream=stream)  # warm-up: one-time function attributes outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], shape.chunk, y, hf, ws,
+                  stream=stream)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        hf.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        S.ssd_check_device_error()
+        assert torch.equal(y, y_ref) and torch.equal(hf, h_ref)
+
+
 def test_fwd_profiled_events():
     shape = synth.WORKLOADS["tiny_f32"]
     d = to_dev(synth.make_fwd_inputs(shape, 1000), shape.io)
