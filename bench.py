@@ -422,6 +422,66 @@ def multistep_work(s: synth.MultistepShape):
                 tok_heads=s.batch * s.K * s.nheads)
 
 
+def run_sequential(args, shape, world, rank, local):
+    """Prefill of the workload through ssd_fwd_sequential (windows of
+    --window tokens chained through the state): one step = the whole
+    sequence.  Reports the same throughput metric and the device workspace,
+    which does not grow with the sequence length."""
+    import torch
+    from state_space_model_09_b300 import ssd as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload] + 17 * rank)
+    io_t = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
+    d = {}
+    for k, v in inp.items():
+        d[k] = None if v is None else (torch.from_numpy(v).to(io_t) if k in ("x", "B", "C")
+                                       else torch.from_numpy(v)).to(dev)
+    b, T, H, P = d["x"].shape
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((b, H, d["B"].shape[3], P), dtype=torch.float32, device=dev)
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    nbytes = S.ssd_fwd_sequential_workspace_size(dims, shape.chunk, args.window)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        S.ssd_fwd_sequential(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                             shape.chunk, args.window, y, hf, ws, True, stream, dims)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    S.ssd_check_device_error(stream)
+    clocks = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    S.ssd_check_device_error(stream)
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": "SSD sequential prefill Mtok·heads/s (windows chained through the state)",
+        "value": round(world * shape.tok_heads / (ms * 1e-3) / 1e6, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
+        "config": dict(config_of(args, shape, "gpu"), window=args.window,
+                       workspace_bytes=nbytes,
+                       whole_call_workspace_bytes=S.ssd_fwd_workspace_size(dims, shape.chunk)),
+        "clocks": clk}), flush=True)
+
+
 def run_multistep(args, world, rank, local):
     """One step = one ssd_multistep call of the speculative chain (each step
     continues from h_j).  The chain of `shape.steps` calls is captured in a
@@ -516,6 +576,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mamba2_2p7b", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="prefill through ssd_fwd_sequential with windows of this many tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -536,6 +598,9 @@ def main():
             run_reference(args, shape, work)
         return
     world, rank, local = dist_setup()
+    if args.window > 0:
+        run_sequential(args, shape, world, rank, local)
+        return
     run_ours(args, shape, work, world, rank, local)
 
 

@@ -82,9 +82,9 @@ typedef struct ssd_dims {
 
 /* Bytes of device workspace ssd_fwd needs for these dims and chunk length
  * (chunk in {64, 128, 256}).  Returns 0 for arguments ssd_fwd would reject.
- * The workspace holds the in-chunk cumulative decays [b, H, nc, Q], the
- * chunk-final states and the chunk initial states [b, nc, H, N, P]
- * (nc = ceil(T / Q)). */
+ * The workspace holds the chunk initial states [b, nc, H, N, P]
+ * (nc = ceil(T / Q); bf16 on the tensor-core path, float32 otherwise) and the
+ * other intermediates of the kernels chosen for these dims. */
 size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk);
 
 /* Chunked SSD prefill (cloud.tencent Mamba-2 page, section "SSD算法").
@@ -119,6 +119,31 @@ ssd_status ssd_fwd_profiled(const ssd_dims *dims, const void *x, const float *dt
                             const void *B, const void *C, const float *D, const float *h0,
                             int32_t chunk, void *y, float *h_final, void *workspace,
                             size_t workspace_bytes, void *const *events, void *stream);
+
+/* Sequential ("chunked-prompt") prefill (the Falcon Mamba 7B release page,
+ * "Mamba 再次挑戰霸主 Transformer", on parallel versus sequential prefill:
+ * processing the prompt in pieces with the recurrent state carried between
+ * them keeps memory independent of the prompt length, which is what lets an
+ * SSM take prompts of any length).  The sequence is processed in windows of at most `window`
+ * tokens; each window is one ssd_fwd whose h0 is the previous window's final
+ * state (the first window's is h0).  The result equals one ssd_fwd over the
+ * whole sequence up to rounding, in device memory that does not grow with T.
+ *   window:   tokens per window, >= 1; a multiple of chunk keeps every window
+ *             on the chunk grid.
+ *   workspace/workspace_bytes: at least ssd_fwd_sequential_workspace_size()
+ *             bytes -- one window's ssd_fwd workspace, two carried float32
+ *             states and, for batch > 1, a staging copy of one window of x,
+ *             dt, B, C and y (windows of a batched [b, T, ...] tensor are
+ *             not contiguous; they are gathered and scattered with
+ *             asynchronous 2-D copies on `stream`).
+ * Other arguments and results as ssd_fwd.  Every step is enqueued on
+ * `stream`, so the call can be captured in a CUDA graph. */
+size_t ssd_fwd_sequential_workspace_size(const ssd_dims *dims, int32_t chunk, int64_t window);
+ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *dt,
+                              const float *A, const void *B, const void *C, const float *D,
+                              const float *h0, int32_t chunk, int64_t window, void *y,
+                              float *h_final, void *workspace, size_t workspace_bytes,
+                              void *stream);
 
 /* K-token multi-step verification decode ("Mamba in the Llama", section
  * "推测解码": MultiStep returns the K outputs, the state at the last verified

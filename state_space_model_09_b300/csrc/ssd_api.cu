@@ -507,6 +507,116 @@ ssd_status ssd_fwd_noalloc(const ssd_dims *dims, const void *x, const float *dt,
                   SSD_NOALLOC_SCRATCH_BYTES, nullptr, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Sequential prefill: windows of at most `window` tokens chained through the
+// state.  Workspace: [ssd_fwd workspace of one window][two carried states]
+// and, for batch > 1, staging copies of one window of x, dt, B, C and y.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct SeqPlan {
+  ssd_dims wd;  // dims of a full window
+  size_t fwd_bytes, carry_off, carry_bytes, stage_off, total;
+  size_t row_x, row_dt, row_b, row_c;  // bytes of one token of each tensor
+};
+
+ssd_status make_seq_plan(const ssd_dims *dims, int32_t chunk, int64_t window, SeqPlan *sp) {
+  ssd_status st = check_dims(dims);
+  if (st != SSD_OK) return st;
+  if (window < 1) return SSD_ERR_INVALID_ARG;
+  sp->wd = *dims;
+  sp->wd.seqlen = std::min<int64_t>(window, dims->seqlen);
+  Plan pl;
+  if ((st = make_plan(&sp->wd, chunk, &pl)) != SSD_OK) return st;
+  const size_t io = dims->io_dtype == SSD_BF16 ? 2 : 4;
+  sp->row_x = static_cast<size_t>(dims->nheads * dims->headdim) * io;
+  sp->row_dt = static_cast<size_t>(dims->nheads) * 4;
+  sp->row_b = static_cast<size_t>(dims->ngroups_b * dims->dstate) * io;
+  sp->row_c = static_cast<size_t>(dims->ngroups_c * dims->dstate) * io;
+  sp->fwd_bytes = pl.total;
+  sp->carry_off = sp->fwd_bytes;
+  sp->carry_bytes = align_up(static_cast<size_t>(dims->batch * dims->nheads * dims->dstate *
+                                                 dims->headdim) * 4);
+  sp->stage_off = sp->carry_off + 2 * sp->carry_bytes;
+  sp->total = sp->stage_off;
+  if (dims->batch > 1) {
+    const size_t rows = static_cast<size_t>(dims->batch * sp->wd.seqlen);
+    sp->total += align_up(rows * sp->row_x) * 2 + align_up(rows * sp->row_dt) +
+                 align_up(rows * sp->row_b) + align_up(rows * sp->row_c);
+  }
+  return SSD_OK;
+}
+
+// Copies tokens [t0, t0 + len) of a [b, T, row] tensor to or from a [b, len, row] one.
+bool copy_window(void *dst, size_t dpitch_tokens, const void *src, size_t spitch_tokens,
+                 size_t row, int64_t b, int64_t len, cudaStream_t s) {
+  return cudaMemcpy2DAsync(dst, dpitch_tokens * row, src, spitch_tokens * row,
+                           static_cast<size_t>(len) * row, static_cast<size_t>(b),
+                           cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+}
+
+}  // namespace
+
+size_t ssd_fwd_sequential_workspace_size(const ssd_dims *dims, int32_t chunk, int64_t window) {
+  SeqPlan sp;
+  return make_seq_plan(dims, chunk, window, &sp) == SSD_OK ? sp.total : 0;
+}
+
+ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *dt,
+                              const float *A, const void *B, const void *C, const float *D,
+                              const float *h0, int32_t chunk, int64_t window, void *y,
+                              float *h_final, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  SeqPlan sp;
+  ssd_status st = make_seq_plan(dims, chunk, window, &sp);
+  if (st != SSD_OK) return st;
+  if (!x || !dt || !A || !B || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
+  if (workspace_bytes < sp.total || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
+  const int64_t b = dims->batch, T = dims->seqlen, W = sp.wd.seqlen;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *carry[2] = {reinterpret_cast<float *>(ws + sp.carry_off),
+                     reinterpret_cast<float *>(ws + sp.carry_off + sp.carry_bytes)};
+  uint8_t *stage = ws + sp.stage_off;
+  const size_t rows = static_cast<size_t>(b * W);
+  uint8_t *sx = stage, *sy = sx + align_up(rows * sp.row_x);
+  uint8_t *sdt = sy + align_up(rows * sp.row_x), *sB = sdt + align_up(rows * sp.row_dt);
+  uint8_t *sC = sB + align_up(rows * sp.row_b);
+  const uint8_t *px = static_cast<const uint8_t *>(x), *pdt = reinterpret_cast<const uint8_t *>(dt),
+                *pB = static_cast<const uint8_t *>(B), *pC = static_cast<const uint8_t *>(C);
+  uint8_t *py = static_cast<uint8_t *>(y);
+  int w = 0;
+  for (int64_t t0 = 0; t0 < T; t0 += W, ++w) {
+    const int64_t len = std::min(W, T - t0);
+    ssd_dims d = sp.wd;
+    d.seqlen = len;
+    const float *hin = w == 0 ? h0 : carry[(w - 1) & 1];
+    float *hout = t0 + len >= T ? h_final : carry[w & 1];
+    const void *wx, *wdt, *wB, *wC;
+    void *wy;
+    if (b == 1) {  // a window of a single sequence is contiguous
+      wx = px + t0 * sp.row_x;
+      wdt = pdt + t0 * sp.row_dt;
+      wB = pB + t0 * sp.row_b;
+      wC = pC + t0 * sp.row_c;
+      wy = py + t0 * sp.row_x;
+    } else {
+      if (!copy_window(sx, len, px + t0 * sp.row_x, T, sp.row_x, b, len, s) ||
+          !copy_window(sdt, len, pdt + t0 * sp.row_dt, T, sp.row_dt, b, len, s) ||
+          !copy_window(sB, len, pB + t0 * sp.row_b, T, sp.row_b, b, len, s) ||
+          !copy_window(sC, len, pC + t0 * sp.row_c, T, sp.row_c, b, len, s))
+        return SSD_ERR_CUDA;
+      wx = sx; wdt = sdt; wB = sB; wC = sC; wy = sy;
+    }
+    st = fwd_impl(&d, wx, static_cast<const float *>(wdt), A, wB, wC, D, hin, chunk, wy, hout, ws,
+                  sp.fwd_bytes, nullptr, stream);
+    if (st != SSD_OK) return st;
+    if (b > 1 && !copy_window(py + t0 * sp.row_x, T, sy, len, sp.row_x, b, len, s))
+      return SSD_ERR_CUDA;
+  }
+  return SSD_OK;
+}
+
 ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                          const void *B, const void *C, const float *D, const float *h_cache,
                          const int32_t *j, void *y, float *h_j, float *h_K, void *stream) {

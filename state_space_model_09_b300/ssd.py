@@ -45,6 +45,11 @@ _vp = ctypes.c_void_p
 _P = ctypes.POINTER(ssd_dims)
 _lib.ssd_fwd_workspace_size.argtypes = [_P, ctypes.c_int32]
 _lib.ssd_fwd_workspace_size.restype = ctypes.c_size_t
+_lib.ssd_fwd_sequential_workspace_size.argtypes = [_P, ctypes.c_int32, ctypes.c_int64]
+_lib.ssd_fwd_sequential_workspace_size.restype = ctypes.c_size_t
+_lib.ssd_fwd_sequential.argtypes = [_P] + [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_int64] + \
+    [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]
+_lib.ssd_fwd_sequential.restype = ctypes.c_int32
 _lib.ssd_fwd_num_stages.argtypes = [_P, ctypes.c_int32]
 _lib.ssd_fwd_num_stages.restype = ctypes.c_int32
 _lib.ssd_fwd_stage_name.argtypes = [_P, ctypes.c_int32, ctypes.c_int32]
@@ -221,6 +226,38 @@ def forward(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, dt_softplus: bool
     h_final = torch.empty((b, H, B.shape[3], P), dtype=torch.float32, device=x.device)
     ws = workspace_for(dims, chunk, x.device)
     ssd_fwd(x, dt, A, B, C, D, h0, chunk, y, h_final, ws, dt_softplus, stream, dims)
+    return y, h_final
+
+
+def ssd_fwd_sequential_workspace_size(dims: ssd_dims, chunk: int, window: int) -> int:
+    return int(_lib.ssd_fwd_sequential_workspace_size(ctypes.byref(dims), int(chunk), int(window)))
+
+
+def ssd_fwd_sequential(x, dt, A, B, C, D, h0, chunk: int, window: int, y, h_final, workspace,
+                       dt_softplus: bool = True, stream=None,
+                       dims: Optional[ssd_dims] = None) -> None:
+    """Enqueue the windowed (sequential) prefill on `stream` (see ssd.h)."""
+    dims = dims or dims_of(x, B, C, dt_softplus)
+    ins, outs = _fwd_ptrs(x, dt, A, B, C, D, h0, y, h_final, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.ssd_fwd_sequential(ctypes.byref(dims), *ins, int(chunk), int(window), outs[0],
+                                 outs[1], outs[2], ws_bytes, _stream(stream))
+    _check(st, "ssd_fwd_sequential")
+
+
+def forward_sequential(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, window: int = 4096,
+                       dt_softplus: bool = True, stream=None):
+    """Allocates y, h_final and the (T-independent) workspace; calls ssd_fwd_sequential."""
+    dims = dims_of(x, B, C, dt_softplus)
+    y = torch.empty_like(x)
+    b, T, H, P = x.shape
+    h_final = torch.empty((b, H, B.shape[3], P), dtype=torch.float32, device=x.device)
+    n = ssd_fwd_sequential_workspace_size(dims, chunk, window)
+    if n == 0:
+        raise SsdError(SSD_ERR_UNSUPPORTED, "ssd_fwd_sequential_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+    ssd_fwd_sequential(x, dt, A, B, C, D, h0, chunk, window, y, h_final, ws, dt_softplus, stream,
+                       dims)
     return y, h_final
 
 

@@ -110,3 +110,28 @@ def test_multistep_validation():
     q = list(p)
     q[9] = q[6]  # h_j aliases h_cache
     assert lib.ssd_multistep(ctypes.byref(d), *q, None) == S.SSD_ERR_INVALID_ARG
+
+
+def test_sequential_workspace_is_independent_of_the_prompt_length():
+    w = S.ssd_fwd_sequential_workspace_size
+    short, long = _dims(batch=1, seqlen=1000), _dims(batch=1, seqlen=1_000_000)
+    assert w(short, 256, 512) == w(long, 256, 512) > 0
+    # batch > 1 adds a staging copy of one window of x, dt, B, C and y
+    assert w(_dims(batch=2, seqlen=1000), 256, 512) > w(_dims(batch=1, seqlen=1000), 256, 512)
+    # a window no longer than the sequence is what is planned for
+    assert w(short, 256, 10_000) == w(short, 256, 1000)
+    assert w(short, 256, 0) == 0 and w(short, 96, 512) == 0
+
+
+def test_sequential_rejects_bad_arguments_on_host():
+    d = _dims(batch=1, seqlen=1000)
+    n = S.ssd_fwd_sequential_workspace_size(d, 256, 256)
+    lib = S.library_handle()
+    fake = ctypes.c_void_p(0x10000)
+    args = [ctypes.byref(d)] + [fake] * 7 + [256, 256, fake, fake, fake]
+    # workspace too small, window 0, NULL x
+    assert lib.ssd_fwd_sequential(*args, n - 1, None) == S.SSD_ERR_INVALID_ARG
+    a2 = list(args); a2[9] = 0
+    assert lib.ssd_fwd_sequential(*a2, n, None) == S.SSD_ERR_INVALID_ARG
+    a3 = list(args); a3[1] = None
+    assert lib.ssd_fwd_sequential(*a3, n, None) == S.SSD_ERR_INVALID_ARG
