@@ -411,14 +411,20 @@ def run_ours(args, shape, work, world, rank, local):
 
 
 # ----------------------------------------------------------------------------- multistep arm
-def multistep_work(s: synth.MultistepShape):
+def multistep_work(s: synth.MultistepShape, verify: bool = False):
     """Bytes of one multi-step call: h_cache in, h_j and h_K out (f32), x and y
-    (io), B, C (io), dt (f32), j (int32)."""
+    (io), B, C (io), dt (f32), j (int32).  A fused verify call moves two states
+    (cache in, next cache out) and also reads the previous drafts' x, B, dt."""
     io = 2 if s.io == synth.BF16 else 4
     st = s.batch * s.nheads * s.dstate * s.headdim * 4
     x = s.batch * s.K * s.nheads * s.headdim * io
     bc = s.batch * s.K * (s.ngroups_b + s.ngroups_c) * s.dstate * io
-    return dict(bytes=3 * st + 2 * x + bc + s.batch * s.K * s.nheads * 4 + s.batch * 4,
+    dt = s.batch * s.K * s.nheads * 4
+    if verify:
+        bp = s.batch * s.K * s.ngroups_b * s.dstate * io
+        return dict(bytes=2 * st + 3 * x + bc + bp + 2 * dt + s.batch * 4,
+                    tok_heads=s.batch * s.K * s.nheads)
+    return dict(bytes=3 * st + 2 * x + bc + dt + s.batch * 4,
                 tok_heads=s.batch * s.K * s.nheads)
 
 
@@ -490,7 +496,7 @@ def run_multistep(args, world, rank, local):
     from state_space_model_09_b300 import ssd as S
 
     shape = synth.WORKLOADS["multistep_k8"]
-    work = multistep_work(shape)
+    work = multistep_work(shape, args.verify)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"] + 17 * rank)
@@ -510,12 +516,21 @@ def run_multistep(args, world, rank, local):
     steps = shape.steps
     stream = torch.cuda.Stream(dev)
 
+    J0 = torch.zeros_like(J[0])
+
     def chain():
         cur = h0
         for i in range(steps):
             nxt = bufs[i % 2]
-            S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur, J[i], Y[i], nxt, hK,
-                            stream=stream, dims=dims)
+            if args.verify:
+                # fused recompute + verify + cache: the cache is the state before
+                # the previous drafts, of which J[i-1] were accepted
+                p = i - 1 if i > 0 else 0
+                S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X[i], DT[i], A,
+                             BB[i], CC[i], D, cur, Y[i], nxt, stream=stream)
+            else:
+                S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur, J[i], Y[i], nxt, hK,
+                                stream=stream, dims=dims)
             cur = nxt
 
     with torch.cuda.stream(stream):
@@ -548,18 +563,21 @@ def run_multistep(args, world, rank, local):
     pk = peaks()
     gbs = work["bytes"] / (ms_step * 1e-3) / 1e9
     line = {
-        "metric": "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)",
+        "metric": ("SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
+                   "1000-step speculative chain)" if args.verify else
+                   "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)"),
         "value": round(world * work["tok_heads"] / (ms_step * 1e-3) / 1e6, 2), "unit": UNIT,
         "n_gpus": world, "steps": reps * steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64)",
         "config": {"workload": "multistep_k8", "batch": shape.batch, "K": shape.K,
                    "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                   "chain": steps, "graph": True,
-                   "l2": "states 3 x 42 MB per step (h_cache, h_j, h_K) ~ L2 size; no flush"},
+                   "chain": steps, "graph": True, "call": "ssd_verify" if args.verify else "ssd_multistep",
+                   "l2": ("states 2 x 42 MB per step (cache, next cache); no flush" if args.verify else
+                          "states 3 x 42 MB per step (h_cache, h_j, h_K) ~ L2 size; no flush")},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(gbs / pk["hbm"], 4),
-                     "traffic": measured_traffic("multistep_kernel", "multistep_k8"),
+                     "traffic": None if args.verify else measured_traffic("multistep_kernel", "multistep_k8"),
                      "kernel": "multistep_kernel",
                      "algorithmic_bytes": work["bytes"], "peak_source": pk["source"] + " (burst)"},
         "gpu_launches": reps * steps,
@@ -576,6 +594,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mamba2_2p7b", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify", action="store_true",
+                    help="multistep_k8: time the chain of fused recompute + verify calls")
     ap.add_argument("--window", type=int, default=0,
                     help="prefill through ssd_fwd_sequential with windows of this many tokens")
     args = ap.parse_args()

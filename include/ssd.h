@@ -162,6 +162,32 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
                          const void *B, const void *C, const float *D, const float *h_cache,
                          const int32_t *j, void *y, float *h_j, float *h_K, void *stream);
 
+/* Fused verification step with recompute ("Mamba in the Llama", section
+ * "硬件特定优化": for the verifier, one kernel first recomputes the previous
+ * steps from the cache, then decodes the new drafts, then caches).  The
+ * cache holds the state before the PREVIOUS call's K drafts, of which
+ * j_prev[b] were accepted; this call advances it through those j_prev[b]
+ * tokens -- the state every accepted prefix ends in -- stores that as the
+ * next cache, and decodes the K new drafts from it.  Per call each state is
+ * read once and written once (ssd_multistep writes two states).  Chaining
+ * ssd_verify(prev = the drafts of call s-1, j_prev = their accepted count)
+ * reproduces a ssd_multistep chain that continues from h_j bit for bit.
+ *   dims.seqlen = K (the same for the previous and the new drafts), K <= 16.
+ *   x_prev [b, K, H, P], dt_prev [b, K, H], B_prev [b, K, G_B, N]: the
+ *             previous call's drafts (their C is not needed).
+ *   j_prev:   DEVICE int32 [b], 0..K.  A value outside 0..K records
+ *             SSD_ERR_INVALID_ARG in the device error word (see
+ *             ssd_check_device_error) and leaves that batch row's y and
+ *             h_next unwritten.
+ *   x, dt, B, C, D: the new drafts, as in ssd_multistep.
+ *   h_cache:  [b, H, N, P] float32, the state before the previous drafts.
+ *   y [b, K, H, P] (io dtype), h_next [b, H, N, P] (float32): outputs; they
+ *             may not alias any input or each other. */
+ssd_status ssd_verify(const ssd_dims *dims, const void *x_prev, const float *dt_prev,
+                      const void *B_prev, const int32_t *j_prev, const void *x, const float *dt,
+                      const float *A, const void *B, const void *C, const float *D,
+                      const float *h_cache, void *y, float *h_next, void *stream);
+
 /* Allocation-free variant of ssd_fwd.  The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc at the point
  * where they run the layer -- code working under a fixed device-memory plan

@@ -311,6 +311,11 @@ __global__ void __launch_bounds__(256) chunk_scan_simt(
 // dynamic smem per item: B[K][N], C[K][N], x[K][PS], a[16], y partials [K][2][PS].
 // ----------------------------------------------------------------------------
 constexpr int kMsThreads = 128;
+// floats of shared memory per item: B, C [K][N], x [K][PS], decays, y partials
+// [K][2][PS]; verify adds the previous drafts' B [K][N], x [K][PS], decays.
+__host__ __device__ constexpr int ms_item_floats(int K, int N, int PS, bool verify) {
+  return 2 * K * N + K * PS + 16 + K * 2 * PS + (verify ? K * N + K * PS + 16 : 0);
+}
 constexpr int kMsItemThreads = 64;
 constexpr int kMsMaxK = 16;
 
@@ -318,13 +323,23 @@ constexpr int kMsMaxK = 16;
 // and the column slice PS when fixed at compile time (0: taken from the
 // arguments); with both fixed every shared-memory index of the row loop is a
 // constant offset, which removes most of its integer work.
-template <typename IO, int KT, int NC = 0, int PSC = 0>
+//
+// VF (verify): the fused recompute + multistep + cache step ("Mamba in the
+// Llama", 硬件特定优化: the verifier first recomputes the previous steps from
+// the cache, then decodes the new drafts, then caches, in one kernel).  The
+// cache h_cache then holds the state before the previous call's drafts
+// (xp, dtp, Bp); jacc[b] of them were accepted.  Each state row is advanced
+// through those jacc[b] tokens, stored to h_next (the next call's cache),
+// and then through the K new drafts for y; h_j and h_K are not written.  Per
+// row that is one state read and one state write instead of one and two.
+template <typename IO, int KT, int NC = 0, int PSC = 0, bool VF = false>
 __global__ void __launch_bounds__(128, 5) multistep_kernel(
     const IO *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const IO *__restrict__ Bm, const IO *__restrict__ Cm, const float *__restrict__ D,
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
     float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N_arg,
-    int P, int PS_arg, int softplus) {
+    int P, int PS_arg, int softplus, const IO *__restrict__ xp, const float *__restrict__ dtp,
+    const IO *__restrict__ Bp, float *__restrict__ h_next) {
   const int N = NC ? NC : N_arg;
   const int PS = PSC ? PSC : PS_arg;
   extern __shared__ float sm_ms[];
@@ -332,12 +347,15 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
   const int h = 2 * blockIdx.x + item, b = blockIdx.y, p0 = blockIdx.z * PS;
   const int tid = threadIdx.x % kMsItemThreads, lane = threadIdx.x & 31;
   const int warp = tid >> 5;  // warp within the item: 0 or 1
-  const int item_floats = 2 * K * N + K * PS + kMsMaxK + K * 2 * PS;
+  const int item_floats = ms_item_floats(K, N, PS, VF);
   float *sB = sm_ms + item * item_floats;
   float *sC = sB + K * N;
   float *sx = sC + K * N;
   float *sa = sx + K * PS;
   float *red = sa + kMsMaxK;
+  float *sBp = red + K * 2 * PS;  // verify: previous drafts' B, x and decays
+  float *sxp = sBp + K * N;
+  float *sap = sxp + K * PS;
   const bool live = h < H;
   const int hh = live ? h : H - 1;
   const int gb = hh / (H / GB), gc = hh / (H / GC);
@@ -357,18 +375,34 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
     const float z = dt[(static_cast<int64_t>(b) * K + tid) * H + hh];
     sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
   }
+  if (VF) {
+    for (int i = tid; i < K * N; i += kMsItemThreads) {
+      const int k = i / N, n = i % N;
+      sBp[i] = to_f32(Bp[((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n]);
+    }
+    for (int i = tid; i < K * PS; i += kMsItemThreads) {
+      const int k = i / PS, p = i % PS;
+      sxp[i] = to_f32(xp[((static_cast<int64_t>(b) * K + k) * H + hh) * P + p0 + p]);
+    }
+    if (tid < K) {
+      const float z = dtp[(static_cast<int64_t>(b) * K + tid) * H + hh];
+      sap[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
+    }
+  }
   int jb = jacc[b];
   if (jb < 0 || jb > K) {
     if (tid == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
     jb = -1;
   }
   __syncthreads();
+  // verify: a batch row whose accepted count is out of range gets no outputs
+  const bool run = !VF || jb >= 0;
 
   float4 yp[KT];
 #pragma unroll
   for (int k = 0; k < KT; ++k) yp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  if (live) {
+  if (live && run) {
     const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
     const int rows = N / R;
     constexpr int PF = 4;  // rows in flight
@@ -386,9 +420,24 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
           if (i + PF < rows)
             buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(n + R * PF) * P));
           const int64_t off = base + static_cast<int64_t>(n) * P;
+          if (VF) {
+            // recompute the accepted previous drafts, then cache the result
+#pragma unroll
+            for (int k = 0; k < KT; ++k) {
+              if (k < jb) {
+                const float bn = sBp[k * N + n], a = sap[k];
+                const float4 xk = *reinterpret_cast<const float4 *>(sxp + k * PS + 4 * q);
+                st.x = fmaf(a, st.x, bn * xk.x);
+                st.y = fmaf(a, st.y, bn * xk.y);
+                st.z = fmaf(a, st.z, bn * xk.z);
+                st.w = fmaf(a, st.w, bn * xk.w);
+              }
+            }
+            *reinterpret_cast<float4 *>(h_next + off) = st;
+          }
           // h_j with ordinary (L2-resident) stores: a speculative decode step
           // usually continues from it, so the next call finds it in L2
-          if (jb == 0) *reinterpret_cast<float4 *>(h_j + off) = st;
+          if (!VF && jb == 0) *reinterpret_cast<float4 *>(h_j + off) = st;
 #pragma unroll
           for (int k = 0; k < KT; ++k) {
             if (k < K) {
@@ -402,10 +451,10 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
               yp[k].y = fmaf(cn, st.y, yp[k].y);
               yp[k].z = fmaf(cn, st.z, yp[k].z);
               yp[k].w = fmaf(cn, st.w, yp[k].w);
-              if (k + 1 == jb) *reinterpret_cast<float4 *>(h_j + off) = st;
+              if (!VF && k + 1 == jb) *reinterpret_cast<float4 *>(h_j + off) = st;
             }
           }
-          __stcs(reinterpret_cast<float4 *>(h_K + off), st);
+          if (!VF) __stcs(reinterpret_cast<float4 *>(h_K + off), st);
         }
       }
     }
@@ -425,7 +474,7 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
     }
   }
   __syncthreads();
-  if (!live) return;
+  if (!live || !run) return;
   const float Dh = D ? D[h] : 0.f;
   for (int i = tid; i < K * PS; i += kMsItemThreads) {
     const int k = i / PS, p = i % PS;

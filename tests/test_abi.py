@@ -135,3 +135,19 @@ def test_sequential_rejects_bad_arguments_on_host():
     assert lib.ssd_fwd_sequential(*a2, n, None) == S.SSD_ERR_INVALID_ARG
     a3 = list(args); a3[1] = None
     assert lib.ssd_fwd_sequential(*a3, n, None) == S.SSD_ERR_INVALID_ARG
+
+
+def test_verify_rejects_bad_arguments_on_host():
+    lib = S.library_handle()
+    d = _dims(batch=2, seqlen=8)
+    fake = [ctypes.c_void_p(0x10000 + 0x1000 * i) for i in range(13)]
+    # NULL previous drafts
+    args = [ctypes.byref(d), None] + fake[1:13] + [None]
+    assert lib.ssd_verify(*args) == S.SSD_ERR_INVALID_ARG
+    # K > 16
+    d17 = _dims(batch=2, seqlen=17)
+    assert lib.ssd_verify(ctypes.byref(d17), *fake, None) == S.SSD_ERR_UNSUPPORTED
+    # h_next aliasing h_cache
+    alias = list(fake)
+    alias[12] = alias[10]
+    assert lib.ssd_verify(ctypes.byref(d), *alias, None) == S.SSD_ERR_INVALID_ARG
