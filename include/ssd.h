@@ -164,29 +164,34 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
 
 /* Fused verification step with recompute ("Mamba in the Llama", section
  * "硬件特定优化": for the verifier, one kernel first recomputes the previous
- * steps from the cache, then decodes the new drafts, then caches).  The
- * cache holds the state before the PREVIOUS call's K drafts, of which
+ * steps from the cache, then decodes the new drafts, then caches; for a Mamba
+ * draft model, recompute, decode and cache are likewise one kernel).  The
+ * cache holds the state before the PREVIOUS call's k_prev drafts, of which
  * j_prev[b] were accepted; this call advances it through those j_prev[b]
  * tokens -- the state every accepted prefix ends in -- stores that as the
- * next cache, and decodes the K new drafts from it.  Per call each state is
- * read once and written once (ssd_multistep writes two states).  Chaining
- * ssd_verify(prev = the drafts of call s-1, j_prev = their accepted count)
- * reproduces a ssd_multistep chain that continues from h_j bit for bit.
- *   dims.seqlen = K (the same for the previous and the new drafts), K <= 16.
- *   x_prev [b, K, H, P], dt_prev [b, K, H], B_prev [b, K, G_B, N]: the
- *             previous call's drafts (their C is not needed).
- *   j_prev:   DEVICE int32 [b], 0..K.  A value outside 0..K records
+ * next cache, and decodes the K new tokens from it.  Per call each state is
+ * read once and written once (ssd_multistep writes two states).
+ *   Verifier: k_prev = K = the draft length.  Chaining ssd_verify(prev = the
+ *             drafts of call s-1, j_prev = their accepted count) reproduces a
+ *             ssd_multistep chain that continues from h_j bit for bit.
+ *   Draft model: the first draft step of a round is ssd_verify with the
+ *             previous round's k_prev drafts and K = 1 new token; the rest of
+ *             the round are ssd_multistep calls with K = 1.
+ *   dims.seqlen = K, the new tokens (1..16); k_prev: 1..16.
+ *   x_prev [b, k_prev, H, P], dt_prev [b, k_prev, H], B_prev [b, k_prev, G_B, N]:
+ *             the previous drafts (their C is not needed).
+ *   j_prev:   DEVICE int32 [b], 0..k_prev.  A value outside that records
  *             SSD_ERR_INVALID_ARG in the device error word (see
  *             ssd_check_device_error) and leaves that batch row's y and
  *             h_next unwritten.
- *   x, dt, B, C, D: the new drafts, as in ssd_multistep.
+ *   x, dt, B, C, D: the new tokens, as in ssd_multistep.
  *   h_cache:  [b, H, N, P] float32, the state before the previous drafts.
  *   y [b, K, H, P] (io dtype), h_next [b, H, N, P] (float32): outputs; they
  *             may not alias any input or each other. */
-ssd_status ssd_verify(const ssd_dims *dims, const void *x_prev, const float *dt_prev,
-                      const void *B_prev, const int32_t *j_prev, const void *x, const float *dt,
-                      const float *A, const void *B, const void *C, const float *D,
-                      const float *h_cache, void *y, float *h_next, void *stream);
+ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
+                      const float *dt_prev, const void *B_prev, const int32_t *j_prev,
+                      const void *x, const float *dt, const float *A, const void *B, const void *C,
+                      const float *D, const float *h_cache, void *y, float *h_next, void *stream);
 
 /* Allocation-free variant of ssd_fwd.  The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc at the point

@@ -288,12 +288,12 @@ ssd_status launch_multistep(dim3 grid, int64_t smem, const ssd_dims *d, const vo
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
       static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus, nullptr,
-      nullptr, nullptr, nullptr);
+      nullptr, nullptr, nullptr, 0);
   return launch_status();
 }
 
 template <typename IO, int KT, int NC = 0, int PSC = 0>
-ssd_status launch_verify(dim3 grid, int64_t smem, const ssd_dims *d, const void *xp,
+ssd_status launch_verify(dim3 grid, int64_t smem, const ssd_dims *d, int KP, const void *xp,
                          const float *dtp, const void *Bp, const int32_t *jp, const void *x,
                          const float *dt, const float *A, const void *B, const void *C,
                          const float *D, const float *h_cache, void *y, float *h_next, int PS,
@@ -308,7 +308,7 @@ ssd_status launch_verify(dim3 grid, int64_t smem, const ssd_dims *d, const void 
       D, h_cache, jp, static_cast<IO *>(y), nullptr, nullptr, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
       static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus,
-      static_cast<const IO *>(xp), dtp, static_cast<const IO *>(Bp), h_next);
+      static_cast<const IO *>(xp), dtp, static_cast<const IO *>(Bp), h_next, KP);
   return launch_status();
 }
 
@@ -693,15 +693,16 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
   return st;
 }
 
-ssd_status ssd_verify(const ssd_dims *dims, const void *x_prev, const float *dt_prev,
-                      const void *B_prev, const int32_t *j_prev, const void *x, const float *dt,
-                      const float *A, const void *B, const void *C, const float *D,
-                      const float *h_cache, void *y, float *h_next, void *stream) {
+ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
+                      const float *dt_prev, const void *B_prev, const int32_t *j_prev,
+                      const void *x, const float *dt, const float *A, const void *B, const void *C,
+                      const float *D, const float *h_cache, void *y, float *h_next, void *stream) {
   ssd_status st = check_dims(dims);
   if (st != SSD_OK) return st;
   const int64_t b = dims->batch, K = dims->seqlen, H = dims->nheads, P = dims->headdim,
-                N = dims->dstate, GB = dims->ngroups_b, GC = dims->ngroups_c;
-  if (K > 16) return SSD_ERR_UNSUPPORTED;
+                N = dims->dstate, GB = dims->ngroups_b, GC = dims->ngroups_c, KP = k_prev;
+  if (K > 16 || KP > 16) return SSD_ERR_UNSUPPORTED;
+  if (KP < 1) return SSD_ERR_INVALID_ARG;
   if (b > 65535 || H > 65535) return SSD_ERR_UNSUPPORTED;
   if (!x_prev || !dt_prev || !B_prev || !j_prev || !x || !dt || !A || !B || !C || !h_cache ||
       !y || !h_next)
@@ -715,8 +716,11 @@ ssd_status ssd_verify(const ssd_dims *dims, const void *x_prev, const float *dt_
   const size_t nst = static_cast<size_t>(b * H * N * P) * 4;
   const size_t ndt = static_cast<size_t>(b * K * H) * 4;
   const size_t nB = static_cast<size_t>(b * K * GB * N) * io;
+  const size_t nxp = static_cast<size_t>(b * KP * H * P) * io;
+  const size_t ndtp = static_cast<size_t>(b * KP * H) * 4;
+  const size_t nBp = static_cast<size_t>(b * KP * GB * N) * io;
   struct Buf { const void *p; size_t n; };
-  const Buf ins[] = {{x_prev, nx}, {dt_prev, ndt}, {B_prev, nB}, {j_prev, static_cast<size_t>(b) * 4},
+  const Buf ins[] = {{x_prev, nxp}, {dt_prev, ndtp}, {B_prev, nBp}, {j_prev, static_cast<size_t>(b) * 4},
                      {x, nx}, {dt, ndt}, {A, static_cast<size_t>(H) * 4}, {B, nB},
                      {C, static_cast<size_t>(b * K * GC * N) * io}, {D, static_cast<size_t>(H) * 4},
                      {h_cache, nst}};
@@ -729,17 +733,17 @@ ssd_status ssd_verify(const ssd_dims *dims, const void *x_prev, const float *dt_
   const int PS = P % 128 == 0 ? 128 : P % 64 == 0 ? 64 : P % 32 == 0 ? 32 : 16;
   const int R = ssd::kMsItemThreads / (PS / 4);
   if (N % R) return SSD_ERR_UNSUPPORTED;
-  const int64_t smem = 2 * static_cast<int64_t>(ssd::ms_item_floats(static_cast<int>(K), static_cast<int>(N), PS, true)) * 4;
+  const int64_t smem = 2 * static_cast<int64_t>(ssd::ms_item_floats(static_cast<int>(K), static_cast<int>(N), PS, true, static_cast<int>(KP))) * 4;
   if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid(static_cast<unsigned>((H + 1) / 2), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
   if (bf16 && K <= 8 && N == 128 && PS == 64)
-    return launch_verify<__nv_bfloat16, 8, 128, 64>(grid, smem, dims, x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
+    return launch_verify<__nv_bfloat16, 8, 128, 64>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
   if (bf16)
-    return K <= 8 ? launch_verify<__nv_bfloat16, 8>(grid, smem, dims, x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
-                  : launch_verify<__nv_bfloat16, 16>(grid, smem, dims, x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
-  return K <= 8 ? launch_verify<float, 8>(grid, smem, dims, x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
-                : launch_verify<float, 16>(grid, smem, dims, x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
+    return K <= 8 ? launch_verify<__nv_bfloat16, 8>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
+                  : launch_verify<__nv_bfloat16, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
+  return K <= 8 ? launch_verify<float, 8>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
+                : launch_verify<float, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
 }
 
 ssd_status ssd_check_device_error(void *stream) {

@@ -312,9 +312,9 @@ __global__ void __launch_bounds__(256) chunk_scan_simt(
 // ----------------------------------------------------------------------------
 constexpr int kMsThreads = 128;
 // floats of shared memory per item: B, C [K][N], x [K][PS], decays, y partials
-// [K][2][PS]; verify adds the previous drafts' B [K][N], x [K][PS], decays.
-__host__ __device__ constexpr int ms_item_floats(int K, int N, int PS, bool verify) {
-  return 2 * K * N + K * PS + 16 + K * 2 * PS + (verify ? K * N + K * PS + 16 : 0);
+// [K][2][PS]; verify adds the previous drafts' B [KP][N], x [KP][PS], decays.
+__host__ __device__ constexpr int ms_item_floats(int K, int N, int PS, bool verify, int KP = 0) {
+  return 2 * K * N + K * PS + 16 + K * 2 * PS + (verify ? KP * N + KP * PS + 16 : 0);
 }
 constexpr int kMsItemThreads = 64;
 constexpr int kMsMaxK = 16;
@@ -327,7 +327,7 @@ constexpr int kMsMaxK = 16;
 // VF (verify): the fused recompute + multistep + cache step ("Mamba in the
 // Llama", 硬件特定优化: the verifier first recomputes the previous steps from
 // the cache, then decodes the new drafts, then caches, in one kernel).  The
-// cache h_cache then holds the state before the previous call's drafts
+// cache h_cache then holds the state before the previous call's KP drafts
 // (xp, dtp, Bp); jacc[b] of them were accepted.  Each state row is advanced
 // through those jacc[b] tokens, stored to h_next (the next call's cache),
 // and then through the K new drafts for y; h_j and h_K are not written.  Per
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
     float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N_arg,
     int P, int PS_arg, int softplus, const IO *__restrict__ xp, const float *__restrict__ dtp,
-    const IO *__restrict__ Bp, float *__restrict__ h_next) {
+    const IO *__restrict__ Bp, float *__restrict__ h_next, int KP) {
   const int N = NC ? NC : N_arg;
   const int PS = PSC ? PSC : PS_arg;
   extern __shared__ float sm_ms[];
@@ -347,15 +347,15 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
   const int h = 2 * blockIdx.x + item, b = blockIdx.y, p0 = blockIdx.z * PS;
   const int tid = threadIdx.x % kMsItemThreads, lane = threadIdx.x & 31;
   const int warp = tid >> 5;  // warp within the item: 0 or 1
-  const int item_floats = ms_item_floats(K, N, PS, VF);
+  const int item_floats = ms_item_floats(K, N, PS, VF, KP);
   float *sB = sm_ms + item * item_floats;
   float *sC = sB + K * N;
   float *sx = sC + K * N;
   float *sa = sx + K * PS;
   float *red = sa + kMsMaxK;
   float *sBp = red + K * 2 * PS;  // verify: previous drafts' B, x and decays
-  float *sxp = sBp + K * N;
-  float *sap = sxp + K * PS;
+  float *sxp = sBp + KP * N;
+  float *sap = sxp + KP * PS;
   const bool live = h < H;
   const int hh = live ? h : H - 1;
   const int gb = hh / (H / GB), gc = hh / (H / GC);
@@ -376,21 +376,21 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
     sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
   }
   if (VF) {
-    for (int i = tid; i < K * N; i += kMsItemThreads) {
+    for (int i = tid; i < KP * N; i += kMsItemThreads) {
       const int k = i / N, n = i % N;
-      sBp[i] = to_f32(Bp[((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n]);
+      sBp[i] = to_f32(Bp[((static_cast<int64_t>(b) * KP + k) * GB + gb) * N + n]);
     }
-    for (int i = tid; i < K * PS; i += kMsItemThreads) {
+    for (int i = tid; i < KP * PS; i += kMsItemThreads) {
       const int k = i / PS, p = i % PS;
-      sxp[i] = to_f32(xp[((static_cast<int64_t>(b) * K + k) * H + hh) * P + p0 + p]);
+      sxp[i] = to_f32(xp[((static_cast<int64_t>(b) * KP + k) * H + hh) * P + p0 + p]);
     }
-    if (tid < K) {
-      const float z = dtp[(static_cast<int64_t>(b) * K + tid) * H + hh];
+    if (tid < KP) {
+      const float z = dtp[(static_cast<int64_t>(b) * KP + tid) * H + hh];
       sap[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
     }
   }
   int jb = jacc[b];
-  if (jb < 0 || jb > K) {
+  if (jb < 0 || jb > (VF ? KP : K)) {
     if (tid == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
     jb = -1;
   }
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(128, 5) multistep_kernel(
           if (VF) {
             // recompute the accepted previous drafts, then cache the result
 #pragma unroll
-            for (int k = 0; k < KT; ++k) {
+            for (int k = 0; k < kMsMaxK; ++k) {
               if (k < jb) {
                 const float bn = sBp[k * N + n], a = sap[k];
                 const float4 xk = *reinterpret_cast<const float4 *>(sxp + k * PS + 4 * q);

@@ -45,7 +45,7 @@ _vp = ctypes.c_void_p
 _P = ctypes.POINTER(ssd_dims)
 _lib.ssd_fwd_workspace_size.argtypes = [_P, ctypes.c_int32]
 _lib.ssd_fwd_workspace_size.restype = ctypes.c_size_t
-_lib.ssd_verify.argtypes = [_P] + [ctypes.c_void_p] * 14
+_lib.ssd_verify.argtypes = [_P, ctypes.c_int32] + [ctypes.c_void_p] * 14
 _lib.ssd_verify.restype = ctypes.c_int32
 _lib.ssd_fwd_sequential_workspace_size.argtypes = [_P, ctypes.c_int32, ctypes.c_int64]
 _lib.ssd_fwd_sequential_workspace_size.restype = ctypes.c_size_t
@@ -265,10 +265,12 @@ def forward_sequential(x, dt, A, B, C, D=None, h0=None, chunk: int = 256, window
 
 def ssd_verify(x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next,
                dt_softplus: bool = True, stream=None) -> None:
-    """Enqueue the fused recompute + verify + cache step on `stream` (see ssd.h)."""
+    """Enqueue the fused recompute + decode + cache step on `stream` (see ssd.h).
+    The number of previous drafts is x_prev.shape[1]; the new tokens x.shape[1]."""
     dims = dims_of(x, B, C, dt_softplus)
     p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
-    st = _lib.ssd_verify(ctypes.byref(dims), p(x_prev), p(dt_prev), p(B_prev), p(j_prev), p(x),
+    st = _lib.ssd_verify(ctypes.byref(dims), int(x_prev.shape[1]), p(x_prev), p(dt_prev),
+                         p(B_prev), p(j_prev), p(x),
                          p(dt), p(A), p(B), p(C), p(D), p(h_cache), p(y), p(h_next),
                          _stream(stream))
     _check(st, "ssd_verify")

@@ -138,16 +138,26 @@ def test_sequential_rejects_bad_arguments_on_host():
 
 
 def test_verify_rejects_bad_arguments_on_host():
+    """Host-side checks only: every case returns before anything touches the
+    (fake, never dereferenced) device pointers."""
     lib = S.library_handle()
     d = _dims(batch=2, seqlen=8)
-    fake = [ctypes.c_void_p(0x10000 + 0x1000 * i) for i in range(13)]
-    # NULL previous drafts
-    args = [ctypes.byref(d), None] + fake[1:13] + [None]
-    assert lib.ssd_verify(*args) == S.SSD_ERR_INVALID_ARG
-    # K > 16
-    d17 = _dims(batch=2, seqlen=17)
-    assert lib.ssd_verify(ctypes.byref(d17), *fake, None) == S.SSD_ERR_UNSUPPORTED
-    # h_next aliasing h_cache
-    alias = list(fake)
+    # 13 distinct, far-apart, 16-byte-aligned addresses for:
+    # x_prev dt_prev B_prev j_prev x dt A B C D h_cache y h_next
+    ptr = [ctypes.c_void_p((i + 1) << 32) for i in range(13)]
+
+    def call(dims, k_prev, p):
+        return lib.ssd_verify(ctypes.byref(dims), k_prev, *p, None)
+
+    no_prev = list(ptr)
+    no_prev[0] = None
+    assert call(d, 8, no_prev) == S.SSD_ERR_INVALID_ARG           # NULL previous drafts
+    assert call(_dims(batch=2, seqlen=17), 8, ptr) == S.SSD_ERR_UNSUPPORTED   # K > 16
+    assert call(d, 17, ptr) == S.SSD_ERR_UNSUPPORTED              # k_prev > 16
+    assert call(d, 0, ptr) == S.SSD_ERR_INVALID_ARG               # k_prev < 1
+    alias = list(ptr)
     alias[12] = alias[10]
-    assert lib.ssd_verify(ctypes.byref(d), *alias, None) == S.SSD_ERR_INVALID_ARG
+    assert call(d, 8, alias) == S.SSD_ERR_INVALID_ARG             # h_next aliases h_cache
+    odd = list(ptr)
+    odd[4] = ctypes.c_void_p(ptr[4].value + 8)
+    assert call(d, 8, odd) == S.SSD_ERR_INVALID_ARG               # x not 16-byte aligned

@@ -115,3 +115,37 @@ def test_verify_bad_j_prev_is_reported_and_row_untouched():
     assert e.value.status == S.SSD_ERR_INVALID_ARG
     assert torch.isfinite(y[0].float()).all() and torch.isfinite(h_next[0]).all()
     assert torch.isnan(y[1].float()).all() and torch.isnan(h_next[1]).all()
+
+
+def test_draft_step_recompute_then_one_token():
+    """Draft-model side: the first draft step of a round rolls the draft's
+    cache through the j_prev accepted tokens of the previous round (8 slots)
+    and decodes ONE new token, in one call (k_prev = 8, K = 1)."""
+    prev_shape = M(3, 8, 4, 64, 128, 1, 1, synth.BF16, 1)
+    new_shape = M(3, 1, 4, 64, 128, 1, 1, synth.BF16, 1)
+    pin = synth.make_multistep_inputs(prev_shape, 75, steps=1)
+    nin = synth.make_multistep_inputs(new_shape, 76, steps=1)
+    prev, cur = _steps(pin, synth.BF16, 0), _steps(nin, synth.BF16, 0)
+    jp = torch.tensor([0, 5, 8], dtype=torch.int32, device="cuda")
+    A, D = torch.from_numpy(pin["A"]).cuda(), torch.from_numpy(pin["D"]).cuda()
+    h_cache = torch.from_numpy(pin["h_cache"]).cuda()
+    y = torch.full_like(cur["x"], float("nan"))
+    h_next = torch.full_like(h_cache, float("nan"))
+    S.ssd_verify(prev["x"], prev["dt"], prev["B"], jp, cur["x"], cur["dt"], A, cur["B"],
+                 cur["C"], D, h_cache, y, h_next)
+    torch.cuda.synchronize()
+    S.ssd_check_device_error()
+    b, H = 3, 4
+    pairs = list(range(b * H))
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    _, h_ref, _ = oracle.ssd_multistep(f64(prev["x"]), pin["dt"][0], pin["A"], f64(prev["B"]),
+                                       f64(prev["B"]), pin["D"], pin["h_cache"],
+                                       jp.cpu().numpy(), pairs=pairs)
+    y_ref, _, _ = oracle.ssd_multistep(f64(cur["x"]), nin["dt"][0], pin["A"], f64(cur["B"]),
+                                       f64(cur["C"]), pin["D"], h_ref.reshape(b, H, 128, 64),
+                                       np.zeros(b, dtype=np.int32), pairs=pairs)
+    hn = f64(h_next).reshape(b * H, 128, 64)
+    yy = f64(y)
+    ys = np.stack([yy[p // H, :, p % H, :] for p in pairs])
+    assert np.abs(hn - h_ref).max() / np.abs(h_ref).max() <= 1e-2
+    assert np.abs(ys - y_ref).max() / np.abs(y_ref).max() <= 1e-2
