@@ -51,8 +51,8 @@ MEASURED_TRAFFIC = {
         (269_728_768, "state_space_model_09_b300/csrc/ssd_state.cuh",
          "03036be1fc4d80f9f3f82cc70eb68c769eafd0b1"),
     ("multistep_kernel", "multistep_k8"):
-        (70_245_120, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
-         "f575ddfdbe1e709db11955094bcca465e1547ba7"),
+        (70_129_920, "state_space_model_09_b300/csrc/ssd_kernels.cuh",
+         "f1267a2133217f991f16eac81edf77c2e16126eb"),
 }
 
 
