@@ -424,7 +424,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
     int group = -1;
     for (int k = 0; k < nh; ++k) {
-      const int h = h_begin + k;
       const int tb = k & 1;  // this head's table buffer
       a_tab = tables + tb * L::kTables * Q;
       e_tab = a_tab + Q;
