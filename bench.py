@@ -45,8 +45,8 @@ L2_BYTES = 126 * 1024 * 1024
 # the summaries are in profiles/.  A changed source reports null.
 MEASURED_TRAFFIC = {
     ("chunk_scan_hl", "mamba2_2p7b"):
-        (406_627_840, "state_space_model_09_b300/csrc/ssd_scan.cuh",
-         "4fb9995bf87887d2f10a730a63c27b4c9c93ad75"),
+        (405_942_016, "state_space_model_09_b300/csrc/ssd_scan.cuh",
+         "3d3f490eb8d129a5aa8a8ba2e290692b46a84ae2"),
     ("chunk_state_pass_tc", "mamba2_2p7b"):
         (269_728_768, "state_space_model_09_b300/csrc/ssd_state.cuh",
          "03036be1fc4d80f9f3f82cc70eb68c769eafd0b1"),
@@ -255,6 +255,65 @@ def run_reference(args, shape, work):
             "data": "synthetic (seeded)", "impl": "reference",
             "config": config_of(args, shape, "cpu"),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": min(cores, n),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line, ensure_ascii=False))
+
+
+def oracle_multistep_chain(calls: int, budget_s: float):
+    """The fp64 oracle walking a multistep_k8 speculative chain (each call
+    continues from the previous call's h_j) on a bounded sample of the
+    (batch, head) pairs per call.  Returns (Mtok·heads/s, ms per call, cores,
+    sample description)."""
+    import oracle
+    shape = synth.WORKLOADS["multistep_k8"]
+    distinct = min(calls, 64)  # drafts drawn for 64 calls, reused cyclically (bounded memory)
+    inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"], steps=distinct)
+    b, H = shape.batch, shape.nheads
+    total = b * H
+    cores = oracle.default_threads()
+    h = inp["h_cache"].copy()
+
+    def call(i, pairs):
+        i %= distinct
+        _, hj, _ = oracle.ssd_multistep(inp["x"][i], inp["dt"][i], inp["A"], inp["B"][i],
+                                        inp["C"][i], inp["D"], h, inp["j"][i], pairs=pairs)
+        for q, pr in enumerate(pairs):  # the sampled pairs continue from h_j
+            h[pr // H, pr % H] = hj[q]
+
+    probe = list(range(min(total, max(cores, 8))))
+    t0 = time.perf_counter()
+    call(0, probe)
+    per_pair = (time.perf_counter() - t0) / len(probe)
+    h[:] = inp["h_cache"]
+    n = int(max(1, min(total, budget_s / calls / max(per_pair, 1e-9))))
+    pairs = list(range(n))
+    warm = min(3, calls - 1)
+    for i in range(warm):
+        call(i, pairs)
+    t0 = time.perf_counter()
+    for i in range(warm, calls):
+        call(i, pairs)
+    t = (time.perf_counter() - t0) / (calls - warm)
+    sample = ("%d of %d (batch, head) pairs per call, a %d-call chain from the cached state "
+              "over %d distinct draft sets (fp64)" % (n, total, calls, distinct))
+    return n * shape.K / t / 1e6, t * 1e3, min(cores, n), sample
+
+
+def run_reference_multistep(args):
+    """--impl reference on multistep_k8: the oracle chain, one call per step."""
+    shape = synth.WORKLOADS["multistep_k8"]
+    value, ms, cores, sample = oracle_multistep_chain(args.warmup + args.steps, 150.0)
+    line = {"metric": "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)",
+            "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": "multistep_k8", "batch": shape.batch, "K": shape.K,
+                       "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                       "chain": shape.steps, "call": "oracle ssd_multistep"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -610,6 +669,46 @@ def run_multistep(args, world, rank, local):
     barrier(world)
     clk = clocks.stop()
     ms_step = max_over_ranks(e0.elapsed_time(e1) / (reps * steps), world, dev)
+
+    # ---- end to end through the public API: each call's drafts (x, dt, B, C)
+    # and accepted count j copied in from pinned host memory, y read back; the
+    # recurrent state stays resident on the device, as a decoder's cache does
+    ke = max(3, min(args.steps, 200))
+    hx = {k: torch.from_numpy(inp[k][:ke]).pin_memory() for k in ("dt", "j")}
+    for k in ("x", "B", "C"):
+        hx[k] = torch.from_numpy(inp[k][:ke]).to(bf).pin_memory()
+    # two device slots: a verify call also reads the previous call's drafts
+    dxs = [{k: torch.zeros_like(v[0], device=dev) for k, v in hx.items()} for _ in range(2)]
+    hy = torch.empty(Y[0].shape, dtype=Y.dtype, pin_memory=True)
+    with torch.cuda.stream(stream):
+        def e2e_call(i, cur, nxt):
+            dx, dp = dxs[i % 2], dxs[(i + 1) % 2]
+            for k in ("x", "dt", "B", "C", "j"):
+                dx[k].copy_(hx[k][i], non_blocking=True)
+            if args.verify:
+                S.ssd_verify(dp["x"], dp["dt"], dp["B"], dp["j"] if i > 0 else J0, dx["x"],
+                             dx["dt"], A, dx["B"], dx["C"], D, cur, Y[0], nxt, stream=stream)
+            else:
+                S.ssd_multistep(dx["x"], dx["dt"], A, dx["B"], dx["C"], D, cur, dx["j"], Y[0],
+                                nxt, hK, stream=stream, dims=dims)
+            hy.copy_(Y[0], non_blocking=True)
+
+        for i in range(3):
+            e2e_call(i, h0, bufs[i % 2])
+        torch.cuda.synchronize()
+        barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        cur = h0
+        for i in range(ke):
+            e2e_call(i, cur, bufs[i % 2])
+            cur = bufs[i % 2]
+        f1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / ke, world, dev)
+    h2d = sum(v[0].numel() * v[0].element_size() for v in hx.values())
+    d2h = hy.numel() * hy.element_size()
     if rank != 0:
         return
     pk = peaks()
@@ -633,8 +732,15 @@ def run_multistep(args, world, rank, local):
                      "kernel": "multistep_kernel",
                      "algorithmic_bytes": work["bytes"], "peak_source": pk["source"] + " (burst)"},
         "gpu_launches": reps * steps,
+        "e2e": {"value": round(world * work["tok_heads"] / (e2e_ms * 1e-3) / 1e6, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
         "clocks": clk,
     }
+    if world == 1 and not args.no_cpu_baseline:
+        value, _, cores, sample = oracle_multistep_chain(40, 20.0)
+        line["cpu_baseline"] = {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "sample": sample}
     print(json.dumps(line, ensure_ascii=False))
 
 
@@ -655,9 +761,9 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.workload == "multistep_k8":
         if args.impl == "reference":
+            # the oracle is host code: rank 0 alone runs it, other ranks exit 0
             if int(os.environ.get("RANK", "0")) == 0:
-                print(json.dumps({"impl": "reference", "unavailable":
-                                  "the oracle arm is timed on the prefill workloads only"}))
+                run_reference_multistep(args)
             return
         world, rank, local = dist_setup()
         run_multistep(args, world, rank, local)

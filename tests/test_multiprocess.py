@@ -65,3 +65,15 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
     assert line["config"]["workload"] == "tiny_f32"
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_multistep_reference_arm_times_the_oracle_chain():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "multistep_k8",
+           "--steps", "2", "--warmup", "3"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600,
+                         env=dict(os.environ, OMP_NUM_THREADS="2"))
+    assert out.returncode == 0, out.stderr[-3000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"]["workload"] == "multistep_k8"
+    assert line["unit"] == "Mtok·heads/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
