@@ -22,6 +22,7 @@
 #include "../../include/ssd.h"
 #include "ssd_kernels.cuh"
 #include "ssd_scan.cuh"
+#include "ssd_scan_hb.cuh"
 #include "ssd_state.cuh"
 #include "ssd_tc.cuh"
 
@@ -43,6 +44,11 @@ struct Plan {
   // workspace of their hand-off (segment final states, decay products)
   int nseg = 1, cps = 0;
   size_t Fseg_off = 0, Lseg_off = 0, Dc_off = 0;
+  // 256-token chunks, 64-wide heads, one (B, C) group: chunk_scan_hb takes
+  // the heads two per MMA and flags (one byte per (b, chunk, head)) those it
+  // leaves to chunk_scan_hl
+  bool hb = false;
+  size_t flags_off = 0;
 };
 
 int num_sms();
@@ -114,6 +120,11 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
       pl->Lseg_off = pl->Fseg_off + align_up(bh * pl->nseg * pl->N * pl->P * sizeof(float));
       pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
       pl->total = pl->Dc_off + align_up(bh * pl->nc * sizeof(float));
+    }
+    pl->hb = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
+    if (pl->hb) {
+      pl->flags_off = pl->total;
+      pl->total += align_up(static_cast<size_t>(pl->b) * pl->nc * pl->H);
     }
   } else {
     pl->cs_off = 0;
@@ -319,7 +330,7 @@ int scan_heads_per_cta(const Plan &pl, int num_sms) {
   const double t_head = 1.0, t_group = shared ? 1.5 : 0.0;
   int best = 1;
   double best_cost = 1e300;
-  for (int hp = 1; hp <= ssd::ScanHL<128, 64>::kMaxHeads && hp <= pl.H; ++hp) {
+  for (int hp = 1; hp <= 16 && hp <= pl.H; ++hp) {
     const int64_t ctas = ((pl.H + hp - 1) / hp) * pl.nc * pl.b;
     const double waves = static_cast<double>((ctas + num_sms - 1) / num_sms);
     const double groups = shared ? 1.0 : static_cast<double>(hp);
@@ -335,18 +346,72 @@ int scan_heads_per_cta(const Plan &pl, int num_sms) {
 template <int Q, int P>
 ssd_status launch_scan_hl(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
-                          const float *dt, const float *A, const float *D, cudaStream_t s) {
+                          const float *dt, const float *A, const float *D,
+                          const uint8_t *only_flagged, cudaStream_t s) {
   using L = ssd::ScanHL<Q, P>;
-  auto k = ssd::chunk_scan_hl<Q, P>;
+  auto k = ssd::chunk_scan_hl<Q, P, false>;
+  static std::once_flag once;
+  static bool ok = false;
+  if constexpr (Q == 256 && P == 64) {  // the only shape with a head-pair kernel before it
+    if (only_flagged) k = ssd::chunk_scan_hl<Q, P, true>;
+    std::call_once(once, [&] {
+      ok = set_smem(ssd::chunk_scan_hl<Q, P, true>, L::kBytes) &&
+           set_smem(ssd::chunk_scan_hl<Q, P, false>, L::kBytes);
+    });
+  } else {
+    if (only_flagged) return SSD_ERR_UNSUPPORTED;
+    std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+  }
+  if (!ok) return SSD_ERR_CUDA;
+  // all heads: the cost model; only the heads a preceding kernel left: about
+  // one CTA per SM, each over a wide head range (most ranges hold few of them)
+  int hpc = scan_heads_per_cta(pl, num_sms());
+  if (only_flagged) {
+    const int64_t bc = pl.b * pl.nc;
+    const int64_t ranges = std::max<int64_t>(1, num_sms() / std::max<int64_t>(bc, 1));
+    hpc = static_cast<int>(std::min<int64_t>((pl.H + ranges - 1) / ranges, L::kMaxFlaggedHeads));
+  }
+  dim3 grid(static_cast<unsigned>((pl.H + hpc - 1) / hpc), pl.nc, static_cast<unsigned>(pl.b));
+  k<<<grid, L::kThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, pl.T,
+                                         static_cast<int>(pl.H), static_cast<int>(pl.GB),
+                                         static_cast<int>(pl.GC), pl.nc, hpc, pl.softplus,
+                                         only_flagged);
+  return launch_status();
+}
+
+// Head pairs per CTA of chunk_scan_hb: the per-CTA C B^T product and mask
+// (~1.75 pairs of work) against wave quantisation.
+int scan_pairs_per_cta(const Plan &pl, int num_sms) {
+  const int64_t pairs = (pl.H + 1) / 2;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int pp = 1; pp <= std::min<int64_t>(pairs, ssd::kHbMaxPairs); ++pp) {
+    const int64_t ctas = ((pairs + pp - 1) / pp) * pl.nc * pl.b;
+    const double waves = static_cast<double>((ctas + num_sms - 1) / num_sms);
+    const double cost = waves * (pp + 1.75);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = pp;
+    }
+  }
+  return best;
+}
+
+ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
+                          const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
+                          const float *dt, const float *A, const float *D, uint8_t *flags,
+                          cudaStream_t s) {
+  using L = ssd::ScanHB;
+  auto k = ssd::chunk_scan_hb;
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
   if (!ok) return SSD_ERR_CUDA;
-  const int hpc = scan_heads_per_cta(pl, num_sms());
-  dim3 grid(static_cast<unsigned>((pl.H + hpc - 1) / hpc), pl.nc, static_cast<unsigned>(pl.b));
-  k<<<grid, L::kThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, pl.T,
-                                         static_cast<int>(pl.H), static_cast<int>(pl.GB),
-                                         static_cast<int>(pl.GC), pl.nc, hpc, pl.softplus);
+  const int pp = scan_pairs_per_cta(pl, num_sms());
+  const int64_t pairs = (pl.H + 1) / 2;
+  dim3 grid(static_cast<unsigned>((pairs + pp - 1) / pp), pl.nc, static_cast<unsigned>(pl.b));
+  k<<<grid, ssd::kHbThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, flags, pl.T,
+                                             static_cast<int>(pl.H), pl.nc, pp, pl.softplus);
   return launch_status();
 }
 
@@ -414,9 +479,20 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     if (st != SSD_OK) return st;
     const int se = pl.nseg > 1 ? 2 : 1;  // events index after the state stages
     record(events, se, s);
-    if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
-    else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
-    else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
+    if (pl.hb) {
+      // head pairs in the scaled form, then the heads it left (long decays)
+      uint8_t *flags = ws + pl.flags_off;
+      st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
+      if (st != SSD_OK) return st;
+      record(events, se + 1, s);
+      st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
+      if (st != SSD_OK) return st;
+      record(events, se + 2, s);
+      return SSD_OK;
+    }
+    if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
+    else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
+    else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
     if (st != SSD_OK) return st;
     record(events, se + 1, s);
     return SSD_OK;
@@ -441,7 +517,12 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
 
 const char *const kStageNamesTc[] = {"chunk_state_pass_tc", "chunk_scan_hl"};
 const char *const kStageNamesTcSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hl"};
-int num_stages(const Plan &pl) { return pl.tc ? (pl.nseg > 1 ? 3 : 2) : 4; }
+const char *const kStageNamesHb[] = {"chunk_state_pass_tc", "chunk_scan_hb", "chunk_scan_hl"};
+const char *const kStageNamesHbSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hb",
+                                        "chunk_scan_hl"};
+int num_stages(const Plan &pl) {
+  return pl.tc ? (pl.nseg > 1 ? 3 : 2) + (pl.hb ? 1 : 0) : 4;
+}
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
 
@@ -495,6 +576,7 @@ const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
   if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= num_stages(pl)) return nullptr;
   if (!pl.tc) return kStageNamesSimt[i];
+  if (pl.hb) return pl.nseg > 1 ? kStageNamesHbSeg[i] : kStageNamesHb[i];
   return pl.nseg > 1 ? kStageNamesTcSeg[i] : kStageNamesTc[i];
 }
 

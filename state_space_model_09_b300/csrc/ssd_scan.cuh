@@ -81,12 +81,15 @@ struct ScanHL {
   static constexpr int kX = P * Q * 2;
   static constexpr int kH = P * N * 2;
   static constexpr int kMaxHeads = 16;            // most heads per CTA
+  static constexpr int kMaxFlaggedHeads = 128;    // ... when computing flagged heads only
   // per-head decay tables, double-buffered: cs*log2e, exp(cs), the factors
   // 2^(a_{j|31} - a_j) and 2^(a_{j&~31} - a_j); plus D of the CTA's heads
   static constexpr int kTables = 4;
-  static constexpr int kFloats = 2 * kTables * Q + kMaxHeads;
+  // + D of the CTA's heads
+  static constexpr int kFloats = 2 * kTables * Q + kMaxFlaggedHeads;
   static constexpr int kBars = 16;
-  static constexpr int kBytes = kC + kU + kX + kH + kFloats * 4 + kBars * 8 + 16 + 1024;
+  static constexpr int kBytes =
+      kC + kU + kX + kH + kFloats * 4 + kBars * 8 + 16 + 4 * (kMaxFlaggedHeads + 2) + 1024;
   static constexpr int kSCols = 128 * MT * (MT + 1) / 2;
   static constexpr int kCols = kSCols + MT * P;
   static constexpr uint32_t kAlloc = kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
@@ -191,15 +194,18 @@ __device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const f
         make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
-template <int Q, int P>
+// FLAGGED: compute only the heads of the range whose byte in only_flagged is
+// 0 (the heads a preceding kernel left); otherwise every head of the range.
+template <int Q, int P, bool FLAGGED = false>
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_hl(const __grid_constant__ CUtensorMap mapC32, const __grid_constant__ CUtensorMap mapB,
                   const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapH,
                   const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
                   const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
-                  int GB, int GC, int nc, int heads_per_cta, int softplus) {
+                  int GB, int GC, int nc, int heads_per_cta, int softplus,
+                  const uint8_t *__restrict__ only_flagged) {
   using L = ScanHL<Q, P>;
-  constexpr int N = L::N, MT = L::MT, KMAX = L::kMaxHeads;
+  constexpr int N = L::N, MT = L::MT, KMAX = FLAGGED ? L::kMaxFlaggedHeads : L::kMaxHeads;
   constexpr int CW = kScanComputeWarps;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -214,15 +220,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(D_s + KMAX);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+  int *hlist = reinterpret_cast<int *>(tslot + 4);  // FLAGGED: the heads this CTA computes
+  int *nh_s = hlist + KMAX;
 
   const int c = blockIdx.y, b = blockIdx.z;
   const int h_begin = blockIdx.x * heads_per_cta;
-  const int nh = min(H, h_begin + heads_per_cta) - h_begin;
+  const int nh_all = min(H, h_begin + heads_per_cta) - h_begin;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg_b = H / GB, hpg_c = H / GC;
+  auto head_at = [&](int k) { return FLAGGED ? hlist[k] : h_begin + k; };
   auto new_group_at = [&](int k) {
-    const int h = h_begin + k;
-    return k == 0 || h / hpg_b != (h - 1) / hpg_b || h / hpg_c != (h - 1) / hpg_c;
+    const int h = head_at(k), hp = FLAGGED ? (k > 0 ? hlist[k - 1] : h) : h - 1;
+    return k == 0 || h / hpg_b != hp / hpg_b || h / hpg_c != hp / hpg_c;
   };
 
   if (tid == 0) {
@@ -234,11 +243,36 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the heads to compute: all of the range, or (FLAGGED) those a preceding
+  // kernel flagged 0, selected in parallel and compacted by thread 0
+  if (FLAGGED) {
+    for (int k = tid; k < nh_all; k += blockDim.x) {
+      hlist[k] = only_flagged[(static_cast<int64_t>(b) * nc + c) * H + h_begin + k] == 0;
+      D_s[k] = D ? D[h_begin + k] : 0.f;
+    }
+  } else if (tid < nh_all) {
+    D_s[tid] = D ? D[h_begin + tid] : 0.f;
+  }
   if (warp == kScanControlWarp) tmem_alloc(tslot, L::kAlloc);
-  if (tid < nh) D_s[tid] = D ? D[h_begin + tid] : 0.f;
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  int nh = nh_all;
+  if (FLAGGED) {
+    if (tid == 0) {
+      int n = 0;
+      for (int k = 0; k < nh_all; ++k) {
+        if (hlist[k]) {
+          hlist[n] = h_begin + k;
+          D_s[n] = D_s[k];
+          ++n;
+        }
+      }
+      *nh_s = n;
+    }
+    __syncthreads();
+    nh = *nh_s;
+  }
   const uint32_t tmem = *tslot;
 
   if (warp == kScanAuxWarp) {
@@ -252,7 +286,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
     for (int k = 0; k <= nh; ++k) {
       if (k < nh) {
-        const int h = h_begin + k, s = k & 1;
+        const int h = head_at(k), s = k & 1;
         float z[PER];
 #pragma unroll
         for (int e = 0; e < PER; ++e)
@@ -298,7 +332,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           if (ok && !*abort_flag) {
 #pragma unroll
             for (int s = 0; s < P / 64; ++s)
-              tma_store_4d(&mapY, Xt + s * Q * 128, 64 * s, h_begin + kp, c * Q, b);
+              tma_store_4d(&mapY, Xt + s * Q * 128, 64 * s, head_at(kp), c * Q, b);
             bulk_commit();
             bulk_wait_read0();
           }
@@ -311,7 +345,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (lane == 0) bulk_wait_all();
   } else if (warp == kScanControlWarp) {
     // ================================================================ control
-    if (lane == 0) {
+    if (lane == 0 && nh > 0) {
       prefetch_tensormap(&mapC32);
       prefetch_tensormap(&mapB);
       prefetch_tensormap(&mapX);
@@ -330,11 +364,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int s = 0; s < P / 64; ++s)
           tma_load_3d(Ht + s * N * 128, &mapH, &bars[kBarH], 64 * s, 0, hrow + hh);
       };
-      load_x(h_begin);
-      load_h(h_begin);
+      load_x(head_at(0));
+      load_h(head_at(0));
       int group = -1;
       for (int k = 0; k < nh && !*abort_flag; ++k) {
-        const int h = h_begin + k;
+        const int h = head_at(k);
         const bool more = k + 1 < nh;
         if (new_group_at(k)) {
           ++group;
@@ -380,7 +414,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         mma_commit(&bars[kBarM3]);
         if (!mbar_wait(&bars[kBarM3], k & 1, abort_flag)) break;
-        if (more) load_h(h + 1);
+        if (more) load_h(head_at(k + 1));
         // MMA2: Y_mt += A2_mt x, the last row tile first (its mask is written first)
         if (!mbar_wait(&bars[kBarX], k & 1, abort_flag)) break;
         bool failed = false;
@@ -407,7 +441,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         // the x tile now holds this head's y until its store has read it
         if (more) {
           if (!mbar_wait(&bars[kBarXFree], k & 1, abort_flag)) break;
-          load_x(h + 1);
+          load_x(head_at(k + 1));
         }
       }
     }

@@ -1,0 +1,470 @@
+// ssd_scan_hb.cuh -- chunk_scan for 256-token chunks, 64-wide heads and one
+// (B, C) group, two heads per MMA.
+//
+// Same result as chunk_scan_hl (ssd_scan.cuh): for one (batch b, chunk c) and
+// each head h, with a = cs * log2(e) the in-chunk inclusive running sum of
+// softplus(dt) * A_h in log2 units and Hin the chunk's true initial state,
+//   y_i = sum_{j <= i} 2^(a_i - a_j) S_ij x_j + 2^(a_i) (C Hin)_i + D_h x_i,   S = C B^T
+// (Mamba-2 page, section "SSD算法": the orange diagonal block in quadratic
+// form and the blue term from the true initial state).
+//
+// Scaled form.  Taking 2^(a_i) out of row i,
+//   y_i = 2^(a_i) [ sum_{j <= i} S_ij (2^(-a_j) x_j) + (C Hin)_i + D_h 2^(-a_i) x_i ],
+// the masked matrix (j <= i) o S no longer depends on the head: it is formed
+// once per CTA and is the A operand of every head's second MMA, while the
+// head's decay rides on its x rows (x_j 2^(-a_j), the B operand).  Two heads
+// share every MMA (N = 2 x 64): C [Hin_h | Hin_h'] and the three masked
+// blocks of S times [x~_h | x~_h'].  No per-head mask, half the MMA
+// instructions of a 64-column head.
+//
+// Range.  The factors 2^(-a_j) are at most 2^(-a_last); a head is taken here
+// when a_last >= -kHbRange, so no factor exceeds 2^96 and sums of |S x| below
+// 2^31 cannot overflow.  A (batch, chunk, head) with a longer decay is flagged
+// (flags[(b nc + c) H + h] = 0, else 1), its y left to chunk_scan_hl, which
+// runs after this kernel on the flagged heads only.
+//
+// Tensor memory (512 columns): the masked S blocks as packed bf16 pairs --
+// rows 0-127 x columns 0-127 ("b00"), rows 128-255 x columns 0-127 ("b10",
+// nothing masked), rows 128-255 x columns 128-255 ("b11") -- then C (the A
+// operand of the C Hin product), 64 columns per 128-row tile, then Y of one
+// row tile for the two heads (128 columns, also the f32 scratch of each S
+// piece while the blocks are built).  Shared memory: two 64 KB buffers (C and
+// the B tile while S is built; then each head pair's scaled x, then its y for
+// the TMA stores) and two Hin pair buffers.  A pair's tile 1 (rows 128-255)
+// is computed and read out first; while tile 0's MMAs run, the compute warps
+// scale the next pair's x, which was loaded a pair earlier.
+//
+// Warp roles: warps 0-15 build the S blocks, copy C, scale x and write y
+// (four per TMEM lane quarter); warp 16 (one lane) issues the C/B/Hin and the
+// first x loads and every MMA; warp 17 computes each pair's decay tables up
+// to two pairs ahead, fetching the next pair's dt while it works; warp 18
+// (one lane) stores each pair's y and loads the x two pairs ahead.  Every
+// wait is bounded in time.
+#pragma once
+
+#include "ssd_scan.cuh"
+
+namespace ssd {
+
+constexpr float kHbRange = 96.f;  // log2 units
+constexpr int kHbStoreWarp = kScanComputeWarps + 2;
+constexpr int kHbThreads = 32 * (kScanComputeWarps + 3);
+constexpr int kHbMaxPairs = 64;  // head pairs per CTA
+
+struct ScanHB {
+  static constexpr int Q = 256, P = 64, N = kTcN;
+  static constexpr int kXS = 2 * P * Q * 2;  // one buffer: C or B tile, or a scaled x / y pair
+  static constexpr int kH = 2 * P * N * 2;   // one Hin pair
+  static_assert(kXS == N * Q * 2, "the C and B tiles fill an x buffer");
+  static constexpr int kTab = 2 * 2 * Q;     // per buffer: [head][t = 2^-a, e = 2^a][Q]
+  // + D and mode of the pair, per buffer; + one mode byte per head of the CTA
+  static constexpr int kFloats = 2 * kTab + 8 + 2 * kHbMaxPairs / 4;
+  static constexpr int kBars = 24;
+  static constexpr int kBytes = 2 * kXS + 2 * kH + kFloats * 4 + kBars * 8 + 16 + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kA00 = 0, kA10 = 64, kA11 = 128;  // masked S blocks (packed)
+  static constexpr uint32_t kC0 = 192, kC1 = 256;             // C row tiles (packed)
+  static constexpr uint32_t kY = 320;                         // Y of one row tile, 2 heads
+  static constexpr uint32_t kAlloc = 512;
+  static_assert(kY + 2 * P <= kAlloc, "TMEM map");
+  static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+
+enum : int {
+  kHbCB = 0, kHbS, kHbConv, kHbX0, kHbX1, kHbH0, kHbH1, kHbXScaled, kHbM2, kHbYFree,
+  kHbYStaged, kHbTabFull0, kHbTabFull1, kHbTabEmpty0, kHbTabEmpty1, kNumHbBars
+};
+static_assert(kNumHbBars <= ScanHB::kBars, "barrier slots");
+
+__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 "
+      "[%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, f32 accumulation.  One thread.
+// A is M x K with row m in TMEM lane m and K packed two bf16 per column
+// (the lower half holds the even element).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 f32 columns of S for the calling thread's row -> 16 packed bf16 pairs,
+// column j kept when j <= lim (pass lim >= 31 to keep every column).
+__device__ __forceinline__ void hb_mask_pack(const float (&v)[32], int lim, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pk[e] = pack_bf16x2(2 * e <= lim ? v[2 * e] : 0.f, 2 * e + 1 <= lim ? v[2 * e + 1] : 0.f);
+}
+
+__global__ void __launch_bounds__(kHbThreads, 1)
+    chunk_scan_hb(const __grid_constant__ CUtensorMap mapC32,
+                  const __grid_constant__ CUtensorMap mapB,
+                  const __grid_constant__ CUtensorMap mapX,
+                  const __grid_constant__ CUtensorMap mapH,
+                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                  const float *__restrict__ A, const float *__restrict__ D,
+                  uint8_t *__restrict__ flags, int64_t T, int H, int nc, int pairs_per_cta,
+                  int softplus) {
+  using L = ScanHB;
+  constexpr int Q = L::Q, P = L::P, N = L::N;
+  constexpr int CW = kScanComputeWarps;
+  constexpr float kLog2e = 1.4426950408889634f;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *Xs = smem;                // two buffers, each [head][Q rows][128 B]
+  uint8_t *Hb = Xs + 2 * L::kXS;     // two Hin pair buffers, each [head][N rows][128 B]
+  // tab[buf][head][0] = 2^-a_j (0 for a head left to chunk_scan_hl), [1] = 2^a_j
+  float *tab = reinterpret_cast<float *>(Hb + 2 * L::kH);
+  float *misc = tab + 2 * L::kTab;  // [buf][4]: D of the two heads, their modes
+  uint8_t *modes = reinterpret_cast<uint8_t *>(misc + 8);  // [pair][head]: 1 = y written here
+  uint64_t *bars = reinterpret_cast<uint64_t *>(modes + 2 * kHbMaxPairs);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
+
+  const int c = blockIdx.y, b = blockIdx.z;
+  const int h_begin = blockIdx.x * 2 * pairs_per_cta;
+  const int h_end = min(H, h_begin + 2 * pairs_per_cta);
+  const int npairs = (h_end - h_begin + 1) / 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < L::kBars; ++i) {
+      const bool per_warp = i == kHbConv || i == kHbXScaled || i == kHbYFree ||
+                            i == kHbYStaged || i == kHbTabEmpty0 || i == kHbTabEmpty1;
+      mbar_init(&bars[i], per_warp ? CW : 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kScanControlWarp) tmem_alloc(tslot, L::kAlloc);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tslot;
+  auto nheads_of = [&](int pr) { return min(2, h_end - (h_begin + 2 * pr)); };
+  // x of pair pr into buffer pr & 1 (issued by one thread)
+  auto load_x = [&](int pr) {
+    const int n = nheads_of(pr);
+    uint64_t *bar = &bars[kHbX0 + (pr & 1)];
+    mbar_arrive_expect_tx(bar, n * P * Q * 2);
+    for (int hh = 0; hh < n; ++hh)
+      tma_load_4d(Xs + (pr & 1) * L::kXS + hh * Q * 128, &mapX, bar, 0, h_begin + 2 * pr + hh,
+                  c * Q, b);
+  };
+
+  if (warp == kScanAuxWarp) {
+    // ================================================================ tables
+    // Tables of pair pr into buffer pr & 1 (lane owns Q/32 consecutive
+    // tokens; running sum, then a warp scan).  The next pair's dt, A and D
+    // are fetched before this pair's buffer is waited for.
+    constexpr int PER = Q / 32;
+    const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
+    float z[2][PER], zn[2][PER], Ap[2], An[2], Dp[2], Dn[2];
+    auto fetch = [&](int pr, float (&zz)[2][PER], float (&aa)[2], float (&dd)[2]) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = min(h_begin + 2 * pr + hh, H - 1);
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          zz[hh][e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
+        aa[hh] = A[h];
+        dd[hh] = D ? D[h] : 0.f;
+      }
+    };
+    if (npairs > 0) fetch(0, zn, An, Dn);
+    for (int pr = 0; pr < npairs; ++pr) {
+      const int s = pr & 1, n = nheads_of(pr);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        Ap[hh] = An[hh];
+        Dp[hh] = Dn[hh];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) z[hh][e] = zn[hh][e];
+      }
+      if (pr + 1 < npairs) fetch(pr + 1, zn, An, Dn);
+      if (pr >= 2 && !mbar_wait(&bars[kHbTabEmpty0 + s], ((pr - 2) >> 1) & 1, abort_flag)) break;
+      float *tb = tab + s * L::kTab;
+      for (int hh = 0; hh < n; ++hh) {
+        const int h = h_begin + 2 * pr + hh;
+        float v[PER];
+        float run = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          if (t0 + e < T) run += (softplus ? softplus_f32(z[hh][e]) : z[hh][e]) * Ap[hh];
+          v[e] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        const float base = incl - run;
+        const float a_last = __shfl_sync(0xffffffffu, (v[PER - 1] + base) * kLog2e, 31);
+        const int fast = a_last >= -kHbRange;
+        float *tt = tb + hh * 2 * Q;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          const float av = (v[e] + base) * kLog2e;
+          tt[lane * PER + e] = fast ? ex2_approx(-av) : 0.f;
+          tt[Q + lane * PER + e] = ex2_approx(av);
+        }
+        if (lane == 0) {
+          misc[4 * s + hh] = Dp[hh];
+          misc[4 * s + 2 + hh] = fast ? 1.f : 0.f;
+          modes[2 * pr + hh] = static_cast<uint8_t>(fast);
+          flags[(static_cast<int64_t>(b) * nc + c) * H + h] = static_cast<uint8_t>(fast);
+        }
+      }
+      if (n < 2 && lane == 0) {
+        misc[4 * s + 3] = 0.f;
+        modes[2 * pr + 1] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kHbTabFull0 + s]);
+    }
+  } else if (warp == kHbStoreWarp) {
+    // ================================================================ y out, x in
+    if (lane == 0) {
+      for (int pr = 0; pr < npairs; ++pr) {
+        if (!mbar_wait(&bars[kHbYStaged], pr & 1, abort_flag) || *abort_flag) break;
+        uint8_t *xb = Xs + (pr & 1) * L::kXS;
+        for (int hh = 0; hh < nheads_of(pr); ++hh)
+          if (modes[2 * pr + hh])
+            tma_store_4d(&mapY, xb + hh * Q * 128, 0, h_begin + 2 * pr + hh, c * Q, b);
+        bulk_commit();
+        bulk_wait_read0();
+        if (pr + 2 < npairs) load_x(pr + 2);  // the buffer is free again
+      }
+      bulk_wait_all();
+    }
+    __syncwarp();
+  } else if (warp == kScanControlWarp) {
+    // ================================================================ control
+    if (lane == 0 && npairs > 0) {
+      prefetch_tensormap(&mapC32);
+      prefetch_tensormap(&mapB);
+      prefetch_tensormap(&mapH);
+      prefetch_tensormap(&mapX);
+      prefetch_tensormap(&mapY);
+      const uint32_t xs = smem_u32(Xs), hb = smem_u32(Hb);
+      const int hrow = (b * nc + c) * H;
+      auto load_h = [&](int pr) {
+        const int n = nheads_of(pr);
+        uint64_t *bar = &bars[kHbH0 + (pr & 1)];
+        mbar_arrive_expect_tx(bar, n * P * N * 2);
+        for (int hh = 0; hh < n; ++hh)
+          tma_load_3d(Hb + (pr & 1) * L::kH + hh * N * 128, &mapH, bar, 0, 0,
+                      hrow + h_begin + 2 * pr + hh);
+      };
+      // C into buffer 0, B into buffer 1 (one group: group index 0)
+      mbar_arrive_expect_tx(&bars[kHbCB], 2 * L::kXS);
+#pragma unroll
+      for (int s = 0; s < N / 64; ++s) {
+#pragma unroll
+        for (int rb = 0; rb < Q / 32; ++rb)
+          tma_load_4d(Xs + s * Q * 128 + rb * 32 * 128, &mapC32, &bars[kHbCB], 64 * s, 0,
+                      c * Q + 32 * rb, b);
+        tma_load_4d(Xs + L::kXS + s * Q * 128, &mapB, &bars[kHbCB], 64 * s, 0, c * Q, b);
+      }
+      load_h(0);
+      if (npairs > 1) load_h(1);
+      bool ok = mbar_wait(&bars[kHbCB], 0, abort_flag);
+      // three S pieces (C0 B0^T, C1 B0^T, C1 B1^T) through the Y columns, each
+      // packed by the compute warps before the next
+      for (int p = 0; p < 3 && ok; ++p) {
+        tc_fence_after_sync();
+        const uint32_t arow = p == 0 ? 0u : 128u * 128u, brow = p == 2 ? 128u * 128u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks) {
+          const uint32_t koff = (ks >> 2) * Q * 128 + (ks & 3) * 32;
+          mma_bf16(tmem + L::kY, sdesc_sw128(xs + koff + arow, 16, 1024),
+                   sdesc_sw128(xs + L::kXS + koff + brow, 16, 1024),
+                   idesc_bf16(128, 128, false, false), ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[kHbS]);
+        ok = mbar_wait(&bars[kHbConv], p & 1, abort_flag);
+      }
+      // C and B are consumed: both buffers take x
+      if (ok) {
+        load_x(0);
+        if (npairs > 1) load_x(1);
+      }
+      constexpr uint32_t idesc_y = idesc_bf16(128, 2 * P, false, true);
+      for (int pr = 0; pr < npairs && ok && !*abort_flag; ++pr) {
+        const uint32_t hk = hb + (pr & 1) * L::kH, xk = xs + (pr & 1) * L::kXS;
+        if (!mbar_wait(&bars[kHbH0 + (pr & 1)], (pr >> 1) & 1, abort_flag)) break;
+        // ---- row tile 1: Y = C1 [Hin | Hin'] + b10 x~[0:128] + b11 x~[128:256]
+        if (pr > 0 && !mbar_wait(&bars[kHbYFree], 1, abort_flag)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks)
+          mma_bf16_tmem_a(tmem + L::kY, tmem + L::kC1 + 8 * ks,
+                          sdesc_sw128(hk + ks * 2048, N * 128, 1024), idesc_y, ks > 0 ? 1u : 0u);
+        if (!mbar_wait(&bars[kHbXScaled], pr & 1, abort_flag)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_tmem_a(tmem + L::kY, tmem + L::kA10 + 8 * ks,
+                          sdesc_sw128(xk + ks * 2048, Q * 128, 1024), idesc_y, 1u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_tmem_a(tmem + L::kY, tmem + L::kA11 + 8 * ks,
+                          sdesc_sw128(xk + 128 * 128 + ks * 2048, Q * 128, 1024), idesc_y, 1u);
+        mma_commit(&bars[kHbM2]);
+        // ---- row tile 0: Y = C0 [Hin | Hin'] + b00 x~[0:128]
+        if (!mbar_wait(&bars[kHbYFree], 0, abort_flag)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks)
+          mma_bf16_tmem_a(tmem + L::kY, tmem + L::kC0 + 8 * ks,
+                          sdesc_sw128(hk + ks * 2048, N * 128, 1024), idesc_y, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16_tmem_a(tmem + L::kY, tmem + L::kA00 + 8 * ks,
+                          sdesc_sw128(xk + ks * 2048, Q * 128, 1024), idesc_y, 1u);
+        mma_commit(&bars[kHbM2]);
+        // the Hin buffer takes pair pr + 2 once these MMAs are done
+        if (pr + 2 < npairs) {
+          if (!mbar_wait(&bars[kHbM2], 1, abort_flag)) break;
+          load_h(pr + 2);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (npairs > 0) {
+    // ================================================================ compute
+    const int q = warp & 3, hs = warp >> 2;  // TMEM lane quarter, sub-warp of the quarter
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const int r = 32 * q + lane;  // row inside a row tile (= TMEM lane)
+    bool ok = true;
+    // ---- S pieces -> masked, packed blocks; C -> tensor memory
+    for (int p = 0; p < 3 && ok; ++p) {
+      // (the C copy below reads the TMA-written tile: wait on its barrier too)
+      bool w = (p > 0 || mbar_wait(&bars[kHbCB], 0, abort_flag)) &&
+               mbar_wait(&bars[kHbS], p & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, w) && !*abort_flag;
+      if (ok) {
+        tc_fence_after_sync();
+        float v[32];
+        uint32_t pk[16];
+        tmem_ld32(tmem + lane_base + L::kY + 32 * hs, v);
+        hb_mask_pack(v, p == 1 ? 31 : r - 32 * hs, pk);
+        tmem_st16_u32(tmem + lane_base + (p == 0 ? L::kA00 : p == 1 ? L::kA10 : L::kA11) + 16 * hs,
+                      pk);
+        if (p == 0) {
+          // C row tiles: row 128 t + r, state columns 32 hs .. + 31 (atom hs / 2)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t cw[16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const uint4 u = *reinterpret_cast<const uint4 *>(
+                  Xs + (hs >> 1) * Q * 128 + sw128_offset(128 * t + r, 32 * (hs & 1) + 8 * g));
+              cw[4 * g] = u.x; cw[4 * g + 1] = u.y; cw[4 * g + 2] = u.z; cw[4 * g + 3] = u.w;
+            }
+            tmem_st16_u32(tmem + lane_base + (t == 0 ? L::kC0 : L::kC1) + 16 * hs, cw);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kHbConv]);
+    }
+    // x rows of pair pr *= 2^-a_j in place (16-byte chunks, eight per thread);
+    // returns the pair's row factors, D and modes, then frees its tables
+    float e[2][2], Dh[2], on[2];
+    auto scale = [&](int pr) -> bool {
+      const int s = pr & 1;
+      bool w = mbar_wait(&bars[kHbTabFull0 + s], (pr >> 1) & 1, abort_flag);
+      w = w && mbar_wait(&bars[kHbX0 + s], (pr >> 1) & 1, abort_flag);
+      if (!(__all_sync(0xffffffffu, w) && !*abort_flag)) return false;
+      const float *tb = tab + s * L::kTab;
+      uint8_t *xb = Xs + s * L::kXS;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int u = tid + 512 * m;
+        const int hh = u >> 11, j = (u >> 3) & 255, cc = u & 7;
+        uint4 *p = reinterpret_cast<uint4 *>(xb + hh * Q * 128 + sw128_offset(j, 8 * cc));
+        *p = scale_bf16x8(*p, tb[hh * 2 * Q + j]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kHbXScaled]);
+      const float *md = misc + 4 * s;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        e[hh][0] = tb[hh * 2 * Q + Q + r];
+        e[hh][1] = tb[hh * 2 * Q + Q + 128 + r];
+        Dh[hh] = md[hh];
+        on[hh] = md[2 + hh];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kHbTabEmpty0 + s]);
+      return true;
+    };
+    // y rows of row tile t of pair pr = 2^a_i (Y + D x~) -> bf16, in place of x~
+    auto output = [&](int pr, int t, const float (&ee)[2][2], const float (&dd)[2],
+                      const float (&oo)[2]) -> bool {
+      bool w = mbar_wait(&bars[kHbM2], t == 1 ? 0 : 1, abort_flag);
+      if (!(__all_sync(0xffffffffu, w) && !*abort_flag)) return false;
+      tc_fence_after_sync();
+      uint8_t *xb = Xs + (pr & 1) * L::kXS;
+      const int i = 128 * t + r;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (oo[hh] == 0.f) continue;
+        float v[16];
+        tmem_ld16(tmem + lane_base + L::kY + 64 * hh + 16 * hs, v);
+        const float f = ee[hh][t], d = dd[hh];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint4 *p = reinterpret_cast<uint4 *>(xb + hh * Q * 128 + sw128_offset(i, 16 * hs + 8 * g));
+          const uint4 xv = *p;
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 xf = unpack_bf16x2(xw[k]);
+            o[k] = pack_bf16x2(f * fmaf(d, xf.x, v[8 * g + 2 * k]),
+                               f * fmaf(d, xf.y, v[8 * g + 2 * k + 1]));
+          }
+          *p = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      tc_fence_before_sync();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kHbYFree]);
+        if (t == 0) mbar_arrive(&bars[kHbYStaged]);
+      }
+      return true;
+    };
+    if (ok) ok = scale(0);
+    for (int pr = 0; pr < npairs && ok; ++pr) {
+      float ce[2][2] = {{e[0][0], e[0][1]}, {e[1][0], e[1][1]}};
+      float cd[2] = {Dh[0], Dh[1]}, co[2] = {on[0], on[1]};
+      if (!(ok = output(pr, 1, ce, cd, co))) break;
+      if (pr + 1 < npairs && !(ok = scale(pr + 1))) break;
+      if (!(ok = output(pr, 0, ce, cd, co))) break;
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kScanControlWarp) tmem_dealloc(tmem, L::kAlloc);
+}
+
+}  // namespace ssd

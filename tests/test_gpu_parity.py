@@ -115,6 +115,30 @@ def test_fwd_small(name):
     check_fwd(shape, seed)
 
 
+@pytest.mark.parametrize("a_scale", [
+    (30.0, 1.0, 30.0, 1.0, 1.0),     # heads 0 and 2 decay past the scaled form's range
+    (30.0, 30.0, 30.0, 30.0, 30.0),  # every head does
+    (0.01, 0.01, 0.01, 0.01, 0.01),  # none does
+])
+def test_fwd_q256_long_decay_heads(a_scale):
+    """256-token chunks of one group: heads whose in-chunk decay exceeds the
+    scaled form's range are left by the head-pair kernel to chunk_scan_hl;
+    either way every head's y and state match the oracle (odd head count, so
+    one pair has a single head; ragged last chunk; random h0)."""
+    shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
+    inp = synth.make_fwd_inputs(shape, 41)
+    inp["A"] = (inp["A"] * np.asarray(a_scale, dtype=np.float32)).astype(np.float32)
+    d = to_dev(inp, shape.io)
+    y, hf = run_fwd(d, shape.chunk)
+    pairs = list(range(shape.batch * shape.nheads))
+    y_ref, h_ref = oracle.ssd_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["h0"], pairs=pairs)
+    ey = rel_err(y_pairs(y, pairs, shape.nheads), y_ref)
+    eh = rel_err(h_pairs(hf, pairs, shape.nheads), h_ref)
+    assert np.isfinite(ey) and ey <= TOL[synth.BF16], ey
+    assert np.isfinite(eh) and eh <= TOL[synth.BF16], eh
+
+
 def test_fwd_tc_without_softplus_and_D():
     check_fwd(F(1, 300, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 41, dt_softplus=False,
               D_none=True)
@@ -127,7 +151,9 @@ def test_fwd_f32_without_softplus_and_D():
 
 def test_fwd_stage_path_matches_dtype():
     d = S.make_dims(8, 2048, 80, 64, 128)
-    assert S.ssd_fwd_stage_name(d, 256, 1) == "chunk_scan_hl"
+    assert S.ssd_fwd_stage_name(d, 256, 1) == "chunk_scan_hb"
+    assert S.ssd_fwd_stage_name(d, 256, 2) == "chunk_scan_hl"
+    assert S.ssd_fwd_stage_name(d, 128, 1) == "chunk_scan_hl"
 
 
 # ---------------------------------------------------------------- full sizes
