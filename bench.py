@@ -82,9 +82,9 @@ def peaks():
 # ----------------------------------------------------------------------------- work model
 def hb_fast_fraction(s: synth.FwdShape, inp) -> float:
     """Share of (batch, chunk, head) units whose in-chunk decay stays within the
-    range of the head-pair chunk-scan kernel (log2 of the chunk's total decay
-    >= -96); the rest go through the per-head kernel.  Recomputed here in
-    float64 for the byte accounting only."""
+    range of the head-pair form of the chunk scan (log2 of the chunk's total
+    decay >= -96); the rest are computed one by one.  Recomputed here in
+    float64, for the report only."""
     dt = inp["dt"].astype(np.float64)
     sp = np.where(dt > 20.0, dt, np.log1p(np.exp(np.minimum(dt, 20.0))))
     dA = sp * inp["A"].astype(np.float64)[None, None, :] / math.log(2.0)
@@ -96,17 +96,14 @@ def hb_fast_fraction(s: synth.FwdShape, inp) -> float:
     return float(np.mean(last >= -96.0))
 
 
-def fwd_work(s: synth.FwdShape, fast_frac=None):
+def fwd_work(s: synth.FwdShape):
     """Algorithmic bytes / flops of the layer and of each stage (per call).
 
     Layer (mandatory I/O): x, y, B, C (io dtype), dt (f32), h0 if given,
     h_final (f32).  Flops count causal work only: P*Q(Q+1) (masked scores times
     x), 2QNP (chunk state), 2QNP (output from the initial state) per
     (b, chunk, head), plus N*Q(Q+1) per (b, chunk, distinct B/C group pair) for
-    C B^T.  Stage bytes count each stage's own inputs and outputs once.  With
-    fast_frac (the head-pair chunk-scan kernel's share of the (b, chunk, head)
-    units), chunk_scan_hb reads every head's x, chunk state and dt and writes
-    that share of y; chunk_scan_hl then reads and writes the rest."""
+    C B^T.  Stage bytes count each stage's own inputs and outputs once."""
     io = 2 if s.io == synth.BF16 else 4
     b, T, H, P, N, Q = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.chunk
     nc = math.ceil(T / Q)
@@ -133,11 +130,8 @@ def fwd_work(s: synth.FwdShape, fast_frac=None):
         "state_passing": (S32 + b * H * nc * 4 + h0 + S32 + st, 2 * b * nc * H * N * P),
         "chunk_scan_simt": (x + Bb + Cb + cs + S32 + x, f_scan),
     }
-    if fast_frac is not None:
-        f = fast_frac
-        stages["chunk_scan_hb"] = (int(x + hin16 + dt + Bb + Cb + f * x), int(f * f_scan))
-        stages["chunk_scan_hl"] = (int((1 - f) * (2 * x + hin16 + dt) + Bb + Cb),
-                                   int((1 - f) * f_scan))
+    # one launch computes every head (two per MMA, or one by one when flagged)
+    stages["chunk_scan_hb"] = stages["chunk_scan_hl"]
     return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 
@@ -401,8 +395,7 @@ def run_ours(args, shape, work, world, rank, local):
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     names = [S.ssd_fwd_stage_name(dims, shape.chunk, i) for i in range(S.ssd_fwd_num_stages(dims, shape.chunk))]
-    if "chunk_scan_hb" in names:
-        work = fwd_work(shape, hb_fast_fraction(shape, inp))
+    pair_share = hb_fast_fraction(shape, inp) if "chunk_scan_hb" in names else None
 
     # Inputs smaller than twice the L2 are rotated over enough device copies
     # that every timed step reads data the previous steps have evicted.
@@ -528,7 +521,8 @@ def run_ours(args, shape, work, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
-        "config": config_of(args, shape, "gpu"),
+        "config": dict(config_of(args, shape, "gpu"),
+                       **({"pair_form_share": round(pair_share, 4)} if pair_share is not None else {})),
         "roofline": roof,
         "layer_roofline": {"bytes": work["layer_bytes"], "flops": work["flops"],
                            "t_bound_us": round(max(t_hbm, t_tc) * 1e6, 2),

@@ -44,9 +44,10 @@ struct Plan {
   // workspace of their hand-off (segment final states, decay products)
   int nseg = 1, cps = 0;
   size_t Fseg_off = 0, Lseg_off = 0, Dc_off = 0;
-  // 256-token chunks, 64-wide heads, one (B, C) group: chunk_scan_hb takes
-  // the heads two per MMA and flags (one byte per (b, chunk, head)) those it
-  // leaves to chunk_scan_hl
+  // 256-token chunks, 64-wide heads, one (B, C) group: the chunk-state kernel
+  // records per (b, chunk, head) whether the chunk's decay allows the
+  // head-pair form (one byte each), and chunk_scan_hb computes the heads two
+  // per MMA or, flagged, one by one
   bool hb = false;
   size_t flags_off = 0;
 };
@@ -261,7 +262,7 @@ template <int Q>
 ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
                              const float *dt, const float *A, const float *h0, __nv_bfloat16 *Hin,
                              float *h_final, float *Fseg, float *Lseg, float *Dc,
-                             void *const *events, cudaStream_t s) {
+                             uint8_t *flags, void *const *events, cudaStream_t s) {
   using L = ssd::StatePass<Q>;
   auto k = ssd::chunk_state_pass_tc<Q>;
   static std::once_flag once;
@@ -273,7 +274,7 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
                                          static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
                                          static_cast<int>(pl.P), pl.softplus, pl.nseg, pl.cps,
-                                         Fseg, Lseg, Dc);
+                                         Fseg, Lseg, Dc, flags);
   if (launch_status() != SSD_OK || pl.nseg == 1) return launch_status();
   record(events, 1, s);
   const int NP = static_cast<int>(pl.N * pl.P);
@@ -346,36 +347,18 @@ int scan_heads_per_cta(const Plan &pl, int num_sms) {
 template <int Q, int P>
 ssd_status launch_scan_hl(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
-                          const float *dt, const float *A, const float *D,
-                          const uint8_t *only_flagged, cudaStream_t s) {
+                          const float *dt, const float *A, const float *D, cudaStream_t s) {
   using L = ssd::ScanHL<Q, P>;
-  auto k = ssd::chunk_scan_hl<Q, P, false>;
+  auto k = ssd::chunk_scan_hl<Q, P>;
   static std::once_flag once;
   static bool ok = false;
-  if constexpr (Q == 256 && P == 64) {  // the only shape with a head-pair kernel before it
-    if (only_flagged) k = ssd::chunk_scan_hl<Q, P, true>;
-    std::call_once(once, [&] {
-      ok = set_smem(ssd::chunk_scan_hl<Q, P, true>, L::kBytes) &&
-           set_smem(ssd::chunk_scan_hl<Q, P, false>, L::kBytes);
-    });
-  } else {
-    if (only_flagged) return SSD_ERR_UNSUPPORTED;
-    std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
-  }
+  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
   if (!ok) return SSD_ERR_CUDA;
-  // all heads: the cost model; only the heads a preceding kernel left: about
-  // one CTA per SM, each over a wide head range (most ranges hold few of them)
-  int hpc = scan_heads_per_cta(pl, num_sms());
-  if (only_flagged) {
-    const int64_t bc = pl.b * pl.nc;
-    const int64_t ranges = std::max<int64_t>(1, num_sms() / std::max<int64_t>(bc, 1));
-    hpc = static_cast<int>(std::min<int64_t>((pl.H + ranges - 1) / ranges, L::kMaxFlaggedHeads));
-  }
+  const int hpc = scan_heads_per_cta(pl, num_sms());
   dim3 grid(static_cast<unsigned>((pl.H + hpc - 1) / hpc), pl.nc, static_cast<unsigned>(pl.b));
   k<<<grid, L::kThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, pl.T,
                                          static_cast<int>(pl.H), static_cast<int>(pl.GB),
-                                         static_cast<int>(pl.GC), pl.nc, hpc, pl.softplus,
-                                         only_flagged);
+                                         static_cast<int>(pl.GC), pl.nc, hpc, pl.softplus);
   return launch_status();
 }
 
@@ -397,21 +380,31 @@ int scan_pairs_per_cta(const Plan &pl, int num_sms) {
   return best;
 }
 
+// Head ranges of the flagged-head items of chunk_scan_hb's launch: each item
+// scans a range of heads for the few the chunk-state kernel flagged, so an
+// item is cheap when its range holds none.
+constexpr int kFlaggedRanges = 4;
+
 ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
-                          const float *dt, const float *A, const float *D, uint8_t *flags,
+                          const float *dt, const float *A, const float *D, const uint8_t *flags,
                           cudaStream_t s) {
-  using L = ssd::ScanHB;
   auto k = ssd::chunk_scan_hb;
   static std::once_flag once;
   static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+  std::call_once(once, [&] { ok = set_smem(k, ssd::kHbLaunchBytes); });
   if (!ok) return SSD_ERR_CUDA;
   const int pp = scan_pairs_per_cta(pl, num_sms());
   const int64_t pairs = (pl.H + 1) / 2;
-  dim3 grid(static_cast<unsigned>((pairs + pp - 1) / pp), pl.nc, static_cast<unsigned>(pl.b));
-  k<<<grid, ssd::kHbThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, flags, pl.T,
-                                             static_cast<int>(pl.H), pl.nc, pp, pl.softplus);
+  const int hb_ranges = static_cast<int>((pairs + pp - 1) / pp);
+  const int64_t hpf = std::min<int64_t>((pl.H + kFlaggedRanges - 1) / kFlaggedRanges,
+                                        ssd::ScanHL<256, 64>::kMaxFlaggedHeads);
+  const int flagged_ranges = static_cast<int>((pl.H + hpf - 1) / hpf);
+  const int64_t blocks = (static_cast<int64_t>(hb_ranges) + flagged_ranges) * pl.nc * pl.b;
+  if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
+  k<<<static_cast<unsigned>(blocks), ssd::kHbThreads, ssd::kHbLaunchBytes, s>>>(
+      mC32, mB, mX, mH, mY, dt, A, D, flags, pl.T, static_cast<int>(pl.b), static_cast<int>(pl.H),
+      pl.nc, pp, hb_ranges, static_cast<int>(hpf), flagged_ranges, pl.softplus);
   return launch_status();
 }
 
@@ -474,25 +467,16 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
     float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
     float *Dc = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Dc_off) : nullptr;
-    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, events, s)
-                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, events, s);
+    uint8_t *flags = pl.hb ? ws + pl.flags_off : nullptr;
+    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s)
+                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s);
     if (st != SSD_OK) return st;
     const int se = pl.nseg > 1 ? 2 : 1;  // events index after the state stages
     record(events, se, s);
-    if (pl.hb) {
-      // head pairs in the scaled form, then the heads it left (long decays)
-      uint8_t *flags = ws + pl.flags_off;
-      st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
-      if (st != SSD_OK) return st;
-      record(events, se + 1, s);
-      st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
-      if (st != SSD_OK) return st;
-      record(events, se + 2, s);
-      return SSD_OK;
-    }
-    if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
-    else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
-    else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, nullptr, s);
+    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
+    else if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
+    else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
+    else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     if (st != SSD_OK) return st;
     record(events, se + 1, s);
     return SSD_OK;
@@ -517,12 +501,9 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
 
 const char *const kStageNamesTc[] = {"chunk_state_pass_tc", "chunk_scan_hl"};
 const char *const kStageNamesTcSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hl"};
-const char *const kStageNamesHb[] = {"chunk_state_pass_tc", "chunk_scan_hb", "chunk_scan_hl"};
-const char *const kStageNamesHbSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hb",
-                                        "chunk_scan_hl"};
-int num_stages(const Plan &pl) {
-  return pl.tc ? (pl.nseg > 1 ? 3 : 2) + (pl.hb ? 1 : 0) : 4;
-}
+const char *const kStageNamesHb[] = {"chunk_state_pass_tc", "chunk_scan_hb"};
+const char *const kStageNamesHbSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hb"};
+int num_stages(const Plan &pl) { return pl.tc ? (pl.nseg > 1 ? 3 : 2) : 4; }
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
 

@@ -194,16 +194,17 @@ __device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const f
         make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
-// FLAGGED: compute only the heads of the range whose byte in only_flagged is
-// 0 (the heads a preceding kernel left); otherwise every head of the range.
-template <int Q, int P, bool FLAGGED = false>
-__global__ void __launch_bounds__(kScanThreads, 1)
-    chunk_scan_hl(const __grid_constant__ CUtensorMap mapC32, const __grid_constant__ CUtensorMap mapB,
-                  const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapH,
-                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
-                  const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
-                  int GB, int GC, int nc, int heads_per_cta, int softplus,
-                  const uint8_t *__restrict__ only_flagged) {
+// The body of one CTA: head range bx of chunk c of batch row b.  FLAGGED:
+// compute only the heads of the range whose byte in only_flagged is 0 (the
+// heads left by the head-pair kernel); otherwise every head of the range.
+// Warps 0-17 take part (warps past them, in a wider launch, only wait).
+template <int Q, int P, bool FLAGGED>
+__device__ __forceinline__ void scan_hl_body(
+    int bx, int c, int b, const CUtensorMap &mapC32, const CUtensorMap &mapB,
+    const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY,
+    const float *__restrict__ dt, const float *__restrict__ A, const float *__restrict__ D,
+    int64_t T, int H, int GB, int GC, int nc, int heads_per_cta, int softplus,
+    const uint8_t *__restrict__ only_flagged) {
   using L = ScanHL<Q, P>;
   constexpr int N = L::N, MT = L::MT, KMAX = FLAGGED ? L::kMaxFlaggedHeads : L::kMaxHeads;
   constexpr int CW = kScanComputeWarps;
@@ -223,8 +224,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   int *hlist = reinterpret_cast<int *>(tslot + 4);  // FLAGGED: the heads this CTA computes
   int *nh_s = hlist + KMAX;
 
-  const int c = blockIdx.y, b = blockIdx.z;
-  const int h_begin = blockIdx.x * heads_per_cta;
+  const int h_begin = bx * heads_per_cta;
   const int nh_all = min(H, h_begin + heads_per_cta) - h_begin;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg_b = H / GB, hpg_c = H / GC;
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < CW) {
     // ================================================================ compute
     const int q = warp & 3, hs = warp >> 2;  // TMEM lane quarter, sub-warp of the quarter
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -543,6 +543,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kScanControlWarp) tmem_dealloc(tmem, L::kAlloc);
+}
+
+template <int Q, int P>
+__global__ void __launch_bounds__(kScanThreads, 1)
+    chunk_scan_hl(const __grid_constant__ CUtensorMap mapC32, const __grid_constant__ CUtensorMap mapB,
+                  const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapH,
+                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                  const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
+                  int GB, int GC, int nc, int heads_per_cta, int softplus) {
+  scan_hl_body<Q, P, false>(blockIdx.x, blockIdx.y, blockIdx.z, mapC32, mapB, mapX, mapH, mapY,
+                            dt, A, D, T, H, GB, GC, nc, heads_per_cta, softplus, nullptr);
 }
 
 }  // namespace ssd

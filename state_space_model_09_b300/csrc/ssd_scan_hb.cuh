@@ -18,10 +18,13 @@
 // instructions of a 64-column head.
 //
 // Range.  The factors 2^(-a_j) are at most 2^(-a_last); a head is taken here
-// when a_last >= -kHbRange, so no factor exceeds 2^96 and sums of |S x| below
-// 2^31 cannot overflow.  A (batch, chunk, head) with a longer decay is flagged
-// (flags[(b nc + c) H + h] = 0, else 1), its y left to chunk_scan_hl, which
-// runs after this kernel on the flagged heads only.
+// when a_last >= -96 (the chunk-state kernel, which runs first, records this
+// per (batch, chunk, head): flags[(b nc + c) H + h] = 1, else 0), so no factor
+// exceeds 2^96 and sums of |S x| below 2^31 cannot overflow.  The other heads
+// are computed by the per-head kernel body (scan_hl_body) in the same launch:
+// the launch's first CTAs take head-pair items, the rest take the flagged
+// heads of (batch, chunk, head range) items, and the flagged items fill the
+// SMs the head-pair items leave.
 //
 // Tensor memory (512 columns): the masked S blocks as packed bf16 pairs --
 // rows 0-127 x columns 0-127 ("b00"), rows 128-255 x columns 0-127 ("b10",
@@ -43,10 +46,9 @@
 #pragma once
 
 #include "ssd_scan.cuh"
+#include "ssd_state.cuh"
 
 namespace ssd {
-
-constexpr float kHbRange = 96.f;  // log2 units
 constexpr int kHbStoreWarp = kScanComputeWarps + 2;
 constexpr int kHbThreads = 32 * (kScanComputeWarps + 3);
 constexpr int kHbMaxPairs = 64;  // head pairs per CTA
@@ -107,15 +109,13 @@ __device__ __forceinline__ void hb_mask_pack(const float (&v)[32], int lim, uint
     pk[e] = pack_bf16x2(2 * e <= lim ? v[2 * e] : 0.f, 2 * e + 1 <= lim ? v[2 * e + 1] : 0.f);
 }
 
-__global__ void __launch_bounds__(kHbThreads, 1)
-    chunk_scan_hb(const __grid_constant__ CUtensorMap mapC32,
-                  const __grid_constant__ CUtensorMap mapB,
-                  const __grid_constant__ CUtensorMap mapX,
-                  const __grid_constant__ CUtensorMap mapH,
-                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
-                  const float *__restrict__ A, const float *__restrict__ D,
-                  uint8_t *__restrict__ flags, int64_t T, int H, int nc, int pairs_per_cta,
-                  int softplus) {
+// The body of one head-pair CTA: pair range bx of chunk c of batch row b.
+__device__ __forceinline__ void scan_hb_body(
+    int bx, int c, int b, const CUtensorMap &mapC32, const CUtensorMap &mapB,
+    const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY,
+    const float *__restrict__ dt, const float *__restrict__ A, const float *__restrict__ D,
+    const uint8_t *__restrict__ flags, int64_t T, int H, int nc, int pairs_per_cta,
+    int softplus) {
   using L = ScanHB;
   constexpr int Q = L::Q, P = L::P, N = L::N;
   constexpr int CW = kScanComputeWarps;
@@ -132,8 +132,7 @@ __global__ void __launch_bounds__(kHbThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
-  const int c = blockIdx.y, b = blockIdx.z;
-  const int h_begin = blockIdx.x * 2 * pairs_per_cta;
+  const int h_begin = bx * 2 * pairs_per_cta;
   const int h_end = min(H, h_begin + 2 * pairs_per_cta);
   const int npairs = (h_end - h_begin + 1) / 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,7 +170,8 @@ __global__ void __launch_bounds__(kHbThreads, 1)
     constexpr int PER = Q / 32;
     const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
     float z[2][PER], zn[2][PER], Ap[2], An[2], Dp[2], Dn[2];
-    auto fetch = [&](int pr, float (&zz)[2][PER], float (&aa)[2], float (&dd)[2]) {
+    int Fp[2], Fn[2];
+    auto fetch = [&](int pr, float (&zz)[2][PER], float (&aa)[2], float (&dd)[2], int (&ff)[2]) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int h = min(h_begin + 2 * pr + hh, H - 1);
@@ -180,23 +180,24 @@ __global__ void __launch_bounds__(kHbThreads, 1)
           zz[hh][e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
         aa[hh] = A[h];
         dd[hh] = D ? D[h] : 0.f;
+        ff[hh] = flags[(static_cast<int64_t>(b) * nc + c) * H + h];
       }
     };
-    if (npairs > 0) fetch(0, zn, An, Dn);
+    if (npairs > 0) fetch(0, zn, An, Dn, Fn);
     for (int pr = 0; pr < npairs; ++pr) {
       const int s = pr & 1, n = nheads_of(pr);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         Ap[hh] = An[hh];
         Dp[hh] = Dn[hh];
+        Fp[hh] = Fn[hh];
 #pragma unroll
         for (int e = 0; e < PER; ++e) z[hh][e] = zn[hh][e];
       }
-      if (pr + 1 < npairs) fetch(pr + 1, zn, An, Dn);
+      if (pr + 1 < npairs) fetch(pr + 1, zn, An, Dn, Fn);
       if (pr >= 2 && !mbar_wait(&bars[kHbTabEmpty0 + s], ((pr - 2) >> 1) & 1, abort_flag)) break;
       float *tb = tab + s * L::kTab;
       for (int hh = 0; hh < n; ++hh) {
-        const int h = h_begin + 2 * pr + hh;
         float v[PER];
         float run = 0.f;
 #pragma unroll
@@ -211,8 +212,7 @@ __global__ void __launch_bounds__(kHbThreads, 1)
           if (lane >= off) incl += o;
         }
         const float base = incl - run;
-        const float a_last = __shfl_sync(0xffffffffu, (v[PER - 1] + base) * kLog2e, 31);
-        const int fast = a_last >= -kHbRange;
+        const int fast = Fp[hh] != 0;
         float *tt = tb + hh * 2 * Q;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
@@ -224,7 +224,6 @@ __global__ void __launch_bounds__(kHbThreads, 1)
           misc[4 * s + hh] = Dp[hh];
           misc[4 * s + 2 + hh] = fast ? 1.f : 0.f;
           modes[2 * pr + hh] = static_cast<uint8_t>(fast);
-          flags[(static_cast<int64_t>(b) * nc + c) * H + h] = static_cast<uint8_t>(fast);
         }
       }
       if (n < 2 && lane == 0) {
@@ -465,6 +464,39 @@ __global__ void __launch_bounds__(kHbThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kScanControlWarp) tmem_dealloc(tmem, L::kAlloc);
+}
+
+// Shared memory of the combined launch: the larger of the two bodies.
+constexpr int kHbLaunchBytes =
+    ScanHB::kBytes > ScanHL<256, 64>::kBytes ? ScanHB::kBytes : ScanHL<256, 64>::kBytes;
+
+// One launch for the chunk outputs of 256-token chunks of one (B, C) group:
+// blocks 0 .. hb_ranges nc batch - 1 are head-pair items (pair range, chunk,
+// batch row, range fastest); the rest are the flagged heads of (head range,
+// chunk, batch row) items, computed per head.
+__global__ void __launch_bounds__(kHbThreads, 1)
+    chunk_scan_hb(const __grid_constant__ CUtensorMap mapC32,
+                  const __grid_constant__ CUtensorMap mapB,
+                  const __grid_constant__ CUtensorMap mapX,
+                  const __grid_constant__ CUtensorMap mapH,
+                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                  const float *__restrict__ A, const float *__restrict__ D,
+                  const uint8_t *__restrict__ flags, int64_t T, int batch, int H, int nc,
+                  int pairs_per_cta, int hb_ranges, int heads_per_flagged_cta, int flagged_ranges,
+                  int softplus) {
+  const int64_t i = blockIdx.x;
+  const int64_t n_hb = static_cast<int64_t>(hb_ranges) * nc * batch;
+  if (i < n_hb) {
+    scan_hb_body(static_cast<int>(i % hb_ranges), static_cast<int>((i / hb_ranges) % nc),
+                 static_cast<int>(i / (static_cast<int64_t>(hb_ranges) * nc)), mapC32, mapB, mapX,
+                 mapH, mapY, dt, A, D, flags, T, H, nc, pairs_per_cta, softplus);
+  } else {
+    const int64_t j = i - n_hb;
+    scan_hl_body<256, 64, true>(
+        static_cast<int>(j % flagged_ranges), static_cast<int>((j / flagged_ranges) % nc),
+        static_cast<int>(j / (static_cast<int64_t>(flagged_ranges) * nc)), mapC32, mapB, mapX,
+        mapH, mapY, dt, A, D, T, H, 1, 1, nc, heads_per_flagged_cta, softplus, flags);
+  }
 }
 
 }  // namespace ssd

@@ -25,12 +25,19 @@
 // state (Fseg), the product of its chunk decays (Lseg) and, per chunk, the
 // product of the decays before it within the segment (Dc).  state_fixup_kernel
 // turns these into the true chunk states.
+//
+// With `flags` (256-token chunks of one (B, C) group), the CTAs of the first
+// column slice also record for every (batch, chunk, head) whether the chunk's
+// total decay stays within the range of the head-pair chunk-scan kernel:
+// flags[(b nc + c) H + h] = 1 when cs_last * log2(e) >= -kScaledRange, else 0.
 #pragma once
 
 #include "ssd_device.cuh"
 #include "ssd_tc.cuh"
 
 namespace ssd {
+
+constexpr float kScaledRange = 96.f;  // log2 units (see chunk_scan_hb)
 
 template <int Q>
 struct StatePass {
@@ -52,7 +59,7 @@ __global__ void __launch_bounds__(256, 2)
                         __nv_bfloat16 *__restrict__ Hin, float *__restrict__ h_final, int64_t T,
                         int H, int GB, int nc, int P, int softplus, int nseg, int cps,
                         float *__restrict__ Fseg, float *__restrict__ Lseg,
-                        float *__restrict__ Dc) {
+                        float *__restrict__ Dc, uint8_t *__restrict__ flags) {
   using L = StatePass<Q>;
   constexpr int N = L::N, PS = L::PS;
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +124,8 @@ __global__ void __launch_bounds__(256, 2)
     const float cl = cs[Q - 1];
     if (tid < Q) w[tid] = __expf(cl - v);
     if (tid == 0) decay_s[lc & 1] = __expf(cl);
+    if (flags && tid == 0 && blockIdx.x == 0)
+      flags[(static_cast<int64_t>(b) * nc + c) * H + h] = cl * 1.4426950408889634f >= -kScaledRange;
     // readers of w / decay synchronise later in the loop
   };
 

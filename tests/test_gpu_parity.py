@@ -122,9 +122,10 @@ def test_fwd_small(name):
 ])
 def test_fwd_q256_long_decay_heads(a_scale):
     """256-token chunks of one group: heads whose in-chunk decay exceeds the
-    scaled form's range are left by the head-pair kernel to chunk_scan_hl;
-    either way every head's y and state match the oracle (odd head count, so
-    one pair has a single head; ragged last chunk; random h0)."""
+    scaled form's range are flagged by the chunk-state kernel and computed one
+    by one in the chunk-scan launch; either way every head's y and state match
+    the oracle (odd head count, so one pair has a single head; ragged last
+    chunk; random h0)."""
     shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 41)
     inp["A"] = (inp["A"] * np.asarray(a_scale, dtype=np.float32)).astype(np.float32)
@@ -152,7 +153,6 @@ def test_fwd_f32_without_softplus_and_D():
 def test_fwd_stage_path_matches_dtype():
     d = S.make_dims(8, 2048, 80, 64, 128)
     assert S.ssd_fwd_stage_name(d, 256, 1) == "chunk_scan_hb"
-    assert S.ssd_fwd_stage_name(d, 256, 2) == "chunk_scan_hl"
     assert S.ssd_fwd_stage_name(d, 128, 1) == "chunk_scan_hl"
 
 
