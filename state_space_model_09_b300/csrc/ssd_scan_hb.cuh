@@ -46,7 +46,6 @@
 #pragma once
 
 #include "ssd_scan.cuh"
-#include "ssd_state.cuh"
 
 namespace ssd {
 constexpr int kHbStoreWarp = kScanComputeWarps + 2;
