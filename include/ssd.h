@@ -97,7 +97,12 @@ size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk);
  *   workspace/workspace_bytes: device scratch of at least
  *             ssd_fwd_workspace_size() bytes; contents need no initialisation
  *             and are garbage afterwards.
- * Returns SSD_OK once every kernel is enqueued on `stream`. */
+ * Returns SSD_OK once every kernel is enqueued on `stream`.
+ * With 256-token chunks, 64-wide heads and one (B, C) group the chunk outputs
+ * can be computed two heads per MMA in a scaled form (chunk_scan_hb) or head
+ * by head (chunk_scan_hl); the call picks by the work per CTA.  The
+ * environment variable SSD_CHUNK_SCAN=pair or =head, read on every call,
+ * forces one of the two (results agree within the stated tolerance). */
 ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                    const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
                    void *y, float *h_final, void *workspace, size_t workspace_bytes,

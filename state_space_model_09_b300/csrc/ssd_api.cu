@@ -17,6 +17,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/ssd.h"
@@ -53,6 +55,11 @@ struct Plan {
 };
 
 int num_sms();
+int scan_pairs_per_cta(const Plan &pl, int num_sms);
+// chunk_scan_hb pays a per-CTA set-up (C B^T, mask, C into tensor memory)
+// and a pipeline fill; below this many head pairs per CTA the per-head
+// kernel is faster (e.g. 4096-token windows of one sequence: 5 pairs)
+constexpr int kHbMinPairs = 10;
 
 // Segments of the tensor-core state pass.  Its CTAs walk their chunks one after
 // another, two per SM; when the (batch, head, slice) items leave SM slots idle
@@ -122,10 +129,16 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
       pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
       pl->total = pl->Dc_off + align_up(bh * pl->nc * sizeof(float));
     }
-    pl->hb = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
-    if (pl->hb) {
+    const bool hb_shape = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
+    if (hb_shape) {  // the flags are reserved for every such shape
       pl->flags_off = pl->total;
       pl->total += align_up(static_cast<size_t>(pl->b) * pl->nc * pl->H);
+      // SSD_CHUNK_SCAN=pair / =head forces the choice (the same result either
+      // way, within the tolerance; for tests and tuning)
+      const char *force = std::getenv("SSD_CHUNK_SCAN");
+      if (force && std::strcmp(force, "pair") == 0) pl->hb = true;
+      else if (force && std::strcmp(force, "head") == 0) pl->hb = false;
+      else pl->hb = scan_pairs_per_cta(*pl, num_sms()) >= kHbMinPairs;
     }
   } else {
     pl->cs_off = 0;

@@ -70,6 +70,25 @@ def test_stage_names_follow_the_path():
     assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
 
 
+def _scan_stage(d, chunk=256):
+    return S.ssd_fwd_stage_name(d, chunk, S.ssd_fwd_num_stages(d, chunk) - 1)
+
+
+def test_chunk_scan_form_follows_work_per_cta_and_override(monkeypatch):
+    monkeypatch.delenv("SSD_CHUNK_SCAN", raising=False)
+    d = _dims()  # 64 (batch, chunk) items x 40 head pairs: head pairs
+    window = _dims(batch=1, seqlen=4096)  # 16 items: too few pairs per CTA
+    assert _scan_stage(d) == "chunk_scan_hb"
+    assert _scan_stage(window) == "chunk_scan_hl"
+    sizes = (S.ssd_fwd_workspace_size(d, 256), S.ssd_fwd_workspace_size(window, 256))
+    monkeypatch.setenv("SSD_CHUNK_SCAN", "head")
+    assert _scan_stage(d) == "chunk_scan_hl"
+    monkeypatch.setenv("SSD_CHUNK_SCAN", "pair")
+    assert _scan_stage(window) == "chunk_scan_hb"
+    # the workspace (with the decay-range flags) does not depend on the choice
+    assert (S.ssd_fwd_workspace_size(d, 256), S.ssd_fwd_workspace_size(window, 256)) == sizes
+
+
 @pytest.mark.parametrize("kw,chunk,status", [
     (dict(headdim=24), 256, S.SSD_ERR_UNSUPPORTED),
     (dict(dstate=272), 256, S.SSD_ERR_UNSUPPORTED),

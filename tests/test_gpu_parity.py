@@ -115,17 +115,35 @@ def test_fwd_small(name):
     check_fwd(shape, seed)
 
 
+# small 256-token, single-group cases, also forced through the head-pair form
+# (the call picks it only when each CTA gets enough head pairs)
+PAIR_FORM = ["tc_q256_p64", "tc_q256_exact", "tc_T1", "tc_segments_q256"]
+
+
+@pytest.mark.parametrize("name", PAIR_FORM)
+def test_fwd_small_pair_form(name, monkeypatch):
+    monkeypatch.setenv("SSD_CHUNK_SCAN", "pair")
+    shape, seed = SMALL[name]
+    d = S.make_dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                    shape.ngroups_b, shape.ngroups_c)
+    assert "chunk_scan_hb" in [S.ssd_fwd_stage_name(d, shape.chunk, i)
+                               for i in range(S.ssd_fwd_num_stages(d, shape.chunk))]
+    check_fwd(shape, seed)
+
+
+@pytest.mark.parametrize("form", ["pair", "head"])
 @pytest.mark.parametrize("a_scale", [
     (30.0, 1.0, 30.0, 1.0, 1.0),     # heads 0 and 2 decay past the scaled form's range
     (30.0, 30.0, 30.0, 30.0, 30.0),  # every head does
     (0.01, 0.01, 0.01, 0.01, 0.01),  # none does
 ])
-def test_fwd_q256_long_decay_heads(a_scale):
+def test_fwd_q256_long_decay_heads(a_scale, form, monkeypatch):
     """256-token chunks of one group: heads whose in-chunk decay exceeds the
     scaled form's range are flagged by the chunk-state kernel and computed one
-    by one in the chunk-scan launch; either way every head's y and state match
-    the oracle (odd head count, so one pair has a single head; ragged last
-    chunk; random h0)."""
+    by one in the head-pair launch; either way, and with the head-by-head
+    kernel throughout, every head's y and state match the oracle (odd head
+    count, so one pair has a single head; ragged last chunk; random h0)."""
+    monkeypatch.setenv("SSD_CHUNK_SCAN", form)
     shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 41)
     inp["A"] = (inp["A"] * np.asarray(a_scale, dtype=np.float32)).astype(np.float32)
