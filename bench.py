@@ -138,8 +138,9 @@ def fwd_work(s: synth.FwdShape):
         "state_passing": (S32 + b * H * nc * 4 + h0 + S32 + st, 2 * b * nc * H * N * P),
         "chunk_scan_simt": (x + Bb + Cb + cs + S32 + x, f_scan),
     }
-    # one launch computes every head (two per MMA, or one by one when flagged)
+    # the head-pair kernels: the same inputs and outputs
     stages["chunk_scan_hb"] = stages["chunk_scan_hl"]
+    stages["chunk_state_hb"] = stages["chunk_state_pass_tc"]
     return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 

@@ -25,6 +25,7 @@
 #include "ssd_kernels.cuh"
 #include "ssd_scan.cuh"
 #include "ssd_scan_hb.cuh"
+#include "ssd_state_hb.cuh"
 #include "ssd_state.cuh"
 #include "ssd_tc.cuh"
 
@@ -52,6 +53,8 @@ struct Plan {
   // per MMA or, flagged, one by one
   bool hb = false;
   size_t flags_off = 0;
+  // the same shapes: chunk states two heads per MMA (chunk_state_hb)
+  bool state_hb = false;
 };
 
 int num_sms();
@@ -65,9 +68,10 @@ constexpr int kHbMinPairs = 10;
 // another, two per SM; when the (batch, head, slice) items leave SM slots idle
 // the sequence is split so that every slot works on a segment of at least four
 // chunks.
+// chunk_state_hb: one CTA per SM, one per (batch, head pair).
 void plan_segments(Plan *pl) {
-  const int64_t items = pl->b * pl->H * (pl->P / 64);
-  const int64_t slots = 2 * static_cast<int64_t>(num_sms());
+  const int64_t items = pl->state_hb ? pl->b * ((pl->H + 1) / 2) : pl->b * pl->H * (pl->P / 64);
+  const int64_t slots = (pl->state_hb ? 1 : 2) * static_cast<int64_t>(num_sms());
   int64_t nseg = items >= slots ? 1 : slots / items;
   nseg = std::min<int64_t>(nseg, pl->nc / 4);
   nseg = std::max<int64_t>(nseg, 1);
@@ -120,6 +124,8 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     pl->cs_off = pl->S_off = 0;
     pl->Hin_off = 0;
     pl->total = align_up(states * 2);
+    const bool hb_shape = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
+    pl->state_hb = hb_shape;
     plan_segments(pl);
     if (pl->nseg > 1) {
       if (pl->b * pl->nseg > 65535) return SSD_ERR_UNSUPPORTED;
@@ -129,7 +135,6 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
       pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
       pl->total = pl->Dc_off + align_up(bh * pl->nc * sizeof(float));
     }
-    const bool hb_shape = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
     if (hb_shape) {  // the flags are reserved for every such shape
       pl->flags_off = pl->total;
       pl->total += align_up(static_cast<size_t>(pl->b) * pl->nc * pl->H);
@@ -276,18 +281,31 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
                              const float *dt, const float *A, const float *h0, __nv_bfloat16 *Hin,
                              float *h_final, float *Fseg, float *Lseg, float *Dc,
                              uint8_t *flags, void *const *events, cudaStream_t s) {
-  using L = ssd::StatePass<Q>;
-  auto k = ssd::chunk_state_pass_tc<Q>;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
-  if (!ok) return SSD_ERR_CUDA;
-  dim3 grid(static_cast<unsigned>(pl.P / L::PS), static_cast<unsigned>(pl.H),
-            static_cast<unsigned>(pl.b * pl.nseg));
-  k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
-                                         static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
-                                         static_cast<int>(pl.P), pl.softplus, pl.nseg, pl.cps,
-                                         Fseg, Lseg, Dc, flags);
+  if (pl.state_hb) {
+    // two heads per MMA; mB / mX are the 128-row tile maps here
+    auto k = ssd::chunk_state_hb;
+    static std::once_flag once;
+    static bool ok = false;
+    std::call_once(once, [&] { ok = set_smem(k, ssd::StateHB::kBytes); });
+    if (!ok) return SSD_ERR_CUDA;
+    dim3 grid(static_cast<unsigned>((pl.H + 1) / 2), 1, static_cast<unsigned>(pl.b * pl.nseg));
+    k<<<grid, ssd::kShThreads, ssd::StateHB::kBytes, s>>>(
+        mB, mX, dt, A, h0, Hin, h_final, pl.T, static_cast<int>(pl.H), pl.nc, pl.softplus,
+        pl.nseg, pl.cps, Fseg, Lseg, Dc, flags);
+  } else {
+    using L = ssd::StatePass<Q>;
+    auto k = ssd::chunk_state_pass_tc<Q>;
+    static std::once_flag once;
+    static bool ok = false;
+    std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
+    if (!ok) return SSD_ERR_CUDA;
+    dim3 grid(static_cast<unsigned>(pl.P / L::PS), static_cast<unsigned>(pl.H),
+              static_cast<unsigned>(pl.b * pl.nseg));
+    k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
+                                           static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
+                                           static_cast<int>(pl.P), pl.softplus, pl.nseg, pl.cps,
+                                           Fseg, Lseg, Dc, flags);
+  }
   if (launch_status() != SSD_OK || pl.nseg == 1) return launch_status();
   record(events, 1, s);
   const int NP = static_cast<int>(pl.N * pl.P);
@@ -476,13 +494,19 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
         !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
         !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
       return SSD_ERR_CUDA;
+    // chunk_state_hb reads B and x in 128-token halves
+    CUtensorMap mB128, mX128;
+    if (pl.state_hb && (!encode_btgw(&mX128, x, pl.b, pl.T, pl.H, pl.P, 128) ||
+                        !encode_btgw(&mB128, B, pl.b, pl.T, pl.GB, pl.N, 128)))
+      return SSD_ERR_CUDA;
+    const CUtensorMap &mBs = pl.state_hb ? mB128 : mB, &mXs = pl.state_hb ? mX128 : mX;
     record(events, 0, s);
     float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
     float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
     float *Dc = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Dc_off) : nullptr;
     uint8_t *flags = pl.hb ? ws + pl.flags_off : nullptr;
-    st = pl.Q == 256 ? launch_state_pass<256>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s)
-                     : launch_state_pass<128>(pl, mB, mX, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s);
+    st = pl.Q == 256 ? launch_state_pass<256>(pl, mBs, mXs, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s)
+                     : launch_state_pass<128>(pl, mBs, mXs, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s);
     if (st != SSD_OK) return st;
     const int se = pl.nseg > 1 ? 2 : 1;  // events index after the state stages
     record(events, se, s);
@@ -512,10 +536,6 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   return SSD_OK;
 }
 
-const char *const kStageNamesTc[] = {"chunk_state_pass_tc", "chunk_scan_hl"};
-const char *const kStageNamesTcSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hl"};
-const char *const kStageNamesHb[] = {"chunk_state_pass_tc", "chunk_scan_hb"};
-const char *const kStageNamesHbSeg[] = {"chunk_state_pass_tc", "state_fixup", "chunk_scan_hb"};
 int num_stages(const Plan &pl) { return pl.tc ? (pl.nseg > 1 ? 3 : 2) : 4; }
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
@@ -570,8 +590,9 @@ const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
   if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= num_stages(pl)) return nullptr;
   if (!pl.tc) return kStageNamesSimt[i];
-  if (pl.hb) return pl.nseg > 1 ? kStageNamesHbSeg[i] : kStageNamesHb[i];
-  return pl.nseg > 1 ? kStageNamesTcSeg[i] : kStageNamesTc[i];
+  if (i == 0) return pl.state_hb ? "chunk_state_hb" : "chunk_state_pass_tc";
+  if (i == 1 && pl.nseg > 1) return "state_fixup";
+  return pl.hb ? "chunk_scan_hb" : "chunk_scan_hl";
 }
 
 ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,

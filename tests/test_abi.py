@@ -52,7 +52,7 @@ def test_workspace_size_layout():
 
 def test_stage_names_follow_the_path():
     assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(2)] == \
-        ["chunk_state_pass_tc", "chunk_scan_hb"]
+        ["chunk_state_hb", "chunk_scan_hb"]
     assert [S.ssd_fwd_stage_name(_dims(ngroups_c=2), 256, i) for i in range(2)] == \
         ["chunk_state_pass_tc", "chunk_scan_hl"]
     assert [S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, i) for i in range(4)] == \
@@ -66,7 +66,7 @@ def test_stage_names_follow_the_path():
     # segments, joined by a fix-up stage
     long = _dims(batch=1, seqlen=16384)
     assert [S.ssd_fwd_stage_name(long, 256, i) for i in range(S.ssd_fwd_num_stages(long, 256))] == \
-        ["chunk_state_pass_tc", "state_fixup", "chunk_scan_hb"]
+        ["chunk_state_hb", "state_fixup", "chunk_scan_hb"]
     assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
 
 
