@@ -141,6 +141,7 @@ def fwd_work(s: synth.FwdShape):
     # the head-pair kernels: the same inputs and outputs
     stages["chunk_scan_hb"] = stages["chunk_scan_hl"]
     stages["chunk_state_hb"] = stages["chunk_state_pass_tc"]
+    stages["dt_decay"] = (2 * dt, 0)  # dt in, the per-head log2 decays out
     return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 

@@ -53,8 +53,10 @@ struct Plan {
   // per MMA or, flagged, one by one
   bool hb = false;
   size_t flags_off = 0;
-  // the same shapes: chunk states two heads per MMA (chunk_state_hb)
+  // the same shapes: chunk states two heads per MMA (chunk_state_hb), after
+  // dt_decay_kernel has written the per-token log2 decays [b, H, T] (u_off)
   bool state_hb = false;
+  size_t u_off = 0;
 };
 
 int num_sms();
@@ -144,6 +146,8 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
       if (force && std::strcmp(force, "pair") == 0) pl->hb = true;
       else if (force && std::strcmp(force, "head") == 0) pl->hb = false;
       else pl->hb = scan_pairs_per_cta(*pl, num_sms()) >= kHbMinPairs;
+      pl->u_off = pl->total;
+      pl->total += align_up(static_cast<size_t>(pl->b) * pl->H * pl->T * sizeof(float));
     }
   } else {
     pl->cs_off = 0;
@@ -278,9 +282,10 @@ int num_sms() {
 
 template <int Q>
 ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtensorMap &mX,
-                             const float *dt, const float *A, const float *h0, __nv_bfloat16 *Hin,
+                             const float *dt, const float *A, const float *u, const float *h0,
+                             __nv_bfloat16 *Hin,
                              float *h_final, float *Fseg, float *Lseg, float *Dc,
-                             uint8_t *flags, void *const *events, cudaStream_t s) {
+                             uint8_t *flags, void *const *events, int ev, cudaStream_t s) {
   if (pl.state_hb) {
     // two heads per MMA; mB / mX are the 128-row tile maps here
     auto k = ssd::chunk_state_hb;
@@ -290,8 +295,8 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
     if (!ok) return SSD_ERR_CUDA;
     dim3 grid(static_cast<unsigned>((pl.H + 1) / 2), 1, static_cast<unsigned>(pl.b * pl.nseg));
     k<<<grid, ssd::kShThreads, ssd::StateHB::kBytes, s>>>(
-        mB, mX, dt, A, h0, Hin, h_final, pl.T, static_cast<int>(pl.H), pl.nc, pl.softplus,
-        pl.nseg, pl.cps, Fseg, Lseg, Dc, flags);
+        mB, mX, u, h0, Hin, h_final, pl.T, static_cast<int>(pl.H), pl.nc, pl.nseg, pl.cps, Fseg,
+        Lseg, Dc, flags);
   } else {
     using L = ssd::StatePass<Q>;
     auto k = ssd::chunk_state_pass_tc<Q>;
@@ -307,7 +312,7 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
                                            Fseg, Lseg, Dc, flags);
   }
   if (launch_status() != SSD_OK || pl.nseg == 1) return launch_status();
-  record(events, 1, s);
+  record(events, ev + 1, s);
   const int NP = static_cast<int>(pl.N * pl.P);
   dim3 g2(static_cast<unsigned>((NP / 4 + 255) / 256), static_cast<unsigned>(pl.H),
           static_cast<unsigned>(pl.b));
@@ -418,8 +423,8 @@ constexpr int kFlaggedRanges = 4;
 
 ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
-                          const float *dt, const float *A, const float *D, const uint8_t *flags,
-                          cudaStream_t s) {
+                          const float *dt, const float *A, const float *D, const float *u,
+                          const uint8_t *flags, cudaStream_t s) {
   auto k = ssd::chunk_scan_hb;
   static std::once_flag once;
   static bool ok = false;
@@ -434,7 +439,7 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
   const int64_t blocks = (static_cast<int64_t>(hb_ranges) + flagged_ranges) * pl.nc * pl.b;
   if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
   k<<<static_cast<unsigned>(blocks), ssd::kHbThreads, ssd::kHbLaunchBytes, s>>>(
-      mC32, mB, mX, mH, mY, dt, A, D, flags, pl.T, static_cast<int>(pl.b), static_cast<int>(pl.H),
+      mC32, mB, mX, mH, mY, dt, A, D, u, flags, pl.T, static_cast<int>(pl.b), static_cast<int>(pl.H),
       pl.nc, pp, hb_ranges, static_cast<int>(hpf), flagged_ranges, pl.softplus);
   return launch_status();
 }
@@ -500,17 +505,26 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
                         !encode_btgw(&mB128, B, pl.b, pl.T, pl.GB, pl.N, 128)))
       return SSD_ERR_CUDA;
     const CUtensorMap &mBs = pl.state_hb ? mB128 : mB, &mXs = pl.state_hb ? mX128 : mX;
-    record(events, 0, s);
+    int ev = 0;  // events[i] just before stage i
+    record(events, ev, s);
+    float *u = nullptr;
+    if (pl.state_hb) {
+      u = reinterpret_cast<float *>(ws + pl.u_off);
+      dim3 g((pl.T + 31) / 32, static_cast<unsigned>((pl.H + 31) / 32), static_cast<unsigned>(pl.b));
+      ssd::dt_decay_kernel<<<g, 256, 0, s>>>(dt, A, u, pl.T, static_cast<int>(pl.H), pl.softplus);
+      if ((st = launch_status()) != SSD_OK) return st;
+      record(events, ++ev, s);
+    }
     float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
     float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
     float *Dc = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Dc_off) : nullptr;
     uint8_t *flags = pl.hb ? ws + pl.flags_off : nullptr;
-    st = pl.Q == 256 ? launch_state_pass<256>(pl, mBs, mXs, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s)
-                     : launch_state_pass<128>(pl, mBs, mXs, dt, A, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, s);
+    st = pl.Q == 256 ? launch_state_pass<256>(pl, mBs, mXs, dt, A, u, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, ev, s)
+                     : launch_state_pass<128>(pl, mBs, mXs, dt, A, u, h0, static_cast<__nv_bfloat16 *>(Hin), h_final, Fseg, Lseg, Dc, flags, events, ev, s);
     if (st != SSD_OK) return st;
-    const int se = pl.nseg > 1 ? 2 : 1;  // events index after the state stages
+    const int se = ev + (pl.nseg > 1 ? 2 : 1);  // events index after the state stages
     record(events, se, s);
-    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, flags, s);
+    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, u, flags, s);
     else if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
@@ -536,7 +550,9 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   return SSD_OK;
 }
 
-int num_stages(const Plan &pl) { return pl.tc ? (pl.nseg > 1 ? 3 : 2) : 4; }
+int num_stages(const Plan &pl) {
+  return pl.tc ? (pl.nseg > 1 ? 3 : 2) + (pl.state_hb ? 1 : 0) : 4;
+}
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
                                        "chunk_scan_simt"};
 
@@ -590,6 +606,7 @@ const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
   if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= num_stages(pl)) return nullptr;
   if (!pl.tc) return kStageNamesSimt[i];
+  if (pl.state_hb && i-- == 0) return "dt_decay";
   if (i == 0) return pl.state_hb ? "chunk_state_hb" : "chunk_state_pass_tc";
   if (i == 1 && pl.nseg > 1) return "state_fixup";
   return pl.hb ? "chunk_scan_hb" : "chunk_scan_hl";

@@ -3,7 +3,8 @@
 //
 // Same result as chunk_scan_hl (ssd_scan.cuh): for one (batch b, chunk c) and
 // each head h, with a = cs * log2(e) the in-chunk inclusive running sum of
-// softplus(dt) * A_h in log2 units and Hin the chunk's true initial state,
+// softplus(dt) * A_h in log2 units (summed here from u = softplus(dt) A
+// log2(e), written by dt_decay_kernel) and Hin the chunk's true initial state,
 //   y_i = sum_{j <= i} 2^(a_i - a_j) S_ij x_j + 2^(a_i) (C Hin)_i + D_h x_i,   S = C B^T
 // (Mamba-2 page, section "SSD算法": the orange diagonal block in quadratic
 // form and the blue term from the true initial state).
@@ -112,13 +113,11 @@ __device__ __forceinline__ void hb_mask_pack(const float (&v)[32], int lim, uint
 __device__ __forceinline__ void scan_hb_body(
     int bx, int c, int b, const CUtensorMap &mapC32, const CUtensorMap &mapB,
     const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY,
-    const float *__restrict__ dt, const float *__restrict__ A, const float *__restrict__ D,
-    const uint8_t *__restrict__ flags, int64_t T, int H, int nc, int pairs_per_cta,
-    int softplus) {
+    const float *__restrict__ u, const float *__restrict__ D, const uint8_t *__restrict__ flags,
+    int64_t T, int H, int nc, int pairs_per_cta) {
   using L = ScanHB;
   constexpr int Q = L::Q, P = L::P, N = L::N;
   constexpr int CW = kScanComputeWarps;
-  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *Xs = smem;                // two buffers, each [head][Q rows][128 B]
@@ -163,37 +162,36 @@ __device__ __forceinline__ void scan_hb_body(
 
   if (warp == kScanAuxWarp) {
     // ================================================================ tables
-    // Tables of pair pr into buffer pr & 1 (lane owns Q/32 consecutive
-    // tokens; running sum, then a warp scan).  The next pair's dt, A and D
-    // are fetched before this pair's buffer is waited for.
+    // Tables of pair pr into buffer pr & 1 (lane owns Q/32 consecutive tokens
+    // of the per-token log2 decays u = softplus(dt) A log2(e); running sum,
+    // then a warp scan).  The next pair's u, D and modes are fetched before
+    // this pair's buffer is waited for.
     constexpr int PER = Q / 32;
     const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
-    float z[2][PER], zn[2][PER], Ap[2], An[2], Dp[2], Dn[2];
+    float z[2][PER], zn[2][PER], Dp[2], Dn[2];
     int Fp[2], Fn[2];
-    auto fetch = [&](int pr, float (&zz)[2][PER], float (&aa)[2], float (&dd)[2], int (&ff)[2]) {
+    auto fetch = [&](int pr, float (&zz)[2][PER], float (&dd)[2], int (&ff)[2]) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int h = min(h_begin + 2 * pr + hh, H - 1);
+        const float *uh = u + (static_cast<int64_t>(b) * H + h) * T;
 #pragma unroll
-        for (int e = 0; e < PER; ++e)
-          zz[hh][e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
-        aa[hh] = A[h];
+        for (int e = 0; e < PER; ++e) zz[hh][e] = t0 + e < T ? uh[t0 + e] : 0.f;
         dd[hh] = D ? D[h] : 0.f;
         ff[hh] = flags[(static_cast<int64_t>(b) * nc + c) * H + h];
       }
     };
-    if (npairs > 0) fetch(0, zn, An, Dn, Fn);
+    if (npairs > 0) fetch(0, zn, Dn, Fn);
     for (int pr = 0; pr < npairs; ++pr) {
       const int s = pr & 1, n = nheads_of(pr);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        Ap[hh] = An[hh];
         Dp[hh] = Dn[hh];
         Fp[hh] = Fn[hh];
 #pragma unroll
         for (int e = 0; e < PER; ++e) z[hh][e] = zn[hh][e];
       }
-      if (pr + 1 < npairs) fetch(pr + 1, zn, An, Dn, Fn);
+      if (pr + 1 < npairs) fetch(pr + 1, zn, Dn, Fn);
       if (pr >= 2 && !mbar_wait(&bars[kHbTabEmpty0 + s], ((pr - 2) >> 1) & 1, abort_flag)) break;
       float *tb = tab + s * L::kTab;
       for (int hh = 0; hh < n; ++hh) {
@@ -201,7 +199,7 @@ __device__ __forceinline__ void scan_hb_body(
         float run = 0.f;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          if (t0 + e < T) run += (softplus ? softplus_f32(z[hh][e]) : z[hh][e]) * Ap[hh];
+          run += z[hh][e];  // 0 past T
           v[e] = run;
         }
         float incl = run;
@@ -215,7 +213,7 @@ __device__ __forceinline__ void scan_hb_body(
         float *tt = tb + hh * 2 * Q;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          const float av = (v[e] + base) * kLog2e;
+          const float av = v[e] + base;
           tt[lane * PER + e] = fast ? ex2_approx(-av) : 0.f;
           tt[Q + lane * PER + e] = ex2_approx(av);
         }
@@ -480,15 +478,15 @@ __global__ void __launch_bounds__(kHbThreads, 1)
                   const __grid_constant__ CUtensorMap mapH,
                   const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
                   const float *__restrict__ A, const float *__restrict__ D,
-                  const uint8_t *__restrict__ flags, int64_t T, int batch, int H, int nc,
-                  int pairs_per_cta, int hb_ranges, int heads_per_flagged_cta, int flagged_ranges,
-                  int softplus) {
+                  const float *__restrict__ u, const uint8_t *__restrict__ flags, int64_t T,
+                  int batch, int H, int nc, int pairs_per_cta, int hb_ranges,
+                  int heads_per_flagged_cta, int flagged_ranges, int softplus) {
   const int64_t i = blockIdx.x;
   const int64_t n_hb = static_cast<int64_t>(hb_ranges) * nc * batch;
   if (i < n_hb) {
     scan_hb_body(static_cast<int>(i % hb_ranges), static_cast<int>((i / hb_ranges) % nc),
                  static_cast<int>(i / (static_cast<int64_t>(hb_ranges) * nc)), mapC32, mapB, mapX,
-                 mapH, mapY, dt, A, D, flags, T, H, nc, pairs_per_cta, softplus);
+                 mapH, mapY, u, D, flags, T, H, nc, pairs_per_cta);
   } else {
     const int64_t j = i - n_hb;
     scan_hl_body<256, 64, true>(

@@ -3,7 +3,8 @@
 //
 // Same result as chunk_state_pass_tc (ssd_state.cuh): for one (batch b, head
 // pair) and every chunk c in order, with a = cs * log2(e) the in-chunk
-// inclusive running sum of softplus(dt) * A_h in log2 units,
+// inclusive running sum of softplus(dt) * A_h in log2 units (summed here from
+// u = softplus(dt) * A * log2(e), written by dt_decay_kernel),
 //   S_c   = B_c^T diag(w) x_c,     w_j = 2^(a_last - a_j)             (green step)
 //   Hin_c = state entering chunk c                                   (stored, bf16)
 //   state = 2^(a_last) * state + S_c                                 (yellow step)
@@ -63,15 +64,14 @@ static_assert(kNumShBars <= StateHB::kBars, "barrier slots");
 
 __global__ void __launch_bounds__(kShThreads, 1)
     chunk_state_hb(const __grid_constant__ CUtensorMap mapB128,
-                   const __grid_constant__ CUtensorMap mapX128, const float *__restrict__ dt,
-                   const float *__restrict__ A, const float *__restrict__ h0,
-                   __nv_bfloat16 *__restrict__ Hin, float *__restrict__ h_final, int64_t T,
-                   int H, int nc, int softplus, int nseg, int cps, float *__restrict__ Fseg,
+                   const __grid_constant__ CUtensorMap mapX128, const float *__restrict__ u,
+                   const float *__restrict__ h0, __nv_bfloat16 *__restrict__ Hin,
+                   float *__restrict__ h_final, int64_t T, int H, int nc, int nseg, int cps,
+                   float *__restrict__ Fseg,
                    float *__restrict__ Lseg, float *__restrict__ Dc,
                    uint8_t *__restrict__ flags) {
   using L = StateHB;
   constexpr int Q = L::Q, P = L::P, N = L::N, HALF = L::HALF;
-  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   // slot s: [B state cols 0-63 | B cols 64-127 | x head 0 | x head 1], each [HALF rows][128 B]
@@ -108,25 +108,24 @@ __global__ void __launch_bounds__(kShThreads, 1)
   if (warp >= kShTables) {
     // ================================================================ tables
     // Head hh = warp - kShTables: chunk lc's w_j = 2^(a_last - a_j) and decay
-    // 2^(a_last) into buffer lc % 3 (lane owns Q/32 consecutive tokens;
-    // running sum, then a warp scan); the next chunk's dt is fetched first.
+    // 2^(a_last) into buffer lc % 3 (lane owns Q/32 consecutive tokens of the
+    // per-token log2 decays u; running sum, then a warp scan); the next
+    // chunk's u is fetched first.
     constexpr int PER = Q / 32;
     const int hh = warp - kShTables;
     const bool mine = hh < nh;
     const int h = hb0 + min(hh, nh - 1);
-    const float Ah = A[h];
+    const float *uh = u + (static_cast<int64_t>(b) * H + h) * T;
     float z[PER], zn[PER];
     float prod = 1.f;  // decays of this segment's chunks so far
     auto fetch = [&](int lc, float (&zz)[PER]) {
       const int64_t t0 = static_cast<int64_t>(c_begin + lc) * Q + lane * PER;
 #pragma unroll
-      for (int e = 0; e < PER; ++e)
-        zz[e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
+      for (int e = 0; e < PER; ++e) zz[e] = t0 + e < T ? uh[t0 + e] : 0.f;
     };
     if (ncl > 0 && mine) fetch(0, zn);
     for (int lc = 0; lc < ncl; ++lc) {
       const int s = lc % L::kTabBufs, c = c_begin + lc;
-      const int64_t t0 = static_cast<int64_t>(c) * Q + lane * PER;
 #pragma unroll
       for (int e = 0; e < PER; ++e) z[e] = zn[e];
       if (mine && lc + 1 < ncl) fetch(lc + 1, zn);
@@ -138,7 +137,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
         float run = 0.f;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          if (t0 + e < T) run += (softplus ? softplus_f32(z[e]) : z[e]) * Ah;
+          run += z[e];  // 0 past T
           v[e] = run;
         }
         float incl = run;
@@ -148,10 +147,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
           if (lane >= off) incl += o;
         }
         const float base = incl - run;
-        const float a_last = __shfl_sync(0xffffffffu, (v[PER - 1] + base) * kLog2e, 31);
+        const float a_last = __shfl_sync(0xffffffffu, v[PER - 1] + base, 31);
         float *tw = tab + s * L::kTab + hh * Q;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) tw[lane * PER + e] = ex2_approx(a_last - (v[e] + base) * kLog2e);
+        for (int e = 0; e < PER; ++e) tw[lane * PER + e] = ex2_approx(a_last - (v[e] + base));
         if (lane == 0) {
           const float decay = ex2_approx(a_last);
           dec[2 * s + hh] = decay;
@@ -302,6 +301,44 @@ __global__ void __launch_bounds__(kShThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kShControl) tmem_dealloc(tmem, L::kAlloc);
+}
+
+// ----------------------------------------------------------------------------
+// dt -> per-token log2 decays for the head-pair kernels:
+//   u[b, h, t] = softplus(dt[b, t, h]) * A_h * log2(e)
+// (the modified A factors of the Mamba-2 page, section "SSD算法", in log2
+// units), written with each head's tokens contiguous so that a table warp
+// reads a chunk of one head in 1 KB.  A 32-token x 32-head tile per block
+// through shared memory (reads coalesced over heads, writes over tokens).
+// grid (ceil(T / 32), ceil(H / 32), batch), 256 threads.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dt_decay_kernel(const float *__restrict__ dt,
+                                                       const float *__restrict__ A,
+                                                       float *__restrict__ u, int64_t T, int H,
+                                                       int softplus) {
+  __shared__ float tile[32][33];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int h0 = blockIdx.y * 32, b = blockIdx.z;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t t = t0 + r;
+    const int h = h0 + tx;
+    float v = 0.f;
+    if (t < T && h < H) {
+      const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
+      v = (softplus ? softplus_f32(z) : z) * A[h] * kLog2e;
+    }
+    tile[r][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = ty; r < 32; r += 8) {
+    const int h = h0 + r;
+    const int64_t t = t0 + tx;
+    if (h < H && t < T) u[(static_cast<int64_t>(b) * H + h) * T + t] = tile[tx][r];
+  }
 }
 
 }  // namespace ssd

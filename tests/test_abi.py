@@ -38,8 +38,9 @@ def test_workspace_size_layout():
     st = 8 * nc * 80 * 128 * 64
     # tensor-core path: the bf16 chunk initial states; one (B, C) group with
     # 256-token chunks of 64-wide heads adds one byte per (batch, chunk, head)
-    # (which of the two chunk-scan kernels writes that head's y)
-    assert S.ssd_fwd_workspace_size(d, 256) == st * 2 + 8 * nc * 80
+    # (whether the head-pair chunk scan takes that unit) and the per-token
+    # log2 decays [b, H, T] in float32
+    assert S.ssd_fwd_workspace_size(d, 256) == st * 2 + 8 * nc * 80 + 8 * 80 * 2048 * 4
     d_g2 = _dims(ngroups_b=2, ngroups_c=2)
     assert S.ssd_fwd_workspace_size(d_g2, 256) == st * 2
     # float32 path: cumsums, chunk states and chunk initial states in float32
@@ -51,22 +52,22 @@ def test_workspace_size_layout():
 
 
 def test_stage_names_follow_the_path():
-    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(2)] == \
-        ["chunk_state_hb", "chunk_scan_hb"]
+    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(3)] == \
+        ["dt_decay", "chunk_state_hb", "chunk_scan_hb"]
     assert [S.ssd_fwd_stage_name(_dims(ngroups_c=2), 256, i) for i in range(2)] == \
         ["chunk_state_pass_tc", "chunk_scan_hl"]
     assert [S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, i) for i in range(4)] == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
     assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"
-    assert S.ssd_fwd_stage_name(_dims(), 256, 2) is None
-    assert S.ssd_fwd_num_stages(_dims(), 256) == 2
+    assert S.ssd_fwd_stage_name(_dims(), 256, 3) is None
+    assert S.ssd_fwd_num_stages(_dims(), 256) == 3
     assert S.ssd_fwd_num_stages(_dims(), 128) == 2
     assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
     # one long sequence over 80 heads: the state pass is split into sequence
     # segments, joined by a fix-up stage
     long = _dims(batch=1, seqlen=16384)
     assert [S.ssd_fwd_stage_name(long, 256, i) for i in range(S.ssd_fwd_num_stages(long, 256))] == \
-        ["chunk_state_hb", "state_fixup", "chunk_scan_hb"]
+        ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
     assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
 
 

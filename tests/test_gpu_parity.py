@@ -170,7 +170,7 @@ def test_fwd_f32_without_softplus_and_D():
 
 def test_fwd_stage_path_matches_dtype():
     d = S.make_dims(8, 2048, 80, 64, 128)
-    assert S.ssd_fwd_stage_name(d, 256, 1) == "chunk_scan_hb"
+    assert S.ssd_fwd_stage_name(d, 256, S.ssd_fwd_num_stages(d, 256) - 1) == "chunk_scan_hb"
     assert S.ssd_fwd_stage_name(d, 128, 1) == "chunk_scan_hl"
 
 
