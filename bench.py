@@ -47,12 +47,13 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_scan_hb", "mamba2_2p7b"):
-        (428_288_000, ("state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
+        (429_509_888, ("state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
                        "state_space_model_09_b300/csrc/ssd_scan.cuh"),
-         "d664e1589144ba8f7a7b93e39ed97c44417cd8d7"),
-    ("chunk_state_pass_tc", "mamba2_2p7b"):
-        (268_224_768, ("state_space_model_09_b300/csrc/ssd_state.cuh",),
-         "66b078fac69fd2861344c0c1e5de619d591e0cdb"),
+         "511c3d1048fa616c7c4ed6cb04127d203c983718"),
+    ("chunk_state_hb", "mamba2_2p7b"):
+        (260_557_312, ("state_space_model_09_b300/csrc/ssd_state_hb.cuh",
+                       "state_space_model_09_b300/csrc/ssd_state.cuh"),
+         "5682630050785ed0ae1b705b8040edf3f517a587"),
     ("multistep_kernel", "multistep_k8"):
         (70_129_920, ("state_space_model_09_b300/csrc/ssd_kernels.cuh",),
          "f1267a2133217f991f16eac81edf77c2e16126eb"),
