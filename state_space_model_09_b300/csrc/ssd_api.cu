@@ -20,6 +20,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "../../include/ssd.h"
 #include "ssd_kernels.cuh"
@@ -44,8 +45,11 @@ struct Plan {
   bool bf16, softplus, tc;
   size_t cs_off, S_off, Hin_off, total;
   // tensor-core path: sequence segments of the state pass (1: none) and the
-  // workspace of their hand-off (segment final states, decay products)
+  // workspace of their hand-off (segment final states, decay products).  The
+  // first `whole` items run unsplit; the hand-off covers the (b, h) rows
+  // seg_bh0 .. seg_bh0 + seg_rows - 1 of the split ones
   int nseg = 1, cps = 0;
+  int64_t whole = 0, seg_bh0 = 0, seg_rows = 0;
   size_t Fseg_off = 0, Lseg_off = 0, Dc_off = 0;
   // 256-token chunks, 64-wide heads, one (B, C) group: the chunk-state kernel
   // records per (b, chunk, head) whether the chunk's decay allows the
@@ -70,15 +74,33 @@ constexpr int kHbMinPairs = 10;
 // another, two per SM; when the (batch, head, slice) items leave SM slots idle
 // the sequence is split so that every slot works on a segment of at least four
 // chunks.
-// chunk_state_hb: one CTA per SM, one per (batch, head pair).
+// chunk_state_hb: one CTA per SM, one per (batch, head pair).  With more items
+// than SMs, the items of a last, partly filled wave are split instead (the
+// full waves' items run whole), into segments of at least two chunks, so that
+// the last wave takes a fraction of an item's time: e.g. 8 x 2048 tokens x 40
+// head pairs on 148 SMs = two full waves + 24 items, split in four.
 void plan_segments(Plan *pl) {
   const int64_t items = pl->state_hb ? pl->b * ((pl->H + 1) / 2) : pl->b * pl->H * (pl->P / 64);
   const int64_t slots = (pl->state_hb ? 1 : 2) * static_cast<int64_t>(num_sms());
-  int64_t nseg = items >= slots ? 1 : slots / items;
-  nseg = std::min<int64_t>(nseg, pl->nc / 4);
+  int64_t nseg = 1, whole = 0;
+  if (items < slots) {
+    nseg = std::min<int64_t>(slots / items, pl->nc / 4);
+  } else if (pl->state_hb && items % slots) {
+    whole = items / slots * slots;
+    nseg = std::min<int64_t>(slots / (items - whole), pl->nc / 2);
+  }
   nseg = std::max<int64_t>(nseg, 1);
   pl->cps = static_cast<int>((pl->nc + nseg - 1) / nseg);
   pl->nseg = (pl->nc + pl->cps - 1) / pl->cps;
+  pl->whole = pl->nseg > 1 ? whole : items;
+  // the split items' (b, h) rows: from the first split item's first head on
+  if (pl->state_hb) {
+    const int64_t npairs = (pl->H + 1) / 2;
+    pl->seg_bh0 = pl->whole / npairs * pl->H + 2 * (pl->whole % npairs);
+  } else {
+    pl->seg_bh0 = 0;
+  }
+  pl->seg_rows = pl->b * pl->H - pl->seg_bh0;
 }
 
 bool valid_dim(int64_t v) { return v >= 1 && v <= (int64_t(1) << 31) - 1; }
@@ -130,8 +152,8 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     pl->state_hb = hb_shape;
     plan_segments(pl);
     if (pl->nseg > 1) {
-      if (pl->b * pl->nseg > 65535) return SSD_ERR_UNSUPPORTED;
-      const size_t bh = static_cast<size_t>(pl->b) * pl->H;
+      if (pl->b * pl->nseg > 65535 || pl->seg_rows > 65535) return SSD_ERR_UNSUPPORTED;
+      const size_t bh = static_cast<size_t>(pl->seg_rows);
       pl->Fseg_off = pl->total;
       pl->Lseg_off = pl->Fseg_off + align_up(bh * pl->nseg * pl->N * pl->P * sizeof(float));
       pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
@@ -211,6 +233,38 @@ ssd_status launch_status() {
 
 void record(void *const *events, int i, cudaStream_t s) {
   if (events && events[i]) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+}
+
+// Programmatic dependent launch (the device side is grid_dep_wait /
+// grid_dep_trigger): the kernels after dt_decay_kernel on the head-pair path
+// may start while the one before them finishes, so that their set-up (barrier
+// and tensor-memory set-up, input loads, the chunk scan's C B^T) overlaps its
+// tail.  Off for a call that records per-stage events (the stages would
+// overlap) and when SSD_PDL=0.
+bool pdl_on(void *const *events) {
+  if (events) return false;
+  const char *e = std::getenv("SSD_PDL");
+  return !(e && std::strcmp(e, "0") == 0);
+}
+
+template <typename... KArgs, typename... Args>
+ssd_status launch_dependent(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();  // clear the recorded launch error
+    return SSD_ERR_CUDA;
+  }
+  return launch_status();
 }
 
 // ---------------------------------------------------------------------------
@@ -293,10 +347,13 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
     static bool ok = false;
     std::call_once(once, [&] { ok = set_smem(k, ssd::StateHB::kBytes); });
     if (!ok) return SSD_ERR_CUDA;
-    dim3 grid(static_cast<unsigned>((pl.H + 1) / 2), 1, static_cast<unsigned>(pl.b * pl.nseg));
-    k<<<grid, ssd::kShThreads, ssd::StateHB::kBytes, s>>>(
-        mB, mX, u, h0, Hin, h_final, pl.T, static_cast<int>(pl.H), pl.nc, pl.nseg, pl.cps, Fseg,
-        Lseg, Dc, flags);
+    const int64_t items = pl.b * ((pl.H + 1) / 2);
+    const int64_t ctas = pl.whole + (items - pl.whole) * (pl.nseg > 1 ? pl.nseg : 1);
+    const ssd_status st = launch_dependent(
+        pdl_on(events), k, dim3(static_cast<unsigned>(ctas)), dim3(ssd::kShThreads),
+        ssd::StateHB::kBytes, s, mB, mX, u, h0, Hin, h_final, pl.T, static_cast<int>(pl.H), pl.nc,
+        static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg, Dc, flags);
+    if (st != SSD_OK) return st;
   } else {
     using L = ssd::StatePass<Q>;
     auto k = ssd::chunk_state_pass_tc<Q>;
@@ -309,16 +366,15 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
     k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
                                            static_cast<int>(pl.H), static_cast<int>(pl.GB), pl.nc,
                                            static_cast<int>(pl.P), pl.softplus, pl.nseg, pl.cps,
-                                           Fseg, Lseg, Dc, flags);
+                                           Fseg, Lseg, Dc);
   }
   if (launch_status() != SSD_OK || pl.nseg == 1) return launch_status();
   record(events, ev + 1, s);
   const int NP = static_cast<int>(pl.N * pl.P);
-  dim3 g2(static_cast<unsigned>((NP / 4 + 255) / 256), static_cast<unsigned>(pl.H),
-          static_cast<unsigned>(pl.b));
-  ssd::state_fixup_kernel<<<g2, 256, 0, s>>>(Fseg, Lseg, Dc, Hin, h_final,
-                                             static_cast<int>(pl.H), pl.nc, pl.cps, pl.nseg, NP);
-  return launch_status();
+  dim3 g2(static_cast<unsigned>((NP / 4 + 255) / 256), static_cast<unsigned>(pl.seg_rows));
+  return launch_dependent(pl.state_hb && pdl_on(events), ssd::state_fixup_kernel, g2, dim3(256),
+                          0, s, Fseg, Lseg, Dc, Hin, h_final, static_cast<int>(pl.H), pl.nc,
+                          pl.cps, pl.nseg, NP, pl.seg_bh0);
 }
 
 template <typename IO, int KT, int NC = 0, int PSC = 0>
@@ -416,15 +472,15 @@ int scan_pairs_per_cta(const Plan &pl, int num_sms) {
   return best;
 }
 
-// Head ranges of the flagged-head items of chunk_scan_hb's launch: each item
-// scans a range of heads for the few the chunk-state kernel flagged, so an
-// item is cheap when its range holds none.
-constexpr int kFlaggedRanges = 4;
+// Head sets of the flagged-head items of chunk_scan_hb's launch: each item
+// scans every kFlaggedSets-th head of its (batch, chunk) for the few the
+// chunk-state kernel flagged (at most ScanHL<256, 64>::kMaxFlaggedHeads).
+constexpr int kFlaggedSets = 4;
 
 ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
                           const float *dt, const float *A, const float *D, const float *u,
-                          const uint8_t *flags, cudaStream_t s) {
+                          const uint8_t *flags, bool pdl, cudaStream_t s) {
   auto k = ssd::chunk_scan_hb;
   static std::once_flag once;
   static bool ok = false;
@@ -433,15 +489,15 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
   const int pp = scan_pairs_per_cta(pl, num_sms());
   const int64_t pairs = (pl.H + 1) / 2;
   const int hb_ranges = static_cast<int>((pairs + pp - 1) / pp);
-  const int64_t hpf = std::min<int64_t>((pl.H + kFlaggedRanges - 1) / kFlaggedRanges,
-                                        ssd::ScanHL<256, 64>::kMaxFlaggedHeads);
-  const int flagged_ranges = static_cast<int>((pl.H + hpf - 1) / hpf);
-  const int64_t blocks = (static_cast<int64_t>(hb_ranges) + flagged_ranges) * pl.nc * pl.b;
+  const int64_t kmax = ssd::ScanHL<256, 64>::kMaxFlaggedHeads;
+  const int flagged_sets =
+      static_cast<int>(std::max<int64_t>(kFlaggedSets, (pl.H + kmax - 1) / kmax));
+  const int64_t blocks = (static_cast<int64_t>(hb_ranges) + flagged_sets) * pl.nc * pl.b;
   if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
-  k<<<static_cast<unsigned>(blocks), ssd::kHbThreads, ssd::kHbLaunchBytes, s>>>(
-      mC32, mB, mX, mH, mY, dt, A, D, u, flags, pl.T, static_cast<int>(pl.b), static_cast<int>(pl.H),
-      pl.nc, pp, hb_ranges, static_cast<int>(hpf), flagged_ranges, pl.softplus);
-  return launch_status();
+  return launch_dependent(pdl, k, dim3(static_cast<unsigned>(blocks)), dim3(ssd::kHbThreads),
+                          ssd::kHbLaunchBytes, s, mC32, mB, mX, mH, mY, dt, A, D, u, flags, pl.T,
+                          static_cast<int>(pl.b), static_cast<int>(pl.H), pl.nc, pp, hb_ranges,
+                          flagged_sets, pl.softplus);
 }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -510,7 +566,8 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     float *u = nullptr;
     if (pl.state_hb) {
       u = reinterpret_cast<float *>(ws + pl.u_off);
-      dim3 g((pl.T + 31) / 32, static_cast<unsigned>((pl.H + 31) / 32), static_cast<unsigned>(pl.b));
+      dim3 g((pl.T + 31) / 32, static_cast<unsigned>((pl.H + ssd::kDtHeads - 1) / ssd::kDtHeads),
+             static_cast<unsigned>(pl.b));
       ssd::dt_decay_kernel<<<g, 256, 0, s>>>(dt, A, u, pl.T, static_cast<int>(pl.H), pl.softplus);
       if ((st = launch_status()) != SSD_OK) return st;
       record(events, ++ev, s);
@@ -524,7 +581,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     if (st != SSD_OK) return st;
     const int se = ev + (pl.nseg > 1 ? 2 : 1);  // events index after the state stages
     record(events, se, s);
-    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, u, flags, s);
+    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, u, flags, pdl_on(events), s);
     else if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);

@@ -65,6 +65,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running, once every CTA of that kernel has called grid_dep_trigger (or
+// exited); a thread that calls grid_dep_wait then waits, in hardware, until
+// the earlier kernels have finished and their writes are visible.  Without
+// the launch attribute both are no-ops.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

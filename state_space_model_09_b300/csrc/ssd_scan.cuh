@@ -195,8 +195,12 @@ __device__ __noinline__ void scan_mask_band(uint8_t *Bt, uint32_t tlane, const f
 }
 
 // The body of one CTA: head range bx of chunk c of batch row b.  FLAGGED:
-// compute only the heads of the range whose byte in only_flagged is 0 (the
-// heads left by the head-pair kernel); otherwise every head of the range.
+// the heads bx, bx + heads_per_cta, bx + 2 heads_per_cta, ... (interleaved, so
+// that the few heads a long decay flags spread evenly over the CTAs), and of
+// those only the ones whose byte in only_flagged is 0 (the heads left by the
+// head-pair kernel); their decays come from u, the per-token log2 decays
+// softplus(dt) A log2(e) with each head's tokens contiguous.  Otherwise every
+// head of the range bx heads_per_cta ... (bx + 1) heads_per_cta - 1.
 // Warps 0-17 take part (warps past them, in a wider launch, only wait).
 template <int Q, int P, bool FLAGGED>
 __device__ __forceinline__ void scan_hl_body(
@@ -204,7 +208,7 @@ __device__ __forceinline__ void scan_hl_body(
     const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY,
     const float *__restrict__ dt, const float *__restrict__ A, const float *__restrict__ D,
     int64_t T, int H, int GB, int GC, int nc, int heads_per_cta, int softplus,
-    const uint8_t *__restrict__ only_flagged) {
+    const uint8_t *__restrict__ only_flagged, const float *__restrict__ u) {
   using L = ScanHL<Q, P>;
   constexpr int N = L::N, MT = L::MT, KMAX = FLAGGED ? L::kMaxFlaggedHeads : L::kMaxHeads;
   constexpr int CW = kScanComputeWarps;
@@ -224,8 +228,10 @@ __device__ __forceinline__ void scan_hl_body(
   int *hlist = reinterpret_cast<int *>(tslot + 4);  // FLAGGED: the heads this CTA computes
   int *nh_s = hlist + KMAX;
 
-  const int h_begin = bx * heads_per_cta;
-  const int nh_all = min(H, h_begin + heads_per_cta) - h_begin;
+  const int h_begin = FLAGGED ? bx : bx * heads_per_cta;
+  const int h_step = FLAGGED ? heads_per_cta : 1;  // the stride of the CTA's heads
+  const int nh_all = FLAGGED ? (H - bx + heads_per_cta - 1) / heads_per_cta
+                             : min(H, h_begin + heads_per_cta) - h_begin;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpg_b = H / GB, hpg_c = H / GC;
   auto head_at = [&](int k) { return FLAGGED ? hlist[k] : h_begin + k; };
@@ -247,8 +253,9 @@ __device__ __forceinline__ void scan_hl_body(
   // kernel flagged 0, selected in parallel and compacted by thread 0
   if (FLAGGED) {
     for (int k = tid; k < nh_all; k += blockDim.x) {
-      hlist[k] = only_flagged[(static_cast<int64_t>(b) * nc + c) * H + h_begin + k] == 0;
-      D_s[k] = D ? D[h_begin + k] : 0.f;
+      const int h = h_begin + k * h_step;
+      hlist[k] = only_flagged[(static_cast<int64_t>(b) * nc + c) * H + h] == 0;
+      D_s[k] = D ? D[h] : 0.f;
     }
   } else if (tid < nh_all) {
     D_s[tid] = D ? D[h_begin + tid] : 0.f;
@@ -263,7 +270,7 @@ __device__ __forceinline__ void scan_hl_body(
       int n = 0;
       for (int k = 0; k < nh_all; ++k) {
         if (hlist[k]) {
-          hlist[n] = h_begin + k;
+          hlist[n] = h_begin + k * h_step;
           D_s[n] = D_s[k];
           ++n;
         }
@@ -288,16 +295,20 @@ __device__ __forceinline__ void scan_hl_body(
       if (k < nh) {
         const int h = head_at(k), s = k & 1;
         float z[PER];
+        const float *uh = FLAGGED ? u + (static_cast<int64_t>(b) * H + h) * T : nullptr;
 #pragma unroll
         for (int e = 0; e < PER; ++e)
-          z[e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
+          z[e] = t0 + e >= T ? 0.f
+                 : FLAGGED  ? uh[t0 + e]
+                            : dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h];
         const float Ah = A[h];
         if (k >= 2 && !mbar_wait(&bars[kBarTabEmpty0 + s], ((k - 2) >> 1) & 1, abort_flag)) break;
         float v[PER];
         float run = 0.f;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          if (t0 + e < T) run += (softplus ? softplus_f32(z[e]) : z[e]) * Ah;
+          if (FLAGGED) run += z[e];  // already in log2 units; 0 past T
+          else if (t0 + e < T) run += (softplus ? softplus_f32(z[e]) : z[e]) * Ah;
           v[e] = run;
         }
         float incl = run;
@@ -310,7 +321,7 @@ __device__ __forceinline__ void scan_hl_body(
         float *ta = tables + s * L::kTables * Q;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          const float av = (v[e] + base) * kLog2e;
+          const float av = FLAGGED ? v[e] + base : (v[e] + base) * kLog2e;
           ta[lane * PER + e] = av;
           ta[Q + lane * PER + e] = ex2_approx(av);
         }
@@ -553,7 +564,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                   const float *__restrict__ A, const float *__restrict__ D, int64_t T, int H,
                   int GB, int GC, int nc, int heads_per_cta, int softplus) {
   scan_hl_body<Q, P, false>(blockIdx.x, blockIdx.y, blockIdx.z, mapC32, mapB, mapX, mapH, mapY,
-                            dt, A, D, T, H, GB, GC, nc, heads_per_cta, softplus, nullptr);
+                            dt, A, D, T, H, GB, GC, nc, heads_per_cta, softplus, nullptr,
+                            nullptr);
 }
 
 }  // namespace ssd

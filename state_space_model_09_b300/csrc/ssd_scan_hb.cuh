@@ -9,23 +9,28 @@
 // (Mamba-2 page, section "SSD算法": the orange diagonal block in quadratic
 // form and the blue term from the true initial state).
 //
-// Scaled form.  Taking 2^(a_i) out of row i,
-//   y_i = 2^(a_i) [ sum_{j <= i} S_ij (2^(-a_j) x_j) + (C Hin)_i + D_h 2^(-a_i) x_i ],
+// Scaled form.  Taking 2^(a_i - r) out of row i, for a reference r <= 0 of
+// the (batch, chunk, head),
+//   y_i = 2^(a_i - r) [ sum_{j <= i} S_ij (2^(r - a_j) x_j) + (C 2^r Hin)_i
+//                       + D_h 2^(r - a_i) x_i ],
 // the masked matrix (j <= i) o S no longer depends on the head: it is formed
 // once per CTA and is the A operand of every head's second MMA, while the
-// head's decay rides on its x rows (x_j 2^(-a_j), the B operand).  Two heads
-// share every MMA (N = 2 x 64): C [Hin_h | Hin_h'] and the three masked
-// blocks of S times [x~_h | x~_h'].  No per-head mask, half the MMA
+// head's decay rides on its x rows (x_j 2^(r - a_j), the B operand).  Two
+// heads share every MMA (N = 2 x 64): C [2^r Hin_h | 2^r' Hin_h'] and the three
+// masked blocks of S times [x~_h | x~_h'].  No per-head mask, half the MMA
 // instructions of a 64-column head.
 //
-// Range.  The factors 2^(-a_j) are at most 2^(-a_last); a head is taken here
-// when a_last >= -96 (the chunk-state kernel, which runs first, records this
-// per (batch, chunk, head): flags[(b nc + c) H + h] = 1, else 0), so no factor
-// exceeds 2^96 and sums of |S x| below 2^31 cannot overflow.  The other heads
-// are computed by the per-head kernel body (scan_hl_body) in the same launch:
-// the launch's first CTAs take head-pair items, the rest take the flagged
-// heads of (batch, chunk, head range) items, and the flagged items fill the
-// SMs the head-pair items leave.
+// Range.  r = min(0, a_last + 96) (scaled_form_ref, ssd_tc.cuh) keeps every
+// factor within 2^-96 .. 2^96 while a_last >= -192; the chunk-state kernel,
+// which runs first, records that per (batch, chunk, head) (flags[(b nc + c) H
+// + h] = 1, else 0) and stores those chunk states already multiplied by 2^r.
+// The other heads -- chunks whose decay falls below 2^-192 -- are computed by
+// the per-head kernel body (scan_hl_body) in the same launch: the launch's
+// first CTAs take head-pair items, the rest take the flagged heads of (batch,
+// chunk, head set) items -- head set r of R: heads r, r + R, r + 2R, ..., so
+// that each set gets about as many of the flagged heads, which a head's decay
+// rate makes cluster -- and the flagged items fill the SMs the head-pair
+// items leave.
 //
 // Tensor memory (512 columns): the masked S blocks as packed bf16 pairs --
 // rows 0-127 x columns 0-127 ("b00"), rows 128-255 x columns 0-127 ("b10",
@@ -41,7 +46,7 @@
 // Warp roles: warps 0-15 build the S blocks, copy C, scale x and write y
 // (four per TMEM lane quarter); warp 16 (one lane) issues the C/B/Hin and the
 // first x loads and every MMA; warp 17 computes each pair's decay tables up
-// to two pairs ahead, fetching the next pair's dt while it works; warp 18
+// to two pairs ahead, fetching the next pair's u while it works; warp 18
 // (one lane) stores each pair's y and loads the x two pairs ahead.  Every
 // wait is bounded in time.
 #pragma once
@@ -181,6 +186,7 @@ __device__ __forceinline__ void scan_hb_body(
         ff[hh] = flags[(static_cast<int64_t>(b) * nc + c) * H + h];
       }
     };
+    grid_dep_wait();  // u and the flags come from the kernels before this one
     if (npairs > 0) fetch(0, zn, Dn, Fn);
     for (int pr = 0; pr < npairs; ++pr) {
       const int s = pr & 1, n = nheads_of(pr);
@@ -210,12 +216,16 @@ __device__ __forceinline__ void scan_hb_body(
         }
         const float base = incl - run;
         const int fast = Fp[hh] != 0;
+        // the reference r of the scaled form, from the chunk's total decay
+        // (the same running sums as the chunk-state kernel, which stored this
+        // head's chunk state times 2^r)
+        const float r = scaled_form_ref(__shfl_sync(0xffffffffu, v[PER - 1] + base, 31));
         float *tt = tb + hh * 2 * Q;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
           const float av = v[e] + base;
-          tt[lane * PER + e] = fast ? ex2_approx(-av) : 0.f;
-          tt[Q + lane * PER + e] = ex2_approx(av);
+          tt[lane * PER + e] = fast ? ex2_approx(r - av) : 0.f;
+          tt[Q + lane * PER + e] = ex2_approx(av - r);
         }
         if (lane == 0) {
           misc[4 * s + hh] = Dp[hh];
@@ -274,8 +284,6 @@ __device__ __forceinline__ void scan_hb_body(
                       c * Q + 32 * rb, b);
         tma_load_4d(Xs + L::kXS + s * Q * 128, &mapB, &bars[kHbCB], 64 * s, 0, c * Q, b);
       }
-      load_h(0);
-      if (npairs > 1) load_h(1);
       bool ok = mbar_wait(&bars[kHbCB], 0, abort_flag);
       // three S pieces (C0 B0^T, C1 B0^T, C1 B1^T) through the Y columns, each
       // packed by the compute warps before the next
@@ -291,6 +299,13 @@ __device__ __forceinline__ void scan_hb_body(
         }
         mma_commit(&bars[kHbS]);
         ok = mbar_wait(&bars[kHbConv], p & 1, abort_flag);
+      }
+      // the set-up above reads inputs only; the chunk states come from the
+      // chunk-state kernel, which may still be running when this CTA starts
+      grid_dep_wait();
+      if (ok) {
+        load_h(0);
+        if (npairs > 1) load_h(1);
       }
       // C and B are consumed: both buffers take x
       if (ok) {
@@ -469,8 +484,9 @@ constexpr int kHbLaunchBytes =
 
 // One launch for the chunk outputs of 256-token chunks of one (B, C) group:
 // blocks 0 .. hb_ranges nc batch - 1 are head-pair items (pair range, chunk,
-// batch row, range fastest); the rest are the flagged heads of (head range,
-// chunk, batch row) items, computed per head.
+// batch row, range fastest); the rest are the flagged heads of (head set,
+// chunk, batch row) items, computed per head (head set r of flagged_sets:
+// heads r, r + flagged_sets, ...).
 __global__ void __launch_bounds__(kHbThreads, 1)
     chunk_scan_hb(const __grid_constant__ CUtensorMap mapC32,
                   const __grid_constant__ CUtensorMap mapB,
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(kHbThreads, 1)
                   const float *__restrict__ A, const float *__restrict__ D,
                   const float *__restrict__ u, const uint8_t *__restrict__ flags, int64_t T,
                   int batch, int H, int nc, int pairs_per_cta, int hb_ranges,
-                  int heads_per_flagged_cta, int flagged_ranges, int softplus) {
+                  int flagged_sets, int softplus) {
   const int64_t i = blockIdx.x;
   const int64_t n_hb = static_cast<int64_t>(hb_ranges) * nc * batch;
   if (i < n_hb) {
@@ -488,11 +504,12 @@ __global__ void __launch_bounds__(kHbThreads, 1)
                  static_cast<int>(i / (static_cast<int64_t>(hb_ranges) * nc)), mapC32, mapB, mapX,
                  mapH, mapY, u, D, flags, T, H, nc, pairs_per_cta);
   } else {
+    grid_dep_wait();  // the flags, u and the chunk states of the kernels before
     const int64_t j = i - n_hb;
     scan_hl_body<256, 64, true>(
-        static_cast<int>(j % flagged_ranges), static_cast<int>((j / flagged_ranges) % nc),
-        static_cast<int>(j / (static_cast<int64_t>(flagged_ranges) * nc)), mapC32, mapB, mapX,
-        mapH, mapY, dt, A, D, T, H, 1, 1, nc, heads_per_flagged_cta, softplus, flags);
+        static_cast<int>(j % flagged_sets), static_cast<int>((j / flagged_sets) % nc),
+        static_cast<int>(j / (static_cast<int64_t>(flagged_sets) * nc)), mapC32, mapB, mapX,
+        mapH, mapY, dt, A, D, T, H, 1, 1, nc, flagged_sets, softplus, flags, u);
   }
 }
 

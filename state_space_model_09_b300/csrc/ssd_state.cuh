@@ -25,11 +25,6 @@
 // state (Fseg), the product of its chunk decays (Lseg) and, per chunk, the
 // product of the decays before it within the segment (Dc).  state_fixup_kernel
 // turns these into the true chunk states.
-//
-// With `flags` (256-token chunks of one (B, C) group), the CTAs of the first
-// column slice also record for every (batch, chunk, head) whether the chunk's
-// total decay stays within the range of the head-pair chunk-scan kernel:
-// flags[(b nc + c) H + h] = 1 when cs_last * log2(e) >= -kScaledRange, else 0.
 #pragma once
 
 #include "ssd_device.cuh"
@@ -37,7 +32,6 @@
 
 namespace ssd {
 
-constexpr float kScaledRange = 96.f;  // log2 units (see chunk_scan_hb)
 
 template <int Q>
 struct StatePass {
@@ -59,7 +53,7 @@ __global__ void __launch_bounds__(256, 2)
                         __nv_bfloat16 *__restrict__ Hin, float *__restrict__ h_final, int64_t T,
                         int H, int GB, int nc, int P, int softplus, int nseg, int cps,
                         float *__restrict__ Fseg, float *__restrict__ Lseg,
-                        float *__restrict__ Dc, uint8_t *__restrict__ flags) {
+                        float *__restrict__ Dc) {
   using L = StatePass<Q>;
   constexpr int N = L::N, PS = L::PS;
   extern __shared__ uint8_t smem_raw[];
@@ -124,8 +118,6 @@ __global__ void __launch_bounds__(256, 2)
     const float cl = cs[Q - 1];
     if (tid < Q) w[tid] = __expf(cl - v);
     if (tid == 0) decay_s[lc & 1] = __expf(cl);
-    if (flags && tid == 0 && blockIdx.x == 0)
-      flags[(static_cast<int64_t>(b) * nc + c) * H + h] = cl * 1.4426950408889634f >= -kScaledRange;
     // readers of w / decay synchronise later in the loop
   };
 
@@ -222,22 +214,27 @@ __global__ void __launch_bounds__(256, 2)
 // start of segment s (T_1 = Fseg_0, since segment 0 started from h0):
 //   Hin_c += Dc_c * T_s           for every chunk c of segment s >= 1
 //   T_{s+1} = Lseg_s * T_s + Fseg_s,   h_final = T_nseg
-// Elementwise over (b, h, n, p); thread = 4 consecutive elements; grid
-// (ceil(N P / 1024), H, batch), 256 threads.
+// for the split (batch, head) rows bh0, bh0 + 1, ... (row = b H + h), whose
+// hand-off arrays are indexed from bh0.  Elementwise over (row, n, p);
+// thread = 4 consecutive elements; grid (ceil(N P / 1024), rows), 256 threads.
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) state_fixup_kernel(
     const float *__restrict__ Fseg, const float *__restrict__ Lseg, const float *__restrict__ Dc,
     __nv_bfloat16 *__restrict__ Hin, float *__restrict__ h_final, int H, int nc, int cps,
-    int nseg, int NP) {
-  const int h = blockIdx.y, b = blockIdx.z;
+    int nseg, int NP, int64_t bh0) {
+  const int64_t r = blockIdx.y;  // row relative to bh0
+  const int64_t bh = bh0 + r;
+  const int64_t b = bh / H;
+  const int h = static_cast<int>(bh % H);
   const int e = 4 * (blockIdx.x * 256 + threadIdx.x);
+  grid_dep_trigger();  // the chunk scan may start its set-up
+  grid_dep_wait();     // the segment results of the chunk-state kernel
   if (e >= NP) return;
-  const int64_t bh = static_cast<int64_t>(b) * H + h;
-  float4 Ts = *reinterpret_cast<const float4 *>(Fseg + bh * nseg * NP + e);
+  float4 Ts = *reinterpret_cast<const float4 *>(Fseg + r * nseg * NP + e);
   for (int s = 1; s < nseg; ++s) {
     const int c0 = s * cps, c1 = min(nc, c0 + cps);
     const int64_t cstride = static_cast<int64_t>(H) * NP;  // one chunk further in Hin
-    uint2 *base = reinterpret_cast<uint2 *>(Hin + ((static_cast<int64_t>(b) * nc + c0) * H + h) * NP + e);
+    uint2 *base = reinterpret_cast<uint2 *>(Hin + ((b * nc + c0) * H + h) * NP + e);
     // eight chunks per round, loads first, so that many reads are in flight
     for (int c = c0; c < c1; c += 8) {
       uint2 v[8];
@@ -246,7 +243,7 @@ __global__ void __launch_bounds__(256) state_fixup_kernel(
       for (int u = 0; u < 8; ++u) {
         if (c + u < c1) {
           v[u] = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(base) + (c - c0 + u) * cstride);
-          d[u] = Dc[bh * nc + c + u];
+          d[u] = Dc[r * nc + c + u];
         }
       }
 #pragma unroll
@@ -260,8 +257,8 @@ __global__ void __launch_bounds__(256) state_fixup_kernel(
         }
       }
     }
-    const float l = Lseg[bh * nseg + s];
-    const float4 f = *reinterpret_cast<const float4 *>(Fseg + (bh * nseg + s) * NP + e);
+    const float l = Lseg[r * nseg + s];
+    const float4 f = *reinterpret_cast<const float4 *>(Fseg + (r * nseg + s) * NP + e);
     Ts = make_float4(fmaf(l, Ts.x, f.x), fmaf(l, Ts.y, f.y), fmaf(l, Ts.z, f.z), fmaf(l, Ts.w, f.w));
   }
   if (h_final) *reinterpret_cast<float4 *>(h_final + bh * NP + e) = Ts;

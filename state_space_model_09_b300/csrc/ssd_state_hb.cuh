@@ -13,6 +13,14 @@
 // at h0 (or zero) and its last value is h_final; sequence segments and their
 // hand-off (Fseg, Lseg, Dc) work as in chunk_state_pass_tc.
 //
+// Items.  Item i is (batch i / npairs, head pair i % npairs).  The first
+// `whole` CTAs take items 0 .. whole - 1 over the whole sequence; the CTAs
+// after them take the remaining items in `nseg` segments of `cps` chunks
+// each (CTA whole + k nseg + s: item whole + k, segment s).  The host splits
+// only the items of a last, partly filled wave, so that wave ends as soon as
+// the full ones; the hand-off arrays then cover the split items' heads alone,
+// indexed from the first of them (bh0 = its b H + h).
+//
 // Schedule.  B is the A operand of every head's MMA, so two heads share one
 // MMA chain (N = 2 x 64).  Each chunk arrives as two 128-token stages (the B
 // half and both heads' x halves, 64 KB) through a ring of three shared-memory
@@ -23,8 +31,12 @@
 // running state (registers: thread = one state row, 32 columns of one head).
 // A table warp computes each chunk's decays up to two chunks ahead.
 //
-// With `flags`, the (batch, chunk, head) decay-range flags of the head-pair
-// chunk scan are recorded here too: 1 when a_last >= -kScaledRange.
+// With `flags` (the head-pair chunk scan follows), the (batch, chunk, head)
+// decay-range flags of that scan are recorded here too -- 1 when
+// a_last >= -kScaledRangeMax -- and each flagged-1 chunk state is stored
+// multiplied by 2^r, r = scaled_form_ref(a_last), the factor the scan's
+// scaled form applies to it (ssd_tc.cuh); the per-chunk decay products Dc of a
+// split item carry the same factor, so the fix-up keeps it.
 //
 // Warp roles: warps 0-15 scale x, fold states and store chunk states (four
 // per TMEM lane quarter); warp 16 (one lane) issues every TMA load and MMA;
@@ -48,7 +60,7 @@ struct StateHB {
   static constexpr int kSlots = 3;
   static constexpr int kTabBufs = 3;
   static constexpr int kTab = 2 * Q;  // per buffer: w_j for the two heads
-  static constexpr int kFloats = kTabBufs * (kTab + 2);  // + the two chunk decays, per buffer
+  static constexpr int kFloats = kTabBufs * (kTab + 4);  // + the two chunk decays and state factors
   static constexpr int kBars = 20;
   static constexpr int kBytes = kSlots * kStage + kFloats * 4 + kBars * 8 + 16 + 1024;
   static constexpr uint32_t kAlloc = 256;  // two chunk accumulators of 128 columns
@@ -66,8 +78,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
     chunk_state_hb(const __grid_constant__ CUtensorMap mapB128,
                    const __grid_constant__ CUtensorMap mapX128, const float *__restrict__ u,
                    const float *__restrict__ h0, __nv_bfloat16 *__restrict__ Hin,
-                   float *__restrict__ h_final, int64_t T, int H, int nc, int nseg, int cps,
-                   float *__restrict__ Fseg,
+                   float *__restrict__ h_final, int64_t T, int H, int nc, int whole, int nseg,
+                   int cps, int64_t bh0, float *__restrict__ Fseg,
                    float *__restrict__ Lseg, float *__restrict__ Dc,
                    uint8_t *__restrict__ flags) {
   using L = StateHB;
@@ -78,14 +90,21 @@ __global__ void __launch_bounds__(kShThreads, 1)
   uint8_t *slots = smem;
   // tables of chunk lc in buffer lc % 3: [buf][head][Q] w_j, [buf][head] decay
   float *tab = reinterpret_cast<float *>(slots + L::kSlots * L::kStage);
-  float *dec = tab + L::kTabBufs * L::kTab;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(dec + 2 * L::kTabBufs);
+  float *dec = tab + L::kTabBufs * L::kTab;  // [buf][head] chunk decay 2^a_last
+  float *hsc = dec + 2 * L::kTabBufs;        // [buf][head] factor of the stored chunk state
+  uint64_t *bars = reinterpret_cast<uint64_t *>(hsc + 2 * L::kTabBufs);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
-  const int pair = blockIdx.x, b = blockIdx.z / nseg, seg = blockIdx.z % nseg;
+  const int npairs = (H + 1) / 2;
+  const int cta = blockIdx.x;
+  const bool split = cta >= whole;  // a segment of a split item
+  const int item = split ? whole + (cta - whole) / nseg : cta;
+  const int seg = split ? (cta - whole) % nseg : 0;
+  const int b = item / npairs, pair = item % npairs;
   const int hb0 = 2 * pair, nh = min(2, H - hb0);  // the CTA's heads hb0, hb0 + 1
-  const int c_begin = seg * cps, ncl = min(nc, c_begin + cps) - c_begin;
+  const int c_begin = split ? seg * cps : 0;
+  const int ncl = split ? min(nc, c_begin + cps) - c_begin : nc;
   const int nstages = 2 * ncl;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -104,6 +123,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tslot;
+  // the kernels after this one may start their set-up (they wait for its end)
+  grid_dep_trigger();
 
   if (warp >= kShTables) {
     // ================================================================ tables
@@ -123,6 +144,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
 #pragma unroll
       for (int e = 0; e < PER; ++e) zz[e] = t0 + e < T ? uh[t0 + e] : 0.f;
     };
+    grid_dep_wait();  // u comes from dt_decay_kernel, which may still be running
     if (ncl > 0 && mine) fetch(0, zn);
     for (int lc = 0; lc < ncl; ++lc) {
       const int s = lc % L::kTabBufs, c = c_begin + lc;
@@ -153,18 +175,21 @@ __global__ void __launch_bounds__(kShThreads, 1)
         for (int e = 0; e < PER; ++e) tw[lane * PER + e] = ex2_approx(a_last - (v[e] + base));
         if (lane == 0) {
           const float decay = ex2_approx(a_last);
+          const bool scaled = flags && scaled_form_ok(a_last);
+          const float f = scaled ? ex2_approx(scaled_form_ref(a_last)) : 1.f;
           dec[2 * s + hh] = decay;
-          const int64_t bh = static_cast<int64_t>(b) * H + h;
-          if (flags) flags[(static_cast<int64_t>(b) * nc + c) * H + h] = a_last >= -kScaledRange;
-          if (Dc) Dc[bh * nc + c] = prod;
+          hsc[2 * s + hh] = f;
+          const int64_t rel = static_cast<int64_t>(b) * H + h - bh0;  // split items only
+          if (flags) flags[(static_cast<int64_t>(b) * nc + c) * H + h] = scaled;
+          if (split) Dc[rel * nc + c] = prod * f;
           prod *= decay;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kShTabFull0 + s]);
     }
-    if (mine && lane == 0 && nseg > 1 && Lseg)
-      Lseg[(static_cast<int64_t>(b) * H + h) * nseg + seg] = prod;
+    if (mine && lane == 0 && split)
+      Lseg[(static_cast<int64_t>(b) * H + h - bh0) * nseg + seg] = prod;
   } else if (warp == kShControl) {
     // ================================================================ control
     if (lane == 0 && nstages > 0) {
@@ -262,15 +287,16 @@ __global__ void __launch_bounds__(kShThreads, 1)
       // the next chunk's x first, so that its MMAs queue behind this chunk's
       if (lc + 1 < ncl && !(ok = tables_ready(lc + 1) && scale(2 * lc + 2) && scale(2 * lc + 3)))
         break;
-      // the state entering chunk c -> Hin (bf16)
+      // the state entering chunk c -> Hin (bf16), times the scan's factor
       if (valid) {
+        const float f = hsc[2 * (lc % L::kTabBufs) + hh];
         __nv_bfloat16 *dst =
             Hin + (((static_cast<int64_t>(b) * nc + c) * H + h) * N + n) * P + p0;
 #pragma unroll
         for (int e = 0; e < 32; e += 8)
-          *reinterpret_cast<uint4 *>(dst + e) =
-              make_uint4(pack_bf16x2(st[e], st[e + 1]), pack_bf16x2(st[e + 2], st[e + 3]),
-                         pack_bf16x2(st[e + 4], st[e + 5]), pack_bf16x2(st[e + 6], st[e + 7]));
+          *reinterpret_cast<uint4 *>(dst + e) = make_uint4(
+              pack_bf16x2(f * st[e], f * st[e + 1]), pack_bf16x2(f * st[e + 2], f * st[e + 3]),
+              pack_bf16x2(f * st[e + 4], f * st[e + 5]), pack_bf16x2(f * st[e + 6], f * st[e + 7]));
       }
       // fold chunk c: state = decay * state + S_c
       bool w = mbar_wait(&bars[kShAccFull0 + (lc & 1)], (lc >> 1) & 1, abort_flag);
@@ -289,10 +315,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
       }
     }
     // the sequence's final state, or this segment's (from its own start state)
-    if (ok && valid && (nseg > 1 || h_final)) {
-      float *fin = nseg == 1 ? h_final + srow
-                             : Fseg + ((static_cast<int64_t>(b) * H + h) * nseg + seg) * N * P +
-                                   static_cast<int64_t>(n) * P + p0;
+    if (ok && valid && (split || h_final)) {
+      float *fin = !split ? h_final + srow
+                          : Fseg + ((static_cast<int64_t>(b) * H + h - bh0) * nseg + seg) * N * P +
+                                static_cast<int64_t>(n) * P + p0;
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
         *reinterpret_cast<float4 *>(fin + e) = make_float4(st[e], st[e + 1], st[e + 2], st[e + 3]);
@@ -308,37 +334,43 @@ __global__ void __launch_bounds__(kShThreads, 1)
 //   u[b, h, t] = softplus(dt[b, t, h]) * A_h * log2(e)
 // (the modified A factors of the Mamba-2 page, section "SSD算法", in log2
 // units), written with each head's tokens contiguous so that a table warp
-// reads a chunk of one head in 1 KB.  A 32-token x 32-head tile per block
-// through shared memory (reads coalesced over heads, writes over tokens).
-// grid (ceil(T / 32), ceil(H / 32), batch), 256 threads.
+// reads a chunk of one head in 1 KB.  A block transposes a tile of 32 tokens
+// x up to kDtHeads heads through shared memory: the tile's rows are
+// contiguous in dt, so every thread issues all of its loads (up to 16) before
+// the first store; the stores run over tokens, 128 bytes per warp.
+// grid (ceil(T / 32), ceil(H / kDtHeads), batch), 256 threads.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) dt_decay_kernel(const float *__restrict__ dt,
-                                                       const float *__restrict__ A,
-                                                       float *__restrict__ u, int64_t T, int H,
-                                                       int softplus) {
-  __shared__ float tile[32][33];
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
-  const int h0 = blockIdx.y * 32, b = blockIdx.z;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+constexpr int kDtHeads = 128;
+
+__global__ void __launch_bounds__(256, 4) dt_decay_kernel(const float *__restrict__ dt,
+                                                          const float *__restrict__ A,
+                                                          float *__restrict__ u, int64_t T, int H,
+                                                          int softplus) {
+  __shared__ float tile[32][kDtHeads + 1];
+  constexpr int kPer = 32 * kDtHeads / 256;
   constexpr float kLog2e = 1.4426950408889634f;
+  grid_dep_trigger();  // the chunk-state kernel may start loading x and B
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int h0 = blockIdx.y * kDtHeads, b = blockIdx.z;
+  const int hc = min(kDtHeads, H - h0);
+  const int tc = T - t0 < 32 ? static_cast<int>(T - t0) : 32;
+  const int n = tc * hc;
+  const float *src = dt + (static_cast<int64_t>(b) * T + t0) * H + h0;
+  float z[kPer];
 #pragma unroll
-  for (int r = ty; r < 32; r += 8) {
-    const int64_t t = t0 + r;
-    const int h = h0 + tx;
-    float v = 0.f;
-    if (t < T && h < H) {
-      const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
-      v = (softplus ? softplus_f32(z) : z) * A[h] * kLog2e;
-    }
-    tile[r][tx] = v;
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + 256 * k, t = i / hc, h = i - t * hc;
+    z[k] = i < n ? src[static_cast<int64_t>(t) * H + h] : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + 256 * k, t = i / hc, h = i - t * hc;
+    if (i < n) tile[t][h] = (softplus ? softplus_f32(z[k]) : z[k]) * A[h0 + h] * kLog2e;
   }
   __syncthreads();
-#pragma unroll
-  for (int r = ty; r < 32; r += 8) {
-    const int h = h0 + r;
-    const int64_t t = t0 + tx;
-    if (h < H && t < T) u[(static_cast<int64_t>(b) * H + h) * T + t] = tile[tx][r];
-  }
+  const int tx = threadIdx.x & 31;
+  for (int h = threadIdx.x >> 5; h < hc; h += 8)
+    if (tx < tc) u[(static_cast<int64_t>(b) * H + h0 + h) * T + t0 + tx] = tile[tx][h];
 }
 
 }  // namespace ssd

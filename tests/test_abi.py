@@ -39,8 +39,14 @@ def test_workspace_size_layout():
     # tensor-core path: the bf16 chunk initial states; one (B, C) group with
     # 256-token chunks of 64-wide heads adds one byte per (batch, chunk, head)
     # (whether the head-pair chunk scan takes that unit) and the per-token
-    # log2 decays [b, H, T] in float32
-    assert S.ssd_fwd_workspace_size(d, 256) == st * 2 + 8 * nc * 80 + 8 * 80 * 2048 * 4
+    # log2 decays [b, H, T] in float32.  Its 320 (batch, head pair) chunk-state
+    # items fill two waves of 148 SMs and 24 more: those 24 (batch 7, heads
+    # 32-79) run in four segments of two chunks, whose hand-off takes each
+    # segment's final state and decay and each chunk's decay product
+    rows, nseg = 48, 4
+    handoff = rows * nseg * 128 * 64 * 4 + rows * nseg * 4 + rows * nc * 4
+    assert S.ssd_fwd_workspace_size(d, 256) == \
+        st * 2 + handoff + 8 * nc * 80 + 8 * 80 * 2048 * 4
     d_g2 = _dims(ngroups_b=2, ngroups_c=2)
     assert S.ssd_fwd_workspace_size(d_g2, 256) == st * 2
     # float32 path: cumsums, chunk states and chunk initial states in float32
@@ -52,15 +58,19 @@ def test_workspace_size_layout():
 
 
 def test_stage_names_follow_the_path():
-    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(3)] == \
-        ["dt_decay", "chunk_state_hb", "chunk_scan_hb"]
+    # the last wave's chunk-state items split into segments: a fix-up stage
+    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(4)] == \
+        ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
+    # 37 x 40 head pairs = ten full waves of 148: no split, no fix-up
+    assert [S.ssd_fwd_stage_name(_dims(batch=37), 256, i) for i in range(4)] == \
+        ["dt_decay", "chunk_state_hb", "chunk_scan_hb", None]
     assert [S.ssd_fwd_stage_name(_dims(ngroups_c=2), 256, i) for i in range(2)] == \
         ["chunk_state_pass_tc", "chunk_scan_hl"]
     assert [S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, i) for i in range(4)] == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
     assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"
-    assert S.ssd_fwd_stage_name(_dims(), 256, 3) is None
-    assert S.ssd_fwd_num_stages(_dims(), 256) == 3
+    assert S.ssd_fwd_stage_name(_dims(), 256, 4) is None
+    assert S.ssd_fwd_num_stages(_dims(), 256) == 4
     assert S.ssd_fwd_num_stages(_dims(), 128) == 2
     assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
     # one long sequence over 80 heads: the state pass is split into sequence

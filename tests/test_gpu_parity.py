@@ -131,22 +131,41 @@ def test_fwd_small_pair_form(name, monkeypatch):
     check_fwd(shape, seed)
 
 
+def chunk_log2_decays(inp, Q):
+    """Total log2 decay of every (batch, chunk, head): sum over the chunk's
+    tokens of softplus(dt) A log2(e) (a property of the inputs, to check that
+    a test reaches the decay ranges it is meant to)."""
+    dt = inp["dt"].astype(np.float64)
+    sp = np.where(dt > 20, dt, np.log1p(np.exp(np.minimum(dt, 20))))
+    a = sp * inp["A"].astype(np.float64)[None, None, :] / np.log(2.0)
+    b, T, H = a.shape
+    nc = -(-T // Q)
+    a = np.pad(a, ((0, 0), (0, nc * Q - T), (0, 0)))
+    return a.reshape(b, nc, Q, H).sum(axis=2)
+
+
 @pytest.mark.parametrize("form", ["pair", "head"])
-@pytest.mark.parametrize("a_scale", [
-    (30.0, 1.0, 30.0, 1.0, 1.0),     # heads 0 and 2 decay past the scaled form's range
-    (30.0, 30.0, 30.0, 30.0, 30.0),  # every head does
-    (0.01, 0.01, 0.01, 0.01, 0.01),  # none does
+@pytest.mark.parametrize("a_scale,window", [
+    ((30.0, 1.0, 30.0, 1.0, 1.0), None),       # heads 0 and 2 decay past the scaled form's range
+    ((30.0, 30.0, 30.0, 30.0, 30.0), None),    # every head does
+    ((0.01, 0.01, 0.01, 0.01, 0.01), None),    # none does
+    ((2.5, 2.0, 1.5, 3.0, 1.0), (-192, -96)),  # decays needing a shifted reference
 ])
-def test_fwd_q256_long_decay_heads(a_scale, form, monkeypatch):
-    """256-token chunks of one group: heads whose in-chunk decay exceeds the
-    scaled form's range are flagged by the chunk-state kernel and computed one
-    by one in the head-pair launch; either way, and with the head-by-head
-    kernel throughout, every head's y and state match the oracle (odd head
-    count, so one pair has a single head; ragged last chunk; random h0)."""
+def test_fwd_q256_long_decay_heads(a_scale, window, form, monkeypatch):
+    """256-token chunks of one group: chunks whose total decay is below 2^-96
+    take the scaled form with a shifted reference (factors 2^(r - a_j) and
+    2^(a_i - r), the chunk state stored times 2^r); below 2^-192 they are
+    flagged by the chunk-state kernel and computed one by one in the head-pair
+    launch; either way, and with the head-by-head kernel throughout, every
+    head's y and state match the oracle (odd head count, so one pair has a
+    single head; ragged last chunk; random h0)."""
     monkeypatch.setenv("SSD_CHUNK_SCAN", form)
     shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 41)
     inp["A"] = (inp["A"] * np.asarray(a_scale, dtype=np.float32)).astype(np.float32)
+    if window:
+        al = chunk_log2_decays(inp, shape.chunk)
+        assert ((al > window[0]) & (al < window[1])).any(), al
     d = to_dev(inp, shape.io)
     y, hf = run_fwd(d, shape.chunk)
     pairs = list(range(shape.batch * shape.nheads))
@@ -156,6 +175,25 @@ def test_fwd_q256_long_decay_heads(a_scale, form, monkeypatch):
     eh = rel_err(h_pairs(hf, pairs, shape.nheads), h_ref)
     assert np.isfinite(ey) and ey <= TOL[synth.BF16], ey
     assert np.isfinite(eh) and eh <= TOL[synth.BF16], eh
+
+
+@pytest.mark.parametrize("form", ["pair", "head"])
+def test_fwd_q256_last_wave_split_into_segments(form, monkeypatch):
+    """4 x 40 head pairs on 148 SMs: the chunk-state kernel runs 148 items
+    whole and splits the last 12 (batch 3, heads 56-79) into sequence
+    segments joined by the fix-up; heads on both sides of the boundary match
+    the oracle (random h0 everywhere, so segment 0 of a split item starts
+    from it), with either chunk-scan form after it."""
+    monkeypatch.setenv("SSD_CHUNK_SCAN", form)
+    shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = S.make_dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate)
+    names = [S.ssd_fwd_stage_name(d, 256, i) for i in range(S.ssd_fwd_num_stages(d, 256))]
+    scan = "chunk_scan_hb" if form == "pair" else "chunk_scan_hl"
+    assert names == ["dt_decay", "chunk_state_hb", "state_fixup", scan]
+    H = shape.nheads
+    pairs = [0, 1, 2 * H + 79, 3 * H + 54, 3 * H + 55, 3 * H + 56, 3 * H + 57, 3 * H + 70,
+             3 * H + 79]
+    check_fwd(shape, 29, pairs=pairs)
 
 
 def test_fwd_tc_without_softplus_and_D():
