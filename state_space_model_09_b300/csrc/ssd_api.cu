@@ -479,6 +479,7 @@ constexpr int kFlaggedSets = 4;
 
 ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtensorMap &mB,
                           const CUtensorMap &mX, const CUtensorMap &mH, const CUtensorMap &mY,
+                          const CUtensorMap &mY128,
                           const float *dt, const float *A, const float *D, const float *u,
                           const uint8_t *flags, bool pdl, cudaStream_t s) {
   auto k = ssd::chunk_scan_hb;
@@ -495,7 +496,8 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
   const int64_t blocks = (static_cast<int64_t>(hb_ranges) + flagged_sets) * pl.nc * pl.b;
   if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
   return launch_dependent(pdl, k, dim3(static_cast<unsigned>(blocks)), dim3(ssd::kHbThreads),
-                          ssd::kHbLaunchBytes, s, mC32, mB, mX, mH, mY, dt, A, D, u, flags, pl.T,
+                          ssd::kHbLaunchBytes, s, mC32, mB, mX, mH, mY, mY128, dt, A, D, u, flags,
+                          pl.T,
                           static_cast<int>(pl.b), static_cast<int>(pl.H), pl.nc, pp, hb_ranges,
                           flagged_sets, pl.softplus);
 }
@@ -556,7 +558,9 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
         !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
       return SSD_ERR_CUDA;
     // chunk_state_hb reads B and x in 128-token halves
-    CUtensorMap mB128, mX128;
+    CUtensorMap mB128, mX128, mY128;
+    // chunk_scan_hb stores y in 128-row tiles
+    if (pl.hb && !encode_btgw(&mY128, y, pl.b, pl.T, pl.H, pl.P, 128)) return SSD_ERR_CUDA;
     if (pl.state_hb && (!encode_btgw(&mX128, x, pl.b, pl.T, pl.H, pl.P, 128) ||
                         !encode_btgw(&mB128, B, pl.b, pl.T, pl.GB, pl.N, 128)))
       return SSD_ERR_CUDA;
@@ -581,7 +585,8 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     if (st != SSD_OK) return st;
     const int se = ev + (pl.nseg > 1 ? 2 : 1);  // events index after the state stages
     record(events, se, s);
-    if (pl.hb) st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, dt, A, D, u, flags, pdl_on(events), s);
+    if (pl.hb)
+      st = launch_scan_hb(pl, mC32, mB, mX, mH, mY, mY128, dt, A, D, u, flags, pdl_on(events), s);
     else if (pl.Q == 256) st = launch_scan_hl<256, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else if (pl.P == 64) st = launch_scan_hl<128, 64>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);
     else st = launch_scan_hl<128, 128>(pl, mC32, mB, mX, mH, mY, dt, A, D, s);

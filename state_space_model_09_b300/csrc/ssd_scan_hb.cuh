@@ -38,17 +38,22 @@
 // operand of the C Hin product), 64 columns per 128-row tile, then Y of one
 // row tile for the two heads (128 columns, also the f32 scratch of each S
 // piece while the blocks are built).  Shared memory: two 64 KB buffers (C and
-// the B tile while S is built; then each head pair's scaled x, then its y for
-// the TMA stores) and two Hin pair buffers.  A pair's tile 1 (rows 128-255)
-// is computed and read out first; while tile 0's MMAs run, the compute warps
-// scale the next pair's x, which was loaded a pair earlier.
+// the B tile while S is built; then each head pair's scaled x) and two Hin
+// pair buffers.  A pair's tile 1 (rows 128-255) is computed and read out
+// first; while tile 0's MMAs run, the compute warps scale the next pair's x,
+// which was loaded a pair earlier.  y leaves by TMA stores, staged where
+// nothing else is needed any more: tile 1's rows in place of the x rows
+// 128-255 (tile 0's MMAs read only rows 0-127), tile 0's rows in the pair's
+// Hin buffer (both C Hin products are done by then).  So the x buffer is
+// free for the x two pairs ahead as soon as tile 0 is written, and the Hin
+// buffer once tile 0's store has read it.
 //
 // Warp roles: warps 0-15 build the S blocks, copy C, scale x and write y
 // (four per TMEM lane quarter); warp 16 (one lane) issues the C/B/Hin and the
 // first x loads and every MMA; warp 17 computes each pair's decay tables up
 // to two pairs ahead, fetching the next pair's u while it works; warp 18
-// (one lane) stores each pair's y and loads the x two pairs ahead.  Every
-// wait is bounded in time.
+// (one lane) stores each pair's y and loads the x and Hin two pairs ahead.
+// Every wait is bounded in time.
 #pragma once
 
 #include "ssd_scan.cuh"
@@ -79,7 +84,8 @@ struct ScanHB {
 
 enum : int {
   kHbCB = 0, kHbS, kHbConv, kHbX0, kHbX1, kHbH0, kHbH1, kHbXScaled, kHbM2, kHbYFree,
-  kHbYStaged, kHbTabFull0, kHbTabFull1, kHbTabEmpty0, kHbTabEmpty1, kNumHbBars
+  kHbYStaged, kHbTabFull0, kHbTabFull1, kHbTabEmpty0, kHbTabEmpty1, kHbY1Staged0, kHbY1Staged1,
+  kNumHbBars
 };
 static_assert(kNumHbBars <= ScanHB::kBars, "barrier slots");
 
@@ -117,7 +123,7 @@ __device__ __forceinline__ void hb_mask_pack(const float (&v)[32], int lim, uint
 // The body of one head-pair CTA: pair range bx of chunk c of batch row b.
 __device__ __forceinline__ void scan_hb_body(
     int bx, int c, int b, const CUtensorMap &mapC32, const CUtensorMap &mapB,
-    const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY,
+    const CUtensorMap &mapX, const CUtensorMap &mapH, const CUtensorMap &mapY128,
     const float *__restrict__ u, const float *__restrict__ D, const uint8_t *__restrict__ flags,
     int64_t T, int H, int nc, int pairs_per_cta) {
   using L = ScanHB;
@@ -143,7 +149,8 @@ __device__ __forceinline__ void scan_hb_body(
   if (tid == 0) {
     for (int i = 0; i < L::kBars; ++i) {
       const bool per_warp = i == kHbConv || i == kHbXScaled || i == kHbYFree ||
-                            i == kHbYStaged || i == kHbTabEmpty0 || i == kHbTabEmpty1;
+                            i == kHbYStaged || i == kHbTabEmpty0 || i == kHbTabEmpty1 ||
+                            i == kHbY1Staged0 || i == kHbY1Staged1;
       mbar_init(&bars[i], per_warp ? CW : 1);
     }
     *abort_flag = 0;
@@ -163,6 +170,16 @@ __device__ __forceinline__ void scan_hb_body(
     for (int hh = 0; hh < n; ++hh)
       tma_load_4d(Xs + (pr & 1) * L::kXS + hh * Q * 128, &mapX, bar, 0, h_begin + 2 * pr + hh,
                   c * Q, b);
+  };
+
+  // chunk states of pair pr into Hin buffer pr & 1 (issued by one thread)
+  auto load_h = [&](int pr) {
+    const int n = nheads_of(pr);
+    uint64_t *bar = &bars[kHbH0 + (pr & 1)];
+    mbar_arrive_expect_tx(bar, n * P * N * 2);
+    for (int hh = 0; hh < n; ++hh)
+      tma_load_3d(Hb + (pr & 1) * L::kH + hh * N * 128, &mapH, bar, 0, 0,
+                  (b * nc + c) * H + h_begin + 2 * pr + hh);
   };
 
   if (warp == kScanAuxWarp) {
@@ -243,15 +260,27 @@ __device__ __forceinline__ void scan_hb_body(
   } else if (warp == kHbStoreWarp) {
     // ================================================================ y out, x in
     if (lane == 0) {
+      const bool tile1 = static_cast<int64_t>(c) * Q + 128 < T;  // rows 128-255 exist
       for (int pr = 0; pr < npairs; ++pr) {
-        if (!mbar_wait(&bars[kHbYStaged], pr & 1, abort_flag) || *abort_flag) break;
-        uint8_t *xb = Xs + (pr & 1) * L::kXS;
-        for (int hh = 0; hh < nheads_of(pr); ++hh)
+        const int s = pr & 1, n = nheads_of(pr);
+        // tile 1 (rows 128-255), staged in the x buffer
+        if (!mbar_wait(&bars[kHbY1Staged0 + s], (pr >> 1) & 1, abort_flag) || *abort_flag) break;
+        for (int hh = 0; hh < n && tile1; ++hh)
           if (modes[2 * pr + hh])
-            tma_store_4d(&mapY, xb + hh * Q * 128, 0, h_begin + 2 * pr + hh, c * Q, b);
+            tma_store_4d(&mapY128, Xs + s * L::kXS + hh * Q * 128 + 128 * 128, 0,
+                         h_begin + 2 * pr + hh, c * Q + 128, b);
         bulk_commit();
-        bulk_wait_read0();
-        if (pr + 2 < npairs) load_x(pr + 2);  // the buffer is free again
+        // tile 0 (rows 0-127), staged in the Hin buffer
+        if (!mbar_wait(&bars[kHbYStaged], pr & 1, abort_flag) || *abort_flag) break;
+        for (int hh = 0; hh < n; ++hh)
+          if (modes[2 * pr + hh])
+            tma_store_4d(&mapY128, Hb + s * L::kH + hh * N * 128, 0, h_begin + 2 * pr + hh,
+                         c * Q, b);
+        bulk_commit();
+        bulk_wait_read1();  // tile 1's store has read the x buffer
+        if (pr + 2 < npairs) load_x(pr + 2);
+        bulk_wait_read0();  // tile 0's store has read the Hin buffer
+        if (pr + 2 < npairs) load_h(pr + 2);
       }
       bulk_wait_all();
     }
@@ -263,17 +292,8 @@ __device__ __forceinline__ void scan_hb_body(
       prefetch_tensormap(&mapB);
       prefetch_tensormap(&mapH);
       prefetch_tensormap(&mapX);
-      prefetch_tensormap(&mapY);
+      prefetch_tensormap(&mapY128);
       const uint32_t xs = smem_u32(Xs), hb = smem_u32(Hb);
-      const int hrow = (b * nc + c) * H;
-      auto load_h = [&](int pr) {
-        const int n = nheads_of(pr);
-        uint64_t *bar = &bars[kHbH0 + (pr & 1)];
-        mbar_arrive_expect_tx(bar, n * P * N * 2);
-        for (int hh = 0; hh < n; ++hh)
-          tma_load_3d(Hb + (pr & 1) * L::kH + hh * N * 128, &mapH, bar, 0, 0,
-                      hrow + h_begin + 2 * pr + hh);
-      };
       // C into buffer 0, B into buffer 1 (one group: group index 0)
       mbar_arrive_expect_tx(&bars[kHbCB], 2 * L::kXS);
 #pragma unroll
@@ -346,11 +366,6 @@ __device__ __forceinline__ void scan_hb_body(
           mma_bf16_tmem_a(tmem + L::kY, tmem + L::kA00 + 8 * ks,
                           sdesc_sw128(xk + ks * 2048, Q * 128, 1024), idesc_y, 1u);
         mma_commit(&bars[kHbM2]);
-        // the Hin buffer takes pair pr + 2 once these MMAs are done
-        if (pr + 2 < npairs) {
-          if (!mbar_wait(&bars[kHbM2], 1, abort_flag)) break;
-          load_h(pr + 2);
-        }
       }
     }
     __syncwarp();
@@ -426,13 +441,16 @@ __device__ __forceinline__ void scan_hb_body(
       if (lane == 0) mbar_arrive(&bars[kHbTabEmpty0 + s]);
       return true;
     };
-    // y rows of row tile t of pair pr = 2^a_i (Y + D x~) -> bf16, in place of x~
+    // y rows of row tile t of pair pr = 2^(a_i - r) (Y + D x~) -> bf16, staged
+    // for the TMA stores: tile 1 in place of x~, tile 0 in the Hin buffer
     auto output = [&](int pr, int t, const float (&ee)[2][2], const float (&dd)[2],
                       const float (&oo)[2]) -> bool {
       bool w = mbar_wait(&bars[kHbM2], t == 1 ? 0 : 1, abort_flag);
       if (!(__all_sync(0xffffffffu, w) && !*abort_flag)) return false;
       tc_fence_after_sync();
       uint8_t *xb = Xs + (pr & 1) * L::kXS;
+      uint8_t *yb = t == 1 ? xb : Hb + (pr & 1) * L::kH;  // [head][rows][128 B]
+      const int yhead = t == 1 ? Q * 128 : N * 128;
       const int i = 128 * t + r;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -442,8 +460,8 @@ __device__ __forceinline__ void scan_hb_body(
         const float f = ee[hh][t], d = dd[hh];
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          uint4 *p = reinterpret_cast<uint4 *>(xb + hh * Q * 128 + sw128_offset(i, 16 * hs + 8 * g));
-          const uint4 xv = *p;
+          const uint4 xv = *reinterpret_cast<const uint4 *>(
+              xb + hh * Q * 128 + sw128_offset(i, 16 * hs + 8 * g));
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
           uint32_t o[4];
 #pragma unroll
@@ -452,7 +470,8 @@ __device__ __forceinline__ void scan_hb_body(
             o[k] = pack_bf16x2(f * fmaf(d, xf.x, v[8 * g + 2 * k]),
                                f * fmaf(d, xf.y, v[8 * g + 2 * k + 1]));
           }
-          *p = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4 *>(yb + hh * yhead + sw128_offset(t == 1 ? i : r, 16 * hs + 8 * g)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
       tc_fence_before_sync();
@@ -460,7 +479,7 @@ __device__ __forceinline__ void scan_hb_body(
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[kHbYFree]);
-        if (t == 0) mbar_arrive(&bars[kHbYStaged]);
+        mbar_arrive(&bars[t == 0 ? kHbYStaged : kHbY1Staged0 + (pr & 1)]);
       }
       return true;
     };
@@ -492,7 +511,8 @@ __global__ void __launch_bounds__(kHbThreads, 1)
                   const __grid_constant__ CUtensorMap mapB,
                   const __grid_constant__ CUtensorMap mapX,
                   const __grid_constant__ CUtensorMap mapH,
-                  const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                  const __grid_constant__ CUtensorMap mapY,
+                  const __grid_constant__ CUtensorMap mapY128, const float *__restrict__ dt,
                   const float *__restrict__ A, const float *__restrict__ D,
                   const float *__restrict__ u, const uint8_t *__restrict__ flags, int64_t T,
                   int batch, int H, int nc, int pairs_per_cta, int hb_ranges,
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__(kHbThreads, 1)
   if (i < n_hb) {
     scan_hb_body(static_cast<int>(i % hb_ranges), static_cast<int>((i / hb_ranges) % nc),
                  static_cast<int>(i / (static_cast<int64_t>(hb_ranges) * nc)), mapC32, mapB, mapX,
-                 mapH, mapY, u, D, flags, T, H, nc, pairs_per_cta);
+                 mapH, mapY128, u, D, flags, T, H, nc, pairs_per_cta);
   } else {
     grid_dep_wait();  // the flags, u and the chunk states of the kernels before
     const int64_t j = i - n_hb;
