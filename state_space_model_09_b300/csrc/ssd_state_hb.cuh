@@ -281,24 +281,30 @@ __global__ void __launch_bounds__(kShThreads, 1)
       bool w = mbar_wait(&bars[kShTabFull0 + lc % L::kTabBufs], (lc / L::kTabBufs) & 1, abort_flag);
       return __all_sync(0xffffffffu, w) && !*abort_flag;
     };
-    bool ok = ncl > 0 && tables_ready(0) && scale(0) && scale(1);
+    // the state entering local chunk lc -> Hin (bf16), times the scan's factor;
+    // issued right after the fold that produced it, so that the stores drain
+    // while the next chunk's x is scaled (tables of lc are ready)
+    auto store_hin = [&](int lc) {
+      if (!valid) return;
+      const float f = hsc[2 * (lc % L::kTabBufs) + hh];
+      __nv_bfloat16 *dst =
+          Hin + (((static_cast<int64_t>(b) * nc + c_begin + lc) * H + h) * N + n) * P + p0;
+#pragma unroll
+      for (int e = 0; e < 32; e += 16) {
+        uint32_t v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = pack_bf16x2(f * st[e + 2 * k], f * st[e + 2 * k + 1]);
+        st_global_v8(dst + e, v);  // 32-byte aligned: row n, columns p0 + e
+      }
+    };
+    bool ok = ncl > 0 && tables_ready(0);
+    if (ok) store_hin(0);
+    ok = ok && scale(0) && scale(1);
     for (int lc = 0; lc < ncl && ok; ++lc) {
-      const int c = c_begin + lc;
       // the next chunk's x first, so that its MMAs queue behind this chunk's
       if (lc + 1 < ncl && !(ok = tables_ready(lc + 1) && scale(2 * lc + 2) && scale(2 * lc + 3)))
         break;
-      // the state entering chunk c -> Hin (bf16), times the scan's factor
-      if (valid) {
-        const float f = hsc[2 * (lc % L::kTabBufs) + hh];
-        __nv_bfloat16 *dst =
-            Hin + (((static_cast<int64_t>(b) * nc + c) * H + h) * N + n) * P + p0;
-#pragma unroll
-        for (int e = 0; e < 32; e += 8)
-          *reinterpret_cast<uint4 *>(dst + e) = make_uint4(
-              pack_bf16x2(f * st[e], f * st[e + 1]), pack_bf16x2(f * st[e + 2], f * st[e + 3]),
-              pack_bf16x2(f * st[e + 4], f * st[e + 5]), pack_bf16x2(f * st[e + 6], f * st[e + 7]));
-      }
-      // fold chunk c: state = decay * state + S_c
+      // fold local chunk lc: state = decay * state + S_c
       bool w = mbar_wait(&bars[kShAccFull0 + (lc & 1)], (lc >> 1) & 1, abort_flag);
       if (!(ok = __all_sync(0xffffffffu, w) && !*abort_flag)) break;
       tc_fence_after_sync();
@@ -313,6 +319,7 @@ __global__ void __launch_bounds__(kShThreads, 1)
         mbar_arrive(&bars[kShAccFree0 + (lc & 1)]);
         mbar_arrive(&bars[kShTabEmpty0 + lc % L::kTabBufs]);
       }
+      if (lc + 1 < ncl) store_hin(lc + 1);
     }
     // the sequence's final state, or this segment's (from its own start state)
     if (ok && valid && (split || h_final)) {
