@@ -47,13 +47,17 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_scan_hb", "mamba2_2p7b"):
-        (429_509_888, ("state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
-                       "state_space_model_09_b300/csrc/ssd_scan.cuh"),
-         "511c3d1048fa616c7c4ed6cb04127d203c983718"),
+        (416_868_864, ("state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
+                       "state_space_model_09_b300/csrc/ssd_scan.cuh",
+                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
+                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
+         "086b020b0454ae8776198ca967df3157fe5a090d"),
     ("chunk_state_hb", "mamba2_2p7b"):
-        (260_557_312, ("state_space_model_09_b300/csrc/ssd_state_hb.cuh",
-                       "state_space_model_09_b300/csrc/ssd_state.cuh"),
-         "5682630050785ed0ae1b705b8040edf3f517a587"),
+        (267_968_000, ("state_space_model_09_b300/csrc/ssd_state_hb.cuh",
+                       "state_space_model_09_b300/csrc/ssd_state.cuh",
+                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
+                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
+         "ac4a9900d54c465b0051ed738499256aa160ae17"),
     ("multistep_kernel", "multistep_k8"):
         (70_129_920, ("state_space_model_09_b300/csrc/ssd_kernels.cuh",),
          "f1267a2133217f991f16eac81edf77c2e16126eb"),
