@@ -102,7 +102,11 @@ size_t ssd_fwd_workspace_size(const ssd_dims *dims, int32_t chunk);
  * can be computed two heads per MMA in a scaled form (chunk_scan_hb) or head
  * by head (chunk_scan_hl); the call picks by the work per CTA.  The
  * environment variable SSD_CHUNK_SCAN=pair or =head, read on every call,
- * forces one of the two (results agree within the stated tolerance). */
+ * forces one of the two (results agree within the stated tolerance).  On
+ * that path the kernels after the first are launched as programmatic
+ * dependents, so that each one's set-up overlaps the end of the one before;
+ * SSD_PDL=0 (read on every call) launches them one after another instead
+ * (bit-identical results). */
 ssd_status ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                    const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
                    void *y, float *h_final, void *workspace, size_t workspace_bytes,
