@@ -282,6 +282,42 @@ def test_fwd_graph_replay_equals_eager(shape, seed):
         assert torch.equal(y, y_ref) and torch.equal(hf, h_ref)
 
 
+def test_fwd_head_pair_path_graph_and_serial_launch_agree(monkeypatch):
+    """The head-pair path with a split last wave (dt_decay, chunk_state_hb,
+    state_fixup, chunk_scan_hb, each after the first a programmatic dependent
+    of the one before): eager, replayed from a CUDA graph, and launched one
+    after another (SSD_PDL=0) give the same bits."""
+    monkeypatch.setenv("SSD_CHUNK_SCAN", "pair")
+    shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = to_dev(synth.make_fwd_inputs(shape, 56), shape.io)
+    y_ref, h_ref = run_fwd(d, 256)
+    monkeypatch.setenv("SSD_PDL", "0")
+    y_ser, h_ser = run_fwd(d, 256)
+    assert torch.equal(y_ser, y_ref) and torch.equal(h_ser, h_ref)
+    monkeypatch.delenv("SSD_PDL")
+    b, T, H, P = d["x"].shape
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    ws = S.workspace_for(dims, 256)
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((b, H, d["B"].shape[3], P), device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], 256, y, hf, ws,
+                  stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], 256, y, hf, ws,
+                  stream=stream)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        hf.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        S.ssd_check_device_error()
+        assert torch.equal(y, y_ref) and torch.equal(hf, h_ref)
+
+
 def test_fwd_profiled_events():
     shape = synth.WORKLOADS["tiny_f32"]
     d = to_dev(synth.make_fwd_inputs(shape, 1000), shape.io)
