@@ -51,7 +51,7 @@ MEASURED_TRAFFIC = {
                        "state_space_model_09_b300/csrc/ssd_scan.cuh",
                        "state_space_model_09_b300/csrc/ssd_tc.cuh",
                        "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "086b020b0454ae8776198ca967df3157fe5a090d"),
+         "f24fd1932ca4eee3cbb093f1d28f1136a52d4a55"),
     ("chunk_state_hb", "mamba2_2p7b"):
         (267_968_000, ("state_space_model_09_b300/csrc/ssd_state_hb.cuh",
                        "state_space_model_09_b300/csrc/ssd_state.cuh",

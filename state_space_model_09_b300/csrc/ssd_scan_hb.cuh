@@ -45,8 +45,9 @@
 // nothing else is needed any more: tile 1's rows in place of the x rows
 // 128-255 (tile 0's MMAs read only rows 0-127), tile 0's rows in the pair's
 // Hin buffer (both C Hin products are done by then).  So the x buffer is
-// free for the x two pairs ahead as soon as tile 0 is written, and the Hin
-// buffer once tile 0's store has read it.
+// free for the x two pairs ahead once tile 0 is written and tile 1's store
+// (issued a tile earlier) has read its rows, and the Hin buffer once tile 0's
+// store has read it.
 //
 // Warp roles: warps 0-15 build the S blocks, copy C, scale x and write y
 // (four per TMEM lane quarter); warp 16 (one lane) issues the C/B/Hin and the
