@@ -570,8 +570,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
     float *u = nullptr;
     if (pl.state_hb) {
       u = reinterpret_cast<float *>(ws + pl.u_off);
-      dim3 g((pl.T + 31) / 32, static_cast<unsigned>((pl.H + ssd::kDtHeads - 1) / ssd::kDtHeads),
-             static_cast<unsigned>(pl.b));
+      dim3 g((pl.T + 31) / 32, static_cast<unsigned>((pl.H + 31) / 32), static_cast<unsigned>(pl.b));
       ssd::dt_decay_kernel<<<g, 256, 0, s>>>(dt, A, u, pl.T, static_cast<int>(pl.H), pl.softplus);
       if ((st = launch_status()) != SSD_OK) return st;
       record(events, ++ev, s);

@@ -341,43 +341,40 @@ __global__ void __launch_bounds__(kShThreads, 1)
 //   u[b, h, t] = softplus(dt[b, t, h]) * A_h * log2(e)
 // (the modified A factors of the Mamba-2 page, section "SSD算法", in log2
 // units), written with each head's tokens contiguous so that a table warp
-// reads a chunk of one head in 1 KB.  A block transposes a tile of 32 tokens
-// x up to kDtHeads heads through shared memory: the tile's rows are
-// contiguous in dt, so every thread issues all of its loads (up to 16) before
-// the first store; the stores run over tokens, 128 bytes per warp.
-// grid (ceil(T / 32), ceil(H / kDtHeads), batch), 256 threads.
+// reads a chunk of one head in 1 KB.  A 32-token x 32-head tile per block
+// through shared memory (reads coalesced over heads, writes over tokens).
+// (A tile of 32 tokens x all heads per block, one wave of 512 blocks at the
+// 2.7B shape, measured slower: 10.4 against 8.7 us.)
+// grid (ceil(T / 32), ceil(H / 32), batch), 256 threads.
 // ----------------------------------------------------------------------------
-constexpr int kDtHeads = 128;
-
-__global__ void __launch_bounds__(256, 4) dt_decay_kernel(const float *__restrict__ dt,
-                                                          const float *__restrict__ A,
-                                                          float *__restrict__ u, int64_t T, int H,
-                                                          int softplus) {
-  __shared__ float tile[32][kDtHeads + 1];
-  constexpr int kPer = 32 * kDtHeads / 256;
+__global__ void __launch_bounds__(256) dt_decay_kernel(const float *__restrict__ dt,
+                                                       const float *__restrict__ A,
+                                                       float *__restrict__ u, int64_t T, int H,
+                                                       int softplus) {
+  __shared__ float tile[32][33];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int h0 = blockIdx.y * 32, b = blockIdx.z;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   constexpr float kLog2e = 1.4426950408889634f;
   grid_dep_trigger();  // the chunk-state kernel may start loading x and B
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
-  const int h0 = blockIdx.y * kDtHeads, b = blockIdx.z;
-  const int hc = min(kDtHeads, H - h0);
-  const int tc = T - t0 < 32 ? static_cast<int>(T - t0) : 32;
-  const int n = tc * hc;
-  const float *src = dt + (static_cast<int64_t>(b) * T + t0) * H + h0;
-  float z[kPer];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x + 256 * k, t = i / hc, h = i - t * hc;
-    z[k] = i < n ? src[static_cast<int64_t>(t) * H + h] : 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x + 256 * k, t = i / hc, h = i - t * hc;
-    if (i < n) tile[t][h] = (softplus ? softplus_f32(z[k]) : z[k]) * A[h0 + h] * kLog2e;
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t t = t0 + r;
+    const int h = h0 + tx;
+    float v = 0.f;
+    if (t < T && h < H) {
+      const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
+      v = (softplus ? softplus_f32(z) : z) * A[h] * kLog2e;
+    }
+    tile[r][tx] = v;
   }
   __syncthreads();
-  const int tx = threadIdx.x & 31;
-  for (int h = threadIdx.x >> 5; h < hc; h += 8)
-    if (tx < tc) u[(static_cast<int64_t>(b) * H + h0 + h) * T + t0 + tx] = tile[tx][h];
+#pragma unroll
+  for (int r = ty; r < 32; r += 8) {
+    const int h = h0 + r;
+    const int64_t t = t0 + tx;
+    if (h < H && t < T) u[(static_cast<int64_t>(b) * H + h) * T + t] = tile[tx][r];
+  }
 }
 
 }  // namespace ssd
