@@ -57,7 +57,7 @@ MEASURED_TRAFFIC = {
                        "state_space_model_09_b300/csrc/ssd_state.cuh",
                        "state_space_model_09_b300/csrc/ssd_tc.cuh",
                        "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "ac4a9900d54c465b0051ed738499256aa160ae17"),
+         "22cac97fdd2d9cfda95adf1a30d34cbaae2c66ea"),
     ("multistep_kernel", "multistep_k8"):
         (70_129_920, ("state_space_model_09_b300/csrc/ssd_kernels.cuh",),
          "f1267a2133217f991f16eac81edf77c2e16126eb"),
