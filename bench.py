@@ -1,13 +1,17 @@
-"""Benchmark of the SSD prefill (and, on request, the multi-step decode).
+"""Benchmark of the SSD prefill and the multi-step decode.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mamba2_2p7b|long_16k|hybrid_llama3_8b|tiny_f32|multistep_k8]
 
-One step = one ssd_fwd call over the whole workload (all four kernels of the
+One step = one ssd_fwd call over the whole workload (every kernel of the
 chunked algorithm) with inputs resident in HBM.  Default workload: one Mamba-2
 2.7B SSD layer (batch 8, T 2048, 80 heads, P 64, N 128, chunk 256, bf16 I/O,
 fp32 state), synthetic seeded inputs.  Metric: tokens x heads per second,
-reported in M tok*heads/s, plus the fraction of the layer's roofline.
+reported in M tok*heads/s, plus the fraction of the layer's roofline
+(mandatory I/O over the measured HBM bandwidth).  The K timed steps are one
+CUDA graph, replayed until at least one second of device time is measured;
+ms_per_step is the median over the replays.  At N = 1 the default line also
+carries the other four workloads (`workloads`), each measured the same way.
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the layer has no exchange between (batch, head) pairs); rank 0 prints one
@@ -92,6 +96,9 @@ def peaks():
     return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
 
 
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s nominal HBM3e figure quoted for the decode target
+
+
 # ----------------------------------------------------------------------------- work model
 def hb_fast_fraction(s: synth.FwdShape, inp) -> float:
     """Share of (batch, chunk, head) units whose in-chunk decay stays within the
@@ -116,7 +123,12 @@ def fwd_work(s: synth.FwdShape):
     h_final (f32).  Flops count causal work only: P*Q(Q+1) (masked scores times
     x), 2QNP (chunk state), 2QNP (output from the initial state) per
     (b, chunk, head), plus N*Q(Q+1) per (b, chunk, distinct B/C group pair) for
-    C B^T.  Stage bytes count each stage's own inputs and outputs once."""
+    C B^T.
+
+    Per stage: `mandatory` = the part of the layer's mandatory I/O the stage
+    reads or writes (dt counts for the stages that read its per-token decays);
+    `io` = everything the stage moves once, intermediates (chunk states, the
+    decays) included; `flops` its causal tensor work."""
     io = 2 if s.io == synth.BF16 else 4
     b, T, H, P, N, Q = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.chunk
     nc = math.ceil(T / Q)
@@ -134,19 +146,24 @@ def fwd_work(s: synth.FwdShape):
     hin16 = b * nc * H * N * P * 2
     f_state = 2 * b * nc * H * Q * N * P
     f_scan = b * nc * H * (P * Q * (Q + 1) + 2 * Q * N * P) + b * nc * pairs * N * Q * (Q + 1)
+
+    def stage(mandatory, io_bytes, fl):
+        return dict(mandatory=mandatory, io=io_bytes, flops=fl)
+
     stages = {
-        "chunk_state_pass_tc": (x + Bb + dt + h0 + hin16 + st, f_state),
-        "chunk_scan_hl": (x + Bb + Cb + dt + hin16 + x, f_scan),
-        "state_fixup": (2 * hin16 + st, 0),  # bound: every head split
-        "dt_cumsum": (dt + cs, 0),
-        "chunk_state_simt": (x + Bb + cs + S32, f_state),
-        "state_passing": (S32 + b * H * nc * 4 + h0 + S32 + st, 2 * b * nc * H * N * P),
-        "chunk_scan_simt": (x + Bb + Cb + cs + S32 + x, f_scan),
+        "dt_decay": stage(dt, 2 * dt, 0),
+        "chunk_state_pass_tc": stage(x + Bb + dt + h0 + st, x + Bb + dt + h0 + hin16 + st, f_state),
+        "chunk_scan_hl": stage(2 * x + Bb + Cb + dt, 2 * x + Bb + Cb + dt + hin16, f_scan),
+        "state_fixup": stage(0, 2 * hin16 + st, 0),  # bound: every head split
+        "dt_cumsum": stage(dt, dt + cs, 0),
+        "chunk_state_simt": stage(x + Bb, x + Bb + cs + S32, f_state),
+        "state_passing": stage(h0 + st, 2 * S32 + b * H * nc * 4 + h0 + st,
+                               2 * b * nc * H * N * P),
+        "chunk_scan_simt": stage(2 * x + Bb + Cb, 2 * x + Bb + Cb + cs + S32, f_scan),
     }
     # the head-pair kernels: the same inputs and outputs
     stages["chunk_scan_hb"] = stages["chunk_scan_hl"]
     stages["chunk_state_hb"] = stages["chunk_state_pass_tc"]
-    stages["dt_decay"] = (2 * dt, 0)  # dt in, the per-head log2 decays out
     return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 
@@ -265,6 +282,21 @@ def cpu_baseline(shape, inp, budget_s=20.0):
                       % (n, total, shape.seqlen, t)}
 
 
+def config_of(workload, shape, world):
+    """The workload named by its sizes; identical in both arms."""
+    if isinstance(shape, synth.MultistepShape):
+        return {"workload": workload, "batch": shape.batch, "K": shape.K,
+                "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                "ngroups_b": shape.ngroups_b, "ngroups_c": shape.ngroups_c,
+                "io": "bf16" if shape.io == synth.BF16 else "f32", "state": "f32",
+                "chain": shape.steps, "parallelism": "replicas%d" % world}
+    return {"workload": workload, "batch": shape.batch, "seq_len": shape.seqlen,
+            "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+            "ngroups_b": shape.ngroups_b, "ngroups_c": shape.ngroups_c, "chunk": shape.chunk,
+            "io": "bf16" if shape.io == synth.BF16 else "f32", "state": "f32",
+            "h0": shape.h0, "parallelism": "replicas%d" % world}
+
+
 def run_reference(args, shape, work):
     """--impl reference: the fp64 oracle on bounded samples of the workload."""
     inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload])
@@ -286,7 +318,7 @@ def run_reference(args, shape, work):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "impl": "reference",
-            "config": config_of(args, shape, "cpu"),
+            "config": config_of(args.workload, shape, args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": min(cores, n),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -334,18 +366,19 @@ def oracle_multistep_chain(calls: int, budget_s: float):
     return n * shape.K / t / 1e6, t * 1e3, min(cores, n), sample
 
 
+MULTISTEP_METRIC = "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)"
+
+
 def run_reference_multistep(args):
     """--impl reference on multistep_k8: the oracle chain, one call per step."""
     shape = synth.WORKLOADS["multistep_k8"]
     value, ms, cores, sample = oracle_multistep_chain(args.warmup + args.steps, 150.0)
-    line = {"metric": "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)",
+    line = {"metric": MULTISTEP_METRIC,
             "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "impl": "reference",
-            "config": {"workload": "multistep_k8", "batch": shape.batch, "K": shape.K,
-                       "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                       "chain": shape.steps, "call": "oracle ssd_multistep"},
+            "config": config_of("multistep_k8", shape, args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -357,37 +390,71 @@ def n_copies(layer_bytes, dev=None):
     """Device copies of a prefill workload's inputs and outputs that the timed
     steps rotate over: enough to fill twice the L2 (one when a single copy
     already does)."""
-    l2 = 126 * 1024 * 1024
+    l2 = L2_BYTES
     if dev is not None:
         import torch
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size or l2
     return 1 if layer_bytes >= 2 * l2 else -(-2 * l2 // layer_bytes)
 
 
-def config_of(args, shape, where):
-    c = {"workload": args.workload, "batch": shape.batch, "seq_len": shape.seqlen,
-         "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-         "ngroups_b": shape.ngroups_b, "ngroups_c": shape.ngroups_c, "chunk": shape.chunk,
-         "io": "bf16" if shape.io == synth.BF16 else "f32", "state": "f32",
-         "h0": shape.h0, "parallelism": "replicas%d" % args.gpus}
-    if where == "gpu":
-        lb = fwd_work(shape)["layer_bytes"]
-        n = n_copies(lb)
-        c["l2"] = ("no flush; inputs+outputs %.0f MB > 2 x 126 MB L2" % (lb / 1e6) if n == 1 else
-                   "no flush; steps rotate over %d copies of the %.1f MB inputs+outputs (%.0f MB > 2 x L2)"
-                   % (n, lb / 1e6, n * lb / 1e6))
-        c["graph"] = True
-    return c
+def timed_replays(replay, steps, stream, min_s):
+    """Replays `replay` (which enqueues `steps` steps on `stream`) until at
+    least min_s of device time has been timed, each replay between two CUDA
+    events on the stream.  Returns (median ms per step, repeats)."""
+    import torch
+    per = []
+    total = 0.0
+    while total < min_s * 1e3 or len(per) < 5:
+        evs = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            replay()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            t = e0.elapsed_time(e1)
+            per.append(t / steps)
+            total += t
+    return statistics.median(per), len(per)
 
 
-# ----------------------------------------------------------------------------- our arm
-def run_ours(args, shape, work, world, rank, local):
+def roofline_of(name, st, seconds, pk, workload):
+    """The roofline entry of one kernel: mandatory I/O (the layer's x, y, B, C,
+    dt, h0, h_final that it moves) or causal tensor flops, per launch, over its
+    event-timed duration."""
+    t_hbm = st["mandatory"] / (pk["hbm"] * 1e9)
+    t_tc = st["flops"] / (pk["bf16"] * 1e12)
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": round(st["flops"] / seconds / 1e12, 2),
+                "peak": pk["bf16"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(st["mandatory"] / seconds / 1e9, 1),
+                "peak": pk["hbm"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = measured_traffic(name, workload)
+    roof["kernel"] = name
+    roof["algorithmic_bytes"] = st["mandatory"]
+    roof["algorithmic_flops"] = st["flops"]
+    roof["kernel_io_bytes"] = st["io"]
+    roof["kernel_io_frac"] = round(st["io"] / seconds / 1e9 / pk["hbm"], 4)
+    if roof["bound"] == "hbm":
+        roof["frac_vs_nominal_8tbs"] = round(st["mandatory"] / seconds / 1e9 / NOMINAL_HBM_GBS, 4)
+    roof["peak_source"] = pk["source"] + " (burst)"
+    return roof
+
+
+# ----------------------------------------------------------------------------- prefill
+def measure_prefill(workload, shape, args, world, rank, dev, min_s, e2e=True, cpu_budget=20.0):
+    """One prefill workload on this rank's GPU: the graph-replayed step, the
+    per-kernel event times, the end-to-end call from host buffers and (rank 0
+    at N = 1) the oracle on the host cores.  Returns the fields of its line."""
     import torch
     from state_space_model_09_b300 import ssd as S
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload] + 17 * rank)
+    work = fwd_work(shape)
+    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[workload] + 17 * rank)
     io_t = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
     host = {}
     for k, v in inp.items():
@@ -406,11 +473,11 @@ def run_ours(args, shape, work, world, rank, local):
     dims = S.dims_of(d["x"], d["B"], d["C"])
     ws = S.workspace_for(dims, shape.chunk, dev)
     # a stream of our own (graphs cannot be captured on the legacy default
-    # stream); every torch op below, the e2e copies included, runs on it
+    # stream); every torch op below runs on it
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
-    names = [S.ssd_fwd_stage_name(dims, shape.chunk, i) for i in range(S.ssd_fwd_num_stages(dims, shape.chunk))]
-    pair_share = hb_fast_fraction(shape, inp) if "chunk_scan_hb" in names else None
+    names = [S.ssd_fwd_stage_name(dims, shape.chunk, i)
+             for i in range(S.ssd_fwd_num_stages(dims, shape.chunk))]
 
     # Inputs smaller than twice the L2 are rotated over enough device copies
     # that every timed step reads data the previous steps have evicted.
@@ -430,39 +497,39 @@ def run_ours(args, shape, work, world, rank, local):
     torch.cuda.synchronize()
     S.ssd_check_device_error(stream)
     # the timed steps replay as CUDA graphs of up to 500 steps (no host launch gaps)
-    gsteps = min(args.steps, max(500, copies))
-    graphs = []
-    for n in ([gsteps] * (args.steps // gsteps) + ([args.steps % gsteps] if args.steps % gsteps else [])):
-        if graphs and graphs[-1][0] == n:
-            graphs.append(graphs[-1])
-            continue
+    K = args.steps
+    gsteps = min(K, max(500, copies))
+    sizes = [gsteps] * (K // gsteps) + ([K % gsteps] if K % gsteps else [])
+    graphs = {}
+    for n in set(sizes):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
                 step(i)
-        graphs.append((n, g))
+        graphs[n] = g
+
+    def replay():
+        for n in sizes:
+            graphs[n].replay()
+
     with torch.cuda.stream(stream):
         for i in range(copies):  # every copy once, so the first timed ones are out of L2
             step(i)
-        graphs[0][1].replay()
+        replay()
     torch.cuda.synchronize()
     S.ssd_check_device_error(stream)
 
-    # ---- timed region: K steps, barrier + synchronize on both sides
+    # ---- timed region: the K-step block replayed until >= min_s, barrier +
+    # synchronize on both sides; the median over the repeats
     clocks = ClockSampler(gpu_id_for(dev))
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _, g in graphs:
-            g.replay()
-        e1.record(stream)
+        ms, reps = timed_replays(replay, K, stream, min_s)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
     S.ssd_check_device_error(stream)
     ms = max_over_ranks(ms, world, dev)
 
@@ -470,7 +537,7 @@ def run_ours(args, shape, work, world, rank, local):
     # bounded device-side delay first lets the host queue every call, so no
     # stage waits on a launch
     nst = len(names)
-    ks = min(args.steps, 200)
+    ks = max(20, min(K, 200))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(ks)]
     with torch.cuda.stream(stream):
         torch.cuda._sleep(20_000_000)
@@ -479,81 +546,163 @@ def run_ours(args, shape, work, world, rank, local):
         S.ssd_fwd_profiled(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["h0"],
                            shape.chunk, yy, hh_, ww, evs[i], True, stream, dims)
     torch.cuda.synchronize()
-    stage_ms = [statistics.mean(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(ks))
+    stage_ms = [statistics.median(evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(ks))
                 for k in range(nst)]
 
-    # ---- end to end through the public API: pinned host inputs in, results out
-    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    hh = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
-    ke = max(3, min(args.steps, 50))
+    out = {"ms": ms, "repeats": reps, "clocks": clk, "names": names, "stage_ms": stage_ms,
+           "work": work, "launches": nst * K * reps}
+    if e2e:
+        out["e2e"] = e2e_prefill(S, shape, host, d, y, hf, ws, dims, stream, world, dev,
+                                 max(3, min(K, 50)))
+    if "chunk_scan_hb" in names:
+        out["pair_form_share"] = round(hb_fast_fraction(shape, inp), 4)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and cpu_budget > 0:
+        out["cpu_baseline"] = cpu_baseline(shape, inp, cpu_budget)
+    return out
 
-    def e2e_step():
-        for k in ("x", "dt", "A", "B", "C", "D", "h0"):
-            if host[k] is not None:
-                d[k].copy_(host[k], non_blocking=True)
-        step()
-        yh.copy_(y, non_blocking=True)
-        hh.copy_(hf, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
+def e2e_prefill(S, shape, host, d, y, hf, ws, dims, stream, world, dev, ke):
+    """End to end through the public API: every step copies its inputs in from
+    pinned host memory, runs ssd_fwd and copies y and h_final back.  Two device
+    sets of inputs and outputs let step i + 1's host-to-device copies (one
+    stream) run while step i computes and step i - 1's results come back
+    (another stream)."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dsets = [(d, y, hf), ({k: (None if v is None else torch.empty_like(v)) for k, v in d.items()},
+                          torch.empty_like(y), torch.empty_like(hf))]
+    outs_h = [(torch.empty(y.shape, dtype=y.dtype, pin_memory=True),
+               torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)) for _ in range(2)]
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "out", "done")}
+
+    def e2e_step(i):
+        k = i % 2
+        dd, yy, hh = dsets[k]
+        s_in.wait_event(ev["out"][k])  # step i - 2 has finished reading this input set
+        with torch.cuda.stream(s_in):
+            for name in ("x", "dt", "A", "B", "C", "D", "h0"):
+                if host[name] is not None:
+                    dd[name].copy_(host[name], non_blocking=True)
+            ev["in"][k].record(s_in)
+        stream.wait_event(ev["in"][k])
+        stream.wait_event(ev["done"][k])  # step i - 2's results have left this output set
+        S.ssd_fwd(dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["h0"], shape.chunk,
+                  yy, hh, ws, True, stream, dims)
+        ev["out"][k].record(stream)
+        s_out.wait_event(ev["out"][k])
+        with torch.cuda.stream(s_out):
+            outs_h[k][0].copy_(yy, non_blocking=True)
+            outs_h[k][1].copy_(hh, non_blocking=True)
+            ev["done"][k].record(s_out)
+
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(ke):
-        e2e_step()
+    s_in.wait_event(f0)
+    for i in range(ke):
+        e2e_step(i)
+    for k in range(2):
+        stream.wait_event(ev["done"][k])
     f1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / ke, world, dev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in host if host[k] is not None)
-    d2h = yh.numel() * yh.element_size() + hh.numel() * hh.element_size()
+    d2h = y.numel() * y.element_size() + hf.numel() * hf.element_size()
+    return {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    if rank != 0:
-        return
-    pk = peaks()
+
+def prefill_fields(workload, shape, m, world, pk):
+    """The JSON fields of a measured prefill workload."""
+    work = m["work"]
+    ms = m["ms"]
     value = world * work["tok_heads"] / (ms * 1e-3) / 1e6
+    names, stage_ms = m["names"], m["stage_ms"]
+    dom = int(np.argmax(stage_ms))
+    roof = roofline_of(names[dom], work["stages"][names[dom]], stage_ms[dom] * 1e-3, pk, workload)
     t_hbm = work["layer_bytes"] / (pk["hbm"] * 1e9)
     t_tc = work["flops"] / (pk["bf16"] * 1e12)
-    dom = int(np.argmax(stage_ms))
-    dom_bytes, dom_flops = work["stages"][names[dom]]
-    dom_s = stage_ms[dom] * 1e-3
-    if dom_flops / (pk["bf16"] * 1e12) > dom_bytes / (pk["hbm"] * 1e9):
-        roof = {"bound": "tensor", "achieved": round(dom_flops / dom_s / 1e12, 2),
-                "peak": pk["bf16"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": round(dom_bytes / dom_s / 1e9, 1), "peak": pk["hbm"],
-                "unit": "GB/s"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = measured_traffic(names[dom], args.workload)
-    roof["kernel"] = names[dom]
-    roof["algorithmic_bytes"] = dom_bytes
-    roof["algorithmic_flops"] = dom_flops
-    roof["peak_source"] = pk["source"] + " (burst)"
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
-        "config": dict(config_of(args, shape, "gpu"),
-                       **({"pair_form_share": round(pair_share, 4)} if pair_share is not None else {})),
+    f = {
+        "value": round(value, 2), "ms_per_step": round(ms, 5), "repeats": m["repeats"],
         "roofline": roof,
         "layer_roofline": {"bytes": work["layer_bytes"], "flops": work["flops"],
                            "t_bound_us": round(max(t_hbm, t_tc) * 1e6, 2),
                            "bound": "hbm" if t_hbm >= t_tc else "tensor",
                            "frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
-                           "peaks": "%s HBM %.1f GB/s, bf16 %.1f TFLOP/s" % (pk["source"], pk["hbm"], pk["bf16"])},
+                           "frac_vs_nominal_8tbs": round(
+                               work["layer_bytes"] / (NOMINAL_HBM_GBS * 1e9) / (ms * 1e-3), 4),
+                           "peaks": "%s HBM %.1f GB/s, bf16 %.1f TFLOP/s"
+                                    % (pk["source"], pk["hbm"], pk["bf16"])},
         "stages_ms": {n: round(t, 5) for n, t in zip(names, stage_ms)},
-        "gpu_launches": nst * args.steps,
-        "e2e": {"value": round(world * work["tok_heads"] / (e2e_ms * 1e-3) / 1e6, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
-        "clocks": clk,
+        "clocks": m["clocks"],
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shape, inp)
-    print(json.dumps(line, ensure_ascii=False))
+    if "pair_form_share" in m:
+        f["pair_form_share"] = m["pair_form_share"]
+    if "e2e" in m:
+        e = m["e2e"]
+        f["e2e"] = {"value": round(world * work["tok_heads"] / (e["ms_per_step"] * 1e-3) / 1e6, 2),
+                    "unit": UNIT, "h2d_bytes_per_step": e["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": e["d2h_bytes_per_step"],
+                    "ms_per_step": round(e["ms_per_step"], 4)}
+    if "cpu_baseline" in m:
+        f["cpu_baseline"] = m["cpu_baseline"]
+    return f
+
+
+def timing_note(work, K, dev=None):
+    lb = work["layer_bytes"]
+    n = n_copies(lb, dev)
+    l2 = ("no flush; inputs+outputs %.0f MB > 2 x 126 MB L2" % (lb / 1e6) if n == 1 else
+          "no flush; steps rotate over %d copies of the %.1f MB inputs+outputs (%.0f MB > 2 x L2)"
+          % (n, lb / 1e6, n * lb / 1e6))
+    return {"l2": l2, "graph": "CUDA graph of the %d steps, replayed until >= 1 s; "
+                              "ms_per_step = median over the replays" % K}
+
+
+EXTRA_WORKLOADS = ("long_16k", "hybrid_llama3_8b", "tiny_f32", "multistep_k8")
+
+
+def run_ours(args, shape, world, rank, local):
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    m = measure_prefill(args.workload, shape, args, world, rank, dev, args.min_seconds,
+                        e2e=True, cpu_budget=20.0)
+    # the other workloads of the layer, each measured the same way (N = 1 only)
+    extra = {}
+    if args.workload == "mamba2_2p7b" and world == 1 and not args.no_workloads:
+        for wl in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            if wl == "multistep_k8":
+                extra[wl] = multistep_summary(args, world, rank, local)
+            else:
+                s2 = synth.WORKLOADS[wl]
+                m2 = measure_prefill(wl, s2, args, world, rank, dev, args.min_seconds,
+                                     e2e=False, cpu_budget=6.0)
+                extra[wl] = dict(config_of(wl, s2, world), **prefill_fields(wl, s2, m2, world, peaks()))
+                extra[wl]["timing"] = timing_note(m2["work"], args.steps, dev)
+    if rank != 0:
+        return
+    pk = peaks()
+    f = prefill_fields(args.workload, shape, m, world, pk)
+    line = {
+        "metric": METRIC, "value": f.pop("value"), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": f.pop("ms_per_step"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
+        "config": config_of(args.workload, shape, world),
+        "timing": timing_note(m["work"], args.steps, dev),
+        "gpu_launches": m["launches"],
+        "peaks_used": {"hbm_gbs": pk["hbm"], "bf16_tflops": pk["bf16"],
+                       "bf16_tflops_sustained": pk["bf16_sus"], "source": pk["source"]},
+    }
+    line.update(f)
+    if extra:
+        line["workloads"] = extra
+    print(json.dumps(line, ensure_ascii=False), flush=True)
 
 
 # ----------------------------------------------------------------------------- multistep arm
@@ -602,6 +751,10 @@ def run_sequential(args, shape, world, rank, local):
         S.ssd_fwd_sequential(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
                              shape.chunk, args.window, y, hf, ws, True, stream, dims)
 
+    def block():
+        for _ in range(args.steps):
+            step()
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -610,15 +763,11 @@ def run_sequential(args, shape, world, rank, local):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    ms, reps = timed_replays(block, args.steps, stream, args.min_seconds)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms = max_over_ranks(ms, world, dev)
     S.ssd_check_device_error(stream)
     if rank != 0:
         return
@@ -626,25 +775,28 @@ def run_sequential(args, shape, world, rank, local):
         "metric": "SSD sequential prefill Mtok·heads/s (windows chained through the state)",
         "value": round(world * shape.tok_heads / (ms * 1e-3) / 1e6, 2), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "repeats": reps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
-        "config": dict(config_of(args, shape, "gpu"), window=args.window,
+        "config": dict(config_of(args.workload, shape, world), window=args.window,
                        workspace_bytes=nbytes,
                        whole_call_workspace_bytes=S.ssd_fwd_workspace_size(dims, shape.chunk)),
         "clocks": clk}), flush=True)
 
 
-def run_multistep(args, world, rank, local):
-    """One step = one ssd_multistep call of the speculative chain (each step
-    continues from h_j).  The chain of `shape.steps` calls is captured in a
-    CUDA graph and replayed; the time per call is the replay time / steps."""
+def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0, e2e=True):
+    """The speculative chain: each call continues from the previous call's h_j
+    (ssd_multistep) or from the next cache it stored (ssd_verify).  The
+    1000-call chain is captured in a CUDA graph and replayed until >= min_s;
+    ms per call = median replay time / calls.  With chains > 1, that many
+    independent chains (own states, the same drafts) run interleaved, call i of
+    every chain before call i + 1 of any: each call's cached state was then
+    written (chains - 1) calls earlier, which at 128 MB a call is beyond the
+    L2 for chains >= 3, so the states come from DRAM."""
     import torch
     from state_space_model_09_b300 import ssd as S
 
     shape = synth.WORKLOADS["multistep_k8"]
-    work = multistep_work(shape, args.verify)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    work = multistep_work(shape, verify)
     inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"] + 17 * rank)
     bf = torch.bfloat16
     X = torch.from_numpy(inp["x"]).to(bf).to(dev)
@@ -655,29 +807,28 @@ def run_multistep(args, world, rank, local):
     A = torch.from_numpy(inp["A"]).to(dev)
     D = torch.from_numpy(inp["D"]).to(dev)
     h0 = torch.from_numpy(inp["h_cache"]).to(dev)
-    bufs = [torch.empty_like(h0), torch.empty_like(h0)]
-    hK = torch.empty_like(h0)
-    Y = torch.empty_like(X)
+    st = [dict(bufs=[torch.empty_like(h0), torch.empty_like(h0)], hK=torch.empty_like(h0),
+               Y=torch.empty_like(X[0])) for _ in range(chains)]
     dims = S.dims_of(X[0], BB[0], CC[0])
     steps = shape.steps
     stream = torch.cuda.Stream(dev)
-
     J0 = torch.zeros_like(J[0])
 
     def chain():
-        cur = h0
+        cur = [h0] * chains
         for i in range(steps):
-            nxt = bufs[i % 2]
-            if args.verify:
-                # fused recompute + verify + cache: the cache is the state before
-                # the previous drafts, of which J[i-1] were accepted
-                p = i - 1 if i > 0 else 0
-                S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X[i], DT[i], A,
-                             BB[i], CC[i], D, cur, Y[i], nxt, stream=stream)
-            else:
-                S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur, J[i], Y[i], nxt, hK,
-                                stream=stream, dims=dims)
-            cur = nxt
+            for c in range(chains):
+                nxt = st[c]["bufs"][i % 2]
+                if verify:
+                    # fused recompute + verify + cache: the cache is the state
+                    # before the previous drafts, of which J[i-1] were accepted
+                    p = i - 1 if i > 0 else 0
+                    S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X[i], DT[i], A,
+                                 BB[i], CC[i], D, cur[c], st[c]["Y"], nxt, stream=stream)
+                else:
+                    S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur[c], J[i], st[c]["Y"],
+                                    nxt, st[c]["hK"], stream=stream, dims=dims)
+                cur[c] = nxt
 
     with torch.cuda.stream(stream):
         chain()
@@ -685,110 +836,201 @@ def run_multistep(args, world, rank, local):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         chain()
-    reps = max(1, args.steps // steps) if args.steps >= steps else 1
-    with torch.cuda.stream(stream):  # replays run on the current stream
-        for _ in range(args.warmup):
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // 3)):
             g.replay()
-        torch.cuda.synchronize()
-        S.ssd_check_device_error(stream)
-        clocks = ClockSampler(gpu_id_for(dev))
-        time.sleep(0.3)
-        barrier(world)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    S.ssd_check_device_error(stream)
+    clocks = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ms_call, reps = timed_replays(g.replay, steps * chains, stream, min_s)
+    torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / (reps * steps), world, dev)
+    ms_call = max_over_ranks(ms_call, world, dev)
+    S.ssd_check_device_error(stream)
+    out = {"ms": ms_call, "repeats": reps, "clocks": clk, "work": work,
+           "launches": steps * chains * reps}
+    del g
+    if e2e:
+        out["e2e"] = e2e_multistep(S, inp, A, D, h0, dims, stream, world, dev, verify,
+                                   max(3, min(args.steps, 200)))
+    return out
 
-    # ---- end to end through the public API: each call's drafts (x, dt, B, C)
-    # and accepted count j copied in from pinned host memory, y read back; the
-    # recurrent state stays resident on the device, as a decoder's cache does
-    ke = max(3, min(args.steps, 200))
+
+def e2e_multistep(S, inp, A, D, h0, dims, stream, world, dev, verify, ke):
+    """End to end through the public API: each call's drafts (x, dt, B, C) and
+    accepted count j copied in from pinned host memory (one stream, a call
+    ahead), y read back (another stream); the recurrent state stays resident
+    on the device, as a decoder's cache does."""
+    import torch
+    bf = torch.bfloat16
     hx = {k: torch.from_numpy(inp[k][:ke]).pin_memory() for k in ("dt", "j")}
     for k in ("x", "B", "C"):
         hx[k] = torch.from_numpy(inp[k][:ke]).to(bf).pin_memory()
-    # two device slots: a verify call also reads the previous call's drafts
-    dxs = [{k: torch.zeros_like(v[0], device=dev) for k, v in hx.items()} for _ in range(2)]
-    hy = torch.empty(Y[0].shape, dtype=Y.dtype, pin_memory=True)
-    with torch.cuda.stream(stream):
-        def e2e_call(i, cur, nxt):
-            dx, dp = dxs[i % 2], dxs[(i + 1) % 2]
-            for k in ("x", "dt", "B", "C", "j"):
-                dx[k].copy_(hx[k][i], non_blocking=True)
-            if args.verify:
-                S.ssd_verify(dp["x"], dp["dt"], dp["B"], dp["j"] if i > 0 else J0, dx["x"],
-                             dx["dt"], A, dx["B"], dx["C"], D, cur, Y[0], nxt, stream=stream)
-            else:
-                S.ssd_multistep(dx["x"], dx["dt"], A, dx["B"], dx["C"], D, cur, dx["j"], Y[0],
-                                nxt, hK, stream=stream, dims=dims)
-            hy.copy_(Y[0], non_blocking=True)
+    # three device slots: a verify call also reads the previous call's drafts
+    ns = 3
+    dxs = [{k: torch.zeros_like(v[0], device=dev) for k, v in hx.items()} for _ in range(ns)]
+    ys = [torch.empty(hx["x"][0].shape, dtype=bf, device=dev) for _ in range(2)]
+    hys = [torch.empty(hx["x"][0].shape, dtype=bf, pin_memory=True) for _ in range(2)]
+    bufs = [torch.empty_like(h0), torch.empty_like(h0)]
+    hK = torch.empty_like(h0)
+    J0 = torch.zeros(h0.shape[0], dtype=torch.int32, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(ns)]
+    ev_used = [torch.cuda.Event() for _ in range(ns)]
+    ev_y = [torch.cuda.Event() for _ in range(2)]
+    ev_ydone = [torch.cuda.Event() for _ in range(2)]
 
-        for i in range(3):
-            e2e_call(i, h0, bufs[i % 2])
-        torch.cuda.synchronize()
-        barrier(world)
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        cur = h0
-        for i in range(ke):
-            e2e_call(i, cur, bufs[i % 2])
-            cur = bufs[i % 2]
-        f1.record(stream)
-        torch.cuda.synchronize()
+    def call(i, cur, nxt):
+        k, kp = i % ns, (i - 1) % ns
+        dx, dp = dxs[k], dxs[kp]
+        s_in.wait_event(ev_used[k])  # calls i - 3 and i - 2 are done with this slot
+        with torch.cuda.stream(s_in):
+            for name in ("x", "dt", "B", "C", "j"):
+                dx[name].copy_(hx[name][i], non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        stream.wait_event(ev_ydone[i % 2])
+        yy = ys[i % 2]
+        if verify:
+            S.ssd_verify(dp["x"], dp["dt"], dp["B"], dp["j"] if i > 0 else J0, dx["x"],
+                         dx["dt"], A, dx["B"], dx["C"], D, cur, yy, nxt, stream=stream)
+        else:
+            S.ssd_multistep(dx["x"], dx["dt"], A, dx["B"], dx["C"], D, cur, dx["j"], yy,
+                            nxt, hK, stream=stream, dims=dims)
+        ev_used[k].record(stream)
+        ev_used[kp].record(stream)  # a verify call read the previous call's slot too
+        ev_y[i % 2].record(stream)
+        s_out.wait_event(ev_y[i % 2])
+        with torch.cuda.stream(s_out):
+            hys[i % 2].copy_(yy, non_blocking=True)
+            ev_ydone[i % 2].record(s_out)
+
+    for i in range(3):
+        call(i, h0, bufs[i % 2])
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    s_in.wait_event(f0)
+    cur = h0
+    for i in range(ke):
+        call(i, cur, bufs[i % 2])
+        cur = bufs[i % 2]
+    for k in range(2):
+        stream.wait_event(ev_ydone[k])
+    f1.record(stream)
+    torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / ke, world, dev)
     h2d = sum(v[0].numel() * v[0].element_size() for v in hx.values())
-    d2h = hy.numel() * hy.element_size()
+    d2h = hys[0].numel() * hys[0].element_size()
+    return {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def multistep_fields(m, world, pk, traffic):
+    work = m["work"]
+    gbs = work["bytes"] / (m["ms"] * 1e-3) / 1e9
+    f = {"value": round(world * work["tok_heads"] / (m["ms"] * 1e-3) / 1e6, 2),
+         "ms_per_step": round(m["ms"], 6), "repeats": m["repeats"],
+         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                      "frac": round(gbs / pk["hbm"], 4),
+                      "frac_vs_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                      "traffic": traffic, "kernel": "multistep_kernel",
+                      "algorithmic_bytes": work["bytes"],
+                      "peak_source": pk["source"] + " (burst)"},
+         "clocks": m["clocks"]}
+    if traffic:
+        f["roofline"]["dram_frac"] = round(traffic / (m["ms"] * 1e-3) / 1e9 / pk["hbm"], 4)
+    if "e2e" in m:
+        e = m["e2e"]
+        f["e2e"] = {"value": round(world * work["tok_heads"] / (e["ms_per_step"] * 1e-3) / 1e6, 2),
+                    "unit": UNIT, "h2d_bytes_per_step": e["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": e["d2h_bytes_per_step"],
+                    "ms_per_step": round(e["ms_per_step"], 4)}
+    return f
+
+
+def multistep_summary(args, world, rank, local):
+    """multistep_k8 inside the prefill line: the chain (states L2-warm), the
+    same chain with cold states (four interleaved chains), and the fused
+    verify chain, each with its own clocks; the oracle chain as CPU baseline."""
+    import torch
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    shape = synth.WORKLOADS["multistep_k8"]
+    m = measure_multistep(args, world, rank, dev, min_s=args.min_seconds)
+    out = dict(config_of("multistep_k8", shape, world),
+               **multistep_fields(m, world, pk, measured_traffic("multistep_kernel", "multistep_k8")))
+    out["timing"] = ("CUDA graph of the 1000-call chain, replayed until >= 1 s; each call reads "
+                     "the h_j the previous call wrote (L2-warm: states 3 x 42 MB per call)")
+    torch.cuda.empty_cache()
+    mc = measure_multistep(args, world, rank, dev, chains=4, min_s=args.min_seconds, e2e=False)
+    out["cold_states"] = dict(multistep_fields(mc, world, pk, None),
+                              timing="four independent chains interleaved: each call's cached "
+                                     "state was written three calls (~385 MB) earlier")
+    torch.cuda.empty_cache()
+    mv = measure_multistep(args, world, rank, dev, verify=True, min_s=args.min_seconds, e2e=False)
+    out["verify"] = dict(multistep_fields(mv, world, pk, None), call="ssd_verify")
+    out["verify"]["roofline"]["kernel"] = "multistep_kernel (verify mode)"
+    if not args.no_cpu_baseline:
+        value, _, cores, sample = oracle_multistep_chain(12, 6.0)
+        out["cpu_baseline"] = {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                               "kind": "oracle", "sample": sample}
+    return out
+
+
+def run_multistep(args, world, rank, local):
+    """--workload multistep_k8: one step = one call of the speculative chain."""
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = synth.WORKLOADS["multistep_k8"]
+    m = measure_multistep(args, world, rank, dev, verify=args.verify, chains=args.chains,
+                          min_s=args.min_seconds)
     if rank != 0:
         return
     pk = peaks()
-    gbs = work["bytes"] / (ms_step * 1e-3) / 1e9
-    line = {
-        "metric": ("SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
-                   "1000-step speculative chain)" if args.verify else
-                   "SSD multistep decode Mtok·heads/s (K=8 verify, 1000-step speculative chain)"),
-        "value": round(world * work["tok_heads"] / (ms_step * 1e-3) / 1e6, 2), "unit": UNIT,
-        "n_gpus": world, "steps": reps * steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64)",
-        "config": {"workload": "multistep_k8", "batch": shape.batch, "K": shape.K,
-                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                   "chain": steps, "graph": True, "call": "ssd_verify" if args.verify else "ssd_multistep",
-                   "l2": ("states 2 x 42 MB per step (cache, next cache); no flush" if args.verify else
-                          "states 3 x 42 MB per step (h_cache, h_j, h_K) ~ L2 size; no flush")},
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm"], 4),
-                     "traffic": None if args.verify else measured_traffic("multistep_kernel", "multistep_k8"),
-                     "kernel": "multistep_kernel",
-                     "algorithmic_bytes": work["bytes"], "peak_source": pk["source"] + " (burst)"},
-        "gpu_launches": reps * steps,
-        "e2e": {"value": round(world * work["tok_heads"] / (e2e_ms * 1e-3) / 1e6, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
-        "clocks": clk,
-    }
+    f = multistep_fields(m, world, pk, None if (args.verify or args.chains > 1)
+                         else measured_traffic("multistep_kernel", "multistep_k8"))
+    metric = ("SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
+              "1000-step speculative chain)" if args.verify else MULTISTEP_METRIC)
+    line = {"metric": metric, "value": f.pop("value"), "unit": UNIT, "n_gpus": world,
+            "steps": shape.steps * args.chains, "warmup": args.warmup,
+            "ms_per_step": f.pop("ms_per_step"), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64)",
+            "config": config_of("multistep_k8", shape, world),
+            "timing": "CUDA graph of the chain (%d interleaved), replayed until >= 1 s; %s"
+                      % (args.chains, "ssd_verify" if args.verify else "ssd_multistep"),
+            "gpu_launches": m["launches"]}
+    line.update(f)
     if world == 1 and not args.no_cpu_baseline:
         value, _, cores, sample = oracle_multistep_chain(40, 20.0)
         line["cpu_baseline"] = {"value": round(value, 4), "unit": UNIT, "cores": cores,
                                 "kind": "oracle", "sample": sample}
-    print(json.dumps(line, ensure_ascii=False))
+    print(json.dumps(line, ensure_ascii=False), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mamba2_2p7b", choices=list(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="the default workload's line without the other workloads")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="replay the timed block until this much device time is measured")
     ap.add_argument("--verify", action="store_true",
                     help="multistep_k8: time the chain of fused recompute + verify calls")
+    ap.add_argument("--chains", type=int, default=1,
+                    help="multistep_k8: independent chains interleaved (3+ keeps states cold)")
     ap.add_argument("--window", type=int, default=0,
                     help="prefill through ssd_fwd_sequential with windows of this many tokens")
     args = ap.parse_args()
@@ -814,7 +1056,7 @@ def main():
     if args.window > 0:
         run_sequential(args, shape, world, rank, local)
         return
-    run_ours(args, shape, work, world, rank, local)
+    run_ours(args, shape, world, rank, local)
 
 
 if __name__ == "__main__":

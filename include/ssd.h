@@ -235,6 +235,17 @@ ssd_status ssd_fwd_noalloc(const ssd_dims *dims, const void *x, const float *dt,
  * entry point that synchronises. */
 ssd_status ssd_check_device_error(void *stream);
 
+/* Diagnostic of the bounded-wait path.  Every wait inside the library's
+ * kernels gives up after a time limit, records SSD_ERR_TIMEOUT in the device
+ * error word and lets the kernel finish (freeing its tensor memory) instead of
+ * hanging or trapping.  This call launches one small kernel whose only work is
+ * such a wait, on a barrier nothing completes, with the limit limit_ns
+ * (1000 .. 1e9 ns, else SSD_ERR_INVALID_ARG) instead of the kernels' 2 s; the
+ * next ssd_check_device_error(stream) then reports SSD_ERR_TIMEOUT and clears
+ * it.  The context stays usable.  Not part of the layer (the pages have no
+ * counterpart): it lets a caller check the failure path without a GPU fault. */
+ssd_status ssd_selftest_timeout(int64_t limit_ns, void *stream);
+
 /* Static, never-NULL description of a status code. */
 const char *ssd_status_string(ssd_status status);
 

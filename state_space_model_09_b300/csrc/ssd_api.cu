@@ -35,6 +35,7 @@ namespace {
 using ssd::kTcN;
 
 constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;  // device ordinals with per-device set-up state
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -221,10 +222,23 @@ bool encode_btgw(CUtensorMap *m, const void *base, int64_t b, int64_t T, int64_t
   return encode_bf16(m, base, 4, dims, strides, box);
 }
 
-template <typename K>
-bool set_smem(K kernel, int bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
-         cudaSuccess;
+// Kernel attributes live in each device's context: the dynamic shared-memory
+// limit of a kernel is raised once per (kernel, device), with that device
+// current, before its first launch there.
+template <auto Kernel>
+bool ensure_smem(int bytes) {
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
 }
 
 ssd_status launch_status() {
@@ -308,10 +322,7 @@ ssd_status launch_scan_simt(const Plan &pl, const void *x, const void *B, const 
                             cudaStream_t s) {
   const int smem = ssd::scan_simt_smem_floats(pl.Q, static_cast<int>(pl.N)) * 4;
   auto k = ssd::chunk_scan_simt<IO, HT>;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, ssd::scan_simt_smem_floats(256, 256) * 4); });
-  if (!ok) return SSD_ERR_CUDA;
+  if (!ensure_smem<ssd::chunk_scan_simt<IO, HT>>(ssd::scan_simt_smem_floats(256, 256) * 4)) return SSD_ERR_CUDA;
   const int64_t blocks = ((pl.Q + 31) / 32) * ((pl.P + 63) / 64) * pl.nc;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.H), static_cast<unsigned>(pl.b));
   k<<<grid, 256, smem, s>>>(static_cast<const IO *>(x), static_cast<const IO *>(B),
@@ -323,15 +334,16 @@ ssd_status launch_scan_simt(const Plan &pl, const void *x, const void *B, const 
 }
 
 int num_sms() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-  });
-  return n;
+  static std::mutex mu;
+  static int n[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (n[dev] <= 0 &&
+      (cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+       n[dev] <= 0))
+    n[dev] = 148;
+  return n[dev];
 }
 
 template <int Q>
@@ -343,10 +355,7 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   if (pl.state_hb) {
     // two heads per MMA; mB / mX are the 128-row tile maps here
     auto k = ssd::chunk_state_hb;
-    static std::once_flag once;
-    static bool ok = false;
-    std::call_once(once, [&] { ok = set_smem(k, ssd::StateHB::kBytes); });
-    if (!ok) return SSD_ERR_CUDA;
+    if (!ensure_smem<ssd::chunk_state_hb>(ssd::StateHB::kBytes)) return SSD_ERR_CUDA;
     const int64_t items = pl.b * ((pl.H + 1) / 2);
     const int64_t ctas = pl.whole + (items - pl.whole) * (pl.nseg > 1 ? pl.nseg : 1);
     const ssd_status st = launch_dependent(
@@ -357,10 +366,7 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
   } else {
     using L = ssd::StatePass<Q>;
     auto k = ssd::chunk_state_pass_tc<Q>;
-    static std::once_flag once;
-    static bool ok = false;
-    std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
-    if (!ok) return SSD_ERR_CUDA;
+    if (!ensure_smem<ssd::chunk_state_pass_tc<Q>>(L::kBytes)) return SSD_ERR_CUDA;
     dim3 grid(static_cast<unsigned>(pl.P / L::PS), static_cast<unsigned>(pl.H),
               static_cast<unsigned>(pl.b * pl.nseg));
     k<<<grid, L::kThreads, L::kBytes, s>>>(mB, mX, dt, A, h0, Hin, h_final, pl.T,
@@ -383,10 +389,7 @@ ssd_status launch_multistep(dim3 grid, int64_t smem, const ssd_dims *d, const vo
                             const float *D, const float *h_cache, const int32_t *j, void *y,
                             float *h_j, float *h_K, int PS, cudaStream_t s) {
   auto k = ssd::multistep_kernel<IO, KT, NC, PSC>;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, 227 * 1024); });
-  if (!ok) return SSD_ERR_CUDA;
+  if (!ensure_smem<ssd::multistep_kernel<IO, KT, NC, PSC>>(227 * 1024)) return SSD_ERR_CUDA;
   k<<<grid, ssd::kMsThreads, static_cast<size_t>(smem), s>>>(
       static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
@@ -403,10 +406,7 @@ ssd_status launch_verify(dim3 grid, int64_t smem, const ssd_dims *d, int KP, con
                          const float *D, const float *h_cache, void *y, float *h_next, int PS,
                          cudaStream_t s) {
   auto k = ssd::multistep_kernel<IO, KT, NC, PSC, true>;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, 227 * 1024); });
-  if (!ok) return SSD_ERR_CUDA;
+  if (!ensure_smem<ssd::multistep_kernel<IO, KT, NC, PSC, true>>(227 * 1024)) return SSD_ERR_CUDA;
   k<<<grid, ssd::kMsThreads, static_cast<size_t>(smem), s>>>(
       static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
       D, h_cache, jp, static_cast<IO *>(y), nullptr, nullptr, static_cast<int>(d->seqlen),
@@ -442,10 +442,7 @@ ssd_status launch_scan_hl(const Plan &pl, const CUtensorMap &mC32, const CUtenso
                           const float *dt, const float *A, const float *D, cudaStream_t s) {
   using L = ssd::ScanHL<Q, P>;
   auto k = ssd::chunk_scan_hl<Q, P>;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, L::kBytes); });
-  if (!ok) return SSD_ERR_CUDA;
+  if (!ensure_smem<ssd::chunk_scan_hl<Q, P>>(L::kBytes)) return SSD_ERR_CUDA;
   const int hpc = scan_heads_per_cta(pl, num_sms());
   dim3 grid(static_cast<unsigned>((pl.H + hpc - 1) / hpc), pl.nc, static_cast<unsigned>(pl.b));
   k<<<grid, L::kThreads, L::kBytes, s>>>(mC32, mB, mX, mH, mY, dt, A, D, pl.T,
@@ -483,10 +480,7 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
                           const float *dt, const float *A, const float *D, const float *u,
                           const uint8_t *flags, bool pdl, cudaStream_t s) {
   auto k = ssd::chunk_scan_hb;
-  static std::once_flag once;
-  static bool ok = false;
-  std::call_once(once, [&] { ok = set_smem(k, ssd::kHbLaunchBytes); });
-  if (!ok) return SSD_ERR_CUDA;
+  if (!ensure_smem<ssd::chunk_scan_hb>(ssd::kHbLaunchBytes)) return SSD_ERR_CUDA;
   const int pp = scan_pairs_per_cta(pl, num_sms());
   const int64_t pairs = (pl.H + 1) / 2;
   const int hb_ranges = static_cast<int>((pairs + pp - 1) / pp);
@@ -508,6 +502,38 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Null, alignment and aliasing checks of a prefill call's buffers, as whole
+// [b, T, ...] tensors of `d`; the workspace counts as an output of ws_used
+// bytes.  Returns SSD_OK or SSD_ERR_INVALID_ARG; launches nothing.
+ssd_status check_fwd_buffers(const ssd_dims *d, const void *x, const float *dt, const float *A,
+                             const void *B, const void *C, const float *D, const float *h0,
+                             const void *y, const float *h_final, const void *workspace,
+                             size_t ws_used) {
+  if (!x || !dt || !A || !B || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, dt, A, B, C, D, h0, y, h_final, workspace};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  const size_t io = d->io_dtype == SSD_BF16 ? 2 : 4;
+  const size_t bt = static_cast<size_t>(d->batch * d->seqlen);
+  const size_t nx = bt * d->nheads * d->headdim * io;
+  const size_t nB = bt * d->ngroups_b * d->dstate * io;
+  const size_t nC = bt * d->ngroups_c * d->dstate * io;
+  const size_t ndt = bt * d->nheads * 4;
+  const size_t nst = static_cast<size_t>(d->batch * d->nheads * d->headdim * d->dstate) * 4;
+  const size_t nh = static_cast<size_t>(d->nheads) * 4;
+  struct Buf { const void *p; size_t n; };
+  const Buf ins[] = {{x, nx}, {dt, ndt}, {A, nh}, {B, nB}, {C, nC}, {D, nh}, {h0, nst}};
+  const Buf outs[] = {{y, nx}, {h_final, nst}, {workspace, ws_used}};
+  for (const Buf &o : outs) {
+    for (const Buf &i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return SSD_ERR_INVALID_ARG;
+  }
+  if (overlaps(y, nx, h_final, nst) || overlaps(y, nx, workspace, ws_used) ||
+      overlaps(h_final, nst, workspace, ws_used))
+    return SSD_ERR_INVALID_ARG;
+  return SSD_OK;
+}
+
 ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                     const void *B, const void *C, const float *D, const float *h0, int32_t chunk,
                     void *y, float *h_final, void *workspace, size_t ws_bytes, void *const *events,
@@ -515,28 +541,10 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   Plan pl;
   ssd_status st = make_plan(dims, chunk, &pl);
   if (st != SSD_OK) return st;
-  if (!x || !dt || !A || !B || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
-  const void *ptrs[] = {x, dt, A, B, C, D, h0, y, h_final, workspace};
-  for (const void *p : ptrs)
-    if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if ((st = check_fwd_buffers(dims, x, dt, A, B, C, D, h0, y, h_final, workspace, pl.total)) !=
+      SSD_OK)
+    return st;
   if (ws_bytes < pl.total) return SSD_ERR_INVALID_ARG;
-  const size_t io = pl.bf16 ? 2 : 4;
-  const size_t nx = static_cast<size_t>(pl.b * pl.T * pl.H * pl.P) * io;
-  const size_t nB = static_cast<size_t>(pl.b * pl.T * pl.GB * pl.N) * io;
-  const size_t nC = static_cast<size_t>(pl.b * pl.T * pl.GC * pl.N) * io;
-  const size_t ndt = static_cast<size_t>(pl.b * pl.T * pl.H) * 4;
-  const size_t nst = static_cast<size_t>(pl.b * pl.H * pl.N * pl.P) * 4;
-  const size_t nh = static_cast<size_t>(pl.H) * 4;
-  struct Buf { const void *p; size_t n; };
-  const Buf ins[] = {{x, nx}, {dt, ndt}, {A, nh}, {B, nB}, {C, nC}, {D, nh}, {h0, nst}};
-  const Buf outs[] = {{y, nx}, {h_final, nst}, {workspace, pl.total}};
-  for (const Buf &o : outs) {
-    for (const Buf &i : ins)
-      if (overlaps(o.p, o.n, i.p, i.n)) return SSD_ERR_INVALID_ARG;
-  }
-  if (overlaps(y, nx, h_final, nst) || overlaps(y, nx, workspace, pl.total) ||
-      overlaps(h_final, nst, workspace, pl.total))
-    return SSD_ERR_INVALID_ARG;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -627,7 +635,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCR
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[kMaxDevices] = {};
 
@@ -714,6 +721,11 @@ struct SeqPlan {
   ssd_dims wd;  // dims of a full window
   size_t fwd_bytes, carry_off, carry_bytes, stage_off, total;
   size_t row_x, row_dt, row_b, row_c;  // bytes of one token of each tensor
+  // windows are staged (copied) in the workspace: all tensors for batch > 1;
+  // for batch 1 only dt, and only when a window's offset t0 H 4 bytes would
+  // leave it off the 16-byte boundary the kernels need (H not a multiple of 4
+  // and a window length that does not restore it)
+  bool stage_all, stage_dt;
 };
 
 ssd_status make_seq_plan(const ssd_dims *dims, int32_t chunk, int64_t window, SeqPlan *sp) {
@@ -735,10 +747,15 @@ ssd_status make_seq_plan(const ssd_dims *dims, int32_t chunk, int64_t window, Se
                                                  dims->headdim) * 4);
   sp->stage_off = sp->carry_off + 2 * sp->carry_bytes;
   sp->total = sp->stage_off;
-  if (dims->batch > 1) {
-    const size_t rows = static_cast<size_t>(dims->batch * sp->wd.seqlen);
+  sp->stage_all = dims->batch > 1;
+  sp->stage_dt = !sp->stage_all && sp->wd.seqlen < dims->seqlen &&
+                 (static_cast<size_t>(sp->wd.seqlen) * sp->row_dt) % 16 != 0;
+  const size_t rows = static_cast<size_t>(dims->batch * sp->wd.seqlen);
+  if (sp->stage_all) {
     sp->total += align_up(rows * sp->row_x) * 2 + align_up(rows * sp->row_dt) +
                  align_up(rows * sp->row_b) + align_up(rows * sp->row_c);
+  } else if (sp->stage_dt) {
+    sp->total += align_up(rows * sp->row_dt);
   }
   return SSD_OK;
 }
@@ -766,8 +783,13 @@ ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *
   SeqPlan sp;
   ssd_status st = make_seq_plan(dims, chunk, window, &sp);
   if (st != SSD_OK) return st;
-  if (!x || !dt || !A || !B || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
-  if (workspace_bytes < sp.total || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
+  // every argument check before the first window is enqueued: the whole
+  // tensors' pointers, alignment and aliasing, and the workspace size (each
+  // window's own ssd_fwd checks then see only aligned, disjoint windows)
+  if ((st = check_fwd_buffers(dims, x, dt, A, B, C, D, h0, y, h_final, workspace, sp.total)) !=
+      SSD_OK)
+    return st;
+  if (workspace_bytes < sp.total) return SSD_ERR_INVALID_ARG;
   const int64_t b = dims->batch, T = dims->seqlen, W = sp.wd.seqlen;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -776,7 +798,8 @@ ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *
   uint8_t *stage = ws + sp.stage_off;
   const size_t rows = static_cast<size_t>(b * W);
   uint8_t *sx = stage, *sy = sx + align_up(rows * sp.row_x);
-  uint8_t *sdt = sy + align_up(rows * sp.row_x), *sB = sdt + align_up(rows * sp.row_dt);
+  uint8_t *sdt = sp.stage_all ? sy + align_up(rows * sp.row_x) : stage;
+  uint8_t *sB = sdt + align_up(rows * sp.row_dt);
   uint8_t *sC = sB + align_up(rows * sp.row_b);
   const uint8_t *px = static_cast<const uint8_t *>(x), *pdt = reinterpret_cast<const uint8_t *>(dt),
                 *pB = static_cast<const uint8_t *>(B), *pC = static_cast<const uint8_t *>(C);
@@ -790,12 +813,18 @@ ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *
     float *hout = t0 + len >= T ? h_final : carry[w & 1];
     const void *wx, *wdt, *wB, *wC;
     void *wy;
-    if (b == 1) {  // a window of a single sequence is contiguous
+    if (!sp.stage_all) {  // a window of a single sequence is contiguous
       wx = px + t0 * sp.row_x;
       wdt = pdt + t0 * sp.row_dt;
       wB = pB + t0 * sp.row_b;
       wC = pC + t0 * sp.row_c;
       wy = py + t0 * sp.row_x;
+      if (sp.stage_dt && !aligned16(wdt)) {
+        if (cudaMemcpyAsync(sdt, wdt, static_cast<size_t>(len) * sp.row_dt,
+                            cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+          return SSD_ERR_CUDA;
+        wdt = sdt;
+      }
     } else {
       if (!copy_window(sx, len, px + t0 * sp.row_x, T, sp.row_x, b, len, s) ||
           !copy_window(sdt, len, pdt + t0 * sp.row_dt, T, sp.row_dt, b, len, s) ||
@@ -807,7 +836,7 @@ ssd_status ssd_fwd_sequential(const ssd_dims *dims, const void *x, const float *
     st = fwd_impl(&d, wx, static_cast<const float *>(wdt), A, wB, wC, D, hin, chunk, wy, hout, ws,
                   sp.fwd_bytes, nullptr, stream);
     if (st != SSD_OK) return st;
-    if (b > 1 && !copy_window(py + t0 * sp.row_x, T, sy, len, sp.row_x, b, len, s))
+    if (sp.stage_all && !copy_window(py + t0 * sp.row_x, T, sy, len, sp.row_x, b, len, s))
       return SSD_ERR_CUDA;
   }
   return SSD_OK;
@@ -931,6 +960,13 @@ ssd_status ssd_check_device_error(void *stream) {
   if (code == ssd::kDevTimeout) return SSD_ERR_TIMEOUT;
   if (code == ssd::kDevBadJ) return SSD_ERR_INVALID_ARG;
   return SSD_OK;
+}
+
+ssd_status ssd_selftest_timeout(int64_t limit_ns, void *stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000) return SSD_ERR_INVALID_ARG;
+  ssd::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint64_t>(limit_ns));
+  return launch_status();
 }
 
 const char *ssd_status_string(ssd_status status) {

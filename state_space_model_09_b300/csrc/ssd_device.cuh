@@ -120,24 +120,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Waits for phase `parity` of `bar`.  Returns false, after recording
-// kDevTimeout, if the phase has not completed within kWaitLimitNs, or at once
+// kDevTimeout, if the phase has not completed within limit_ns, or at once
 // if `abort_flag` (shared memory, may be null) is already set by another
 // thread's timeout.  Callers then skip the work that depended on the wait.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort_flag, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         report_error(kDevTimeout);
         if (abort_flag) *abort_flag = 1;
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+  return mbar_wait_limit(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------------------------

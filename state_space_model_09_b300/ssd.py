@@ -67,6 +67,8 @@ _lib.ssd_multistep.argtypes = [_P] + [_vp] * 11 + [_vp]
 _lib.ssd_multistep.restype = ctypes.c_int
 _lib.ssd_check_device_error.argtypes = [_vp]
 _lib.ssd_check_device_error.restype = ctypes.c_int
+_lib.ssd_selftest_timeout.argtypes = [ctypes.c_int64, _vp]
+_lib.ssd_selftest_timeout.restype = ctypes.c_int
 _lib.ssd_status_string.argtypes = [ctypes.c_int]
 _lib.ssd_status_string.restype = ctypes.c_char_p
 _lib.ssd_version.argtypes = []
@@ -204,6 +206,11 @@ def ssd_multistep(x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, dt_softplus: bool 
                                                                       y, h_j, h_K)],
                             _stream(stream))
     _check(st, "ssd_multistep")
+
+
+def ssd_selftest_timeout(limit_ns: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test kernel (see ssd.h)."""
+    _check(_lib.ssd_selftest_timeout(int(limit_ns), _stream(stream)), "ssd_selftest_timeout")
 
 
 def ssd_check_device_error(stream=None) -> None:

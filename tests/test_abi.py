@@ -174,6 +174,48 @@ def test_sequential_rejects_bad_arguments_on_host():
     assert lib.ssd_fwd_sequential(*a3, n, None) == S.SSD_ERR_INVALID_ARG
 
 
+def test_sequential_checks_every_buffer_before_the_first_window():
+    """Aliasing and misalignment anywhere in the whole tensors are reported
+    before any window is enqueued (fake, never dereferenced pointers)."""
+    d = _dims(batch=1, seqlen=1000)
+    n = S.ssd_fwd_sequential_workspace_size(d, 256, 256)
+    lib = S.library_handle()
+    # x dt A B C D h0 | y h_final workspace: distinct, far apart, 16-byte aligned
+    ptr = [ctypes.c_void_p((i + 1) << 34) for i in range(10)]
+
+    def call(p):
+        return lib.ssd_fwd_sequential(ctypes.byref(d), *p[:7], 256, 256, *p[7:], n, None)
+
+    alias = list(ptr)
+    alias[7] = alias[0]                      # y aliases x
+    assert call(alias) == S.SSD_ERR_INVALID_ARG
+    tail = list(ptr)
+    tail[8] = ctypes.c_void_p(ptr[0].value + 64)  # h_final inside x
+    assert call(tail) == S.SSD_ERR_INVALID_ARG
+    odd = list(ptr)
+    odd[1] = ctypes.c_void_p(ptr[1].value + 8)    # dt off the 16-byte boundary
+    assert call(odd) == S.SSD_ERR_INVALID_ARG
+    ws_in = list(ptr)
+    ws_in[9] = ctypes.c_void_p(ptr[3].value + 16)  # workspace overlapping B
+    assert call(ws_in) == S.SSD_ERR_INVALID_ARG
+
+
+def test_sequential_stages_dt_windows_that_would_break_alignment():
+    """Batch 1 with H = 3: a 250-token window starts 3000 bytes into dt, off
+    the 16-byte boundary, so dt windows are staged (more workspace); with a
+    window that keeps the boundary (256 x 3 x 4 bytes) nothing is staged."""
+    w = S.ssd_fwd_sequential_workspace_size
+    d = _dims(batch=1, seqlen=1000, nheads=3, ngroups_b=1, ngroups_c=1)
+    d256 = w(d, 256, 256)
+    d250 = w(d, 256, 250)
+    assert d250 > 0 and d256 > 0
+    fwd250 = S.ssd_fwd_workspace_size(_dims(batch=1, seqlen=250, nheads=3, ngroups_b=1,
+                                            ngroups_c=1), 256)
+    fwd256 = S.ssd_fwd_workspace_size(_dims(batch=1, seqlen=256, nheads=3, ngroups_b=1,
+                                            ngroups_c=1), 256)
+    assert d250 - fwd250 > d256 - fwd256
+
+
 def test_verify_rejects_bad_arguments_on_host():
     """Host-side checks only: every case returns before anything touches the
     (fake, never dereferenced) device pointers."""

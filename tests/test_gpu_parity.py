@@ -201,6 +201,17 @@ def test_fwd_tc_without_softplus_and_D():
               D_none=True)
 
 
+def test_fwd_pair_form_without_softplus_and_D(monkeypatch):
+    """The head-pair chunk scan (forced) with dt used as given and no D."""
+    monkeypatch.setenv("SSD_CHUNK_SCAN", "pair")
+    shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = S.make_dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                    dt_softplus=False)
+    assert "chunk_scan_hb" in [S.ssd_fwd_stage_name(d, 256, i)
+                               for i in range(S.ssd_fwd_num_stages(d, 256))]
+    check_fwd(shape, 43, dt_softplus=False, D_none=True)
+
+
 def test_fwd_f32_without_softplus_and_D():
     check_fwd(F(1, 130, 2, 32, 32, 1, 1, 64, synth.F32, "all"), 42, dt_softplus=False,
               D_none=True)
@@ -396,8 +407,11 @@ def test_multistep_bad_j_reported():
     S.ssd_check_device_error()  # the word was cleared
 
 
-def _chain(shape, inp, steps, graph: bool):
-    """Speculative chain: each step continues from h_j (ping-pong buffers)."""
+def _chain(shape, inp, steps, graph: bool, hk_rows=None):
+    """Speculative chain: each step continues from h_j (ping-pong buffers).
+    With hk_rows (flat b * H + h indices), every step's h_K of those (b, h)
+    pairs is also copied out, inside the graph, to a [steps, rows, N, P]
+    buffer returned third."""
     dt_io = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
     X = torch.from_numpy(inp["x"][:steps]).to(dt_io).cuda()
     DT = torch.from_numpy(inp["dt"][:steps]).cuda()
@@ -410,19 +424,25 @@ def _chain(shape, inp, steps, graph: bool):
     hK = torch.empty_like(h0)
     Y = torch.empty_like(X)
     dims = S.dims_of(X[0], BB[0], CC[0])
+    b, _, H, P = X[0].shape
+    N = BB.shape[-1]
+    rows = None if hk_rows is None else torch.tensor(hk_rows, dtype=torch.long, device="cuda")
+    HK = None if rows is None else torch.empty((steps, len(hk_rows), N, P), device="cuda")
 
     def run():
         cur = h0
         for s in range(steps):
             nxt = bufs[s % 2]
             S.ssd_multistep(X[s], DT[s], A, BB[s], CC[s], D, cur, J[s], Y[s], nxt, hK, dims=dims)
+            if rows is not None:
+                torch.index_select(hK.view(b * H, N, P), 0, rows, out=HK[s])
             cur = nxt
         return cur
 
     out = run()
     torch.cuda.synchronize()
     if not graph:
-        return Y, out
+        return (Y, out) if rows is None else (Y, out, HK)
     Y.fill_(float("nan"))
     stream = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
@@ -430,31 +450,38 @@ def _chain(shape, inp, steps, graph: bool):
         out = run()
     g.replay()
     torch.cuda.synchronize()
-    return Y, out
+    return (Y, out) if rows is None else (Y, out, HK)
 
 
 def test_multistep_chain_full_size_sampled():
-    """The 1000-step speculative chain at the full decode shape; sampled
-    (b, h) pairs follow the oracle's chain step by step."""
+    """The 1000-step speculative chain at the full decode shape, in the graph
+    the benchmark replays; sampled (b, h) pairs (every 20th) follow the
+    oracle's chain on every step: y of every step and h_K of every step (the
+    state after all K drafts, which the next step does not read), and the
+    state the chain ends in (h_j of the last step)."""
     shape = synth.WORKLOADS["multistep_k8"]
     steps = shape.steps
     inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"])
-    Y, h_last = _chain(shape, inp, steps, graph=True)
-    S.ssd_check_device_error()
     b, K, H, P = inp["x"][0].shape
-    N = inp["B"].shape[-1]
     pairs = list(range(0, b * H, 20))
+    Y, h_last, HK = _chain(shape, inp, steps, graph=True, hk_rows=pairs)
+    S.ssd_check_device_error()
+    Yh = Y.float().cpu().numpy()
+    HKh = HK.cpu().numpy()
     cache = inp["h_cache"].copy()
-    worst = 0.0
+    worst_y = worst_k = 0.0
     for s in range(steps):
-        yr, hjr, _ = oracle.ssd_multistep(inp["x"][s], inp["dt"][s], inp["A"], inp["B"][s],
-                                          inp["C"][s], inp["D"], cache, inp["j"][s], pairs=pairs)
+        yr, hjr, hkr = oracle.ssd_multistep(inp["x"][s], inp["dt"][s], inp["A"], inp["B"][s],
+                                            inp["C"][s], inp["D"], cache, inp["j"][s],
+                                            pairs=pairs)
         # the oracle continues from its own states (float32-rounded like the GPU's)
         for q, p in enumerate(pairs):
             cache[p // H, p % H] = hjr[q].astype(np.float32)
-        if s % 100 == 0 or s == steps - 1:
-            worst = max(worst, rel_err(y_pairs(Y[s], pairs, H), yr))
-    assert worst <= 1e-2
+        ys = np.stack([Yh[s, p // H, :, p % H, :] for p in pairs]).astype(np.float64)
+        worst_y = max(worst_y, rel_err(ys, yr))
+        worst_k = max(worst_k, rel_err(HKh[s].astype(np.float64), hkr))
+    assert worst_y <= 1e-2, worst_y
+    assert worst_k <= 1e-2, worst_k
     assert rel_err(h_pairs(h_last, pairs, H), np.stack([cache[p // H, p % H] for p in pairs])) <= 1e-2
 
 

@@ -35,6 +35,7 @@ def _rel(a, b):
     (F(2, 900, 4, 64, 128, 1, 2, 128, synth.BF16, "half"), 300, 82),   # staged, off the chunk grid
     (F(3, 700, 4, 32, 32, 1, 1, 64, synth.F32, "all"), 192, 83),       # float32 path, staged
     (F(1, 130, 2, 64, 64, 1, 1, 64, synth.F32, "zero"), 1000, 84),     # window longer than T
+    (F(1, 1000, 3, 64, 128, 1, 1, 256, synth.BF16, "all"), 250, 86),   # dt windows staged (H = 3)
 ])
 def test_sequential_equals_whole_and_oracle(shape, window, seed):
     inp = synth.make_fwd_inputs(shape, seed)
