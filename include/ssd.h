@@ -202,6 +202,46 @@ ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
                       const void *x, const float *dt, const float *A, const void *B, const void *C,
                       const float *D, const float *h_cache, void *y, float *h_next, void *stream);
 
+/* Context parallelism over the sequence (Mamba-2 page, section "序列并行的两种形式",
+ * context parallelism: each GPU computes the outputs and the final state of
+ * its own segment of the sequence, then the states are passed from GPU to
+ * GPU).  Rank r of nranks holds tokens [t_r, t_{r+1}) of every sequence:
+ *   1. ssd_fwd on the segment, with h0 on rank 0 and NULL (zero) elsewhere:
+ *      y (local) and F_r = the segment's final state (h_final);
+ *   2. ssd_cp_segment_decay: Lambda_r[b, h], the segment's total decay (the
+ *      product over its tokens of exp(dt_t A_h));
+ *   3. the caller gathers every rank's Lambda and F (e.g. an all-gather),
+ *      rank-ordered, into decays [nranks, b, H] and finals [nranks, b, H, N, P];
+ *   4. ssd_cp_correct: the true state entering segment r,
+ *         H_in(0) = 0,  H_in(r'+1) = Lambda_r' H_in(r') + F_r'
+ *      (the scan over ranks; F_0 already includes h0), then
+ *         y_t += exp(cs_t) C_t^T H_in(r)   for every token t of the segment,
+ *         h_final = Lambda_r H_in(r) + F_r,
+ *      with cs_t the running sum of dt A from the segment's start to t
+ *      (inclusive).  The concatenated y and the last rank's h_final then
+ *      equal one ssd_fwd over the whole sequence up to rounding.
+ * dims describe this rank's segment (seqlen = its length).  Workspace: at
+ * least ssd_cp_workspace_size(dims) bytes, no initialisation needed.  All
+ * work is enqueued on `stream`; nothing is allocated or synchronised. */
+size_t ssd_cp_workspace_size(const ssd_dims *dims);
+
+/* decay [b, H] float32 (output): the segment's total decay Lambda.  dt, A as
+ * in ssd_fwd (dims.dt_softplus applies). */
+ssd_status ssd_cp_segment_decay(const ssd_dims *dims, const float *dt, const float *A,
+                                float *decay, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* nranks >= 1, 0 <= rank < nranks.  decays [nranks, b, H] and finals
+ * [nranks, b, H, N, P] (float32, rank-ordered; entries of ranks after `rank`
+ * are not read).  dt, A, C: this segment's, as in ssd_fwd.  y: this segment's
+ * ssd_fwd output, updated in place (rank 0: unchanged).  h_final (output,
+ * [b, H, N, P], may be NULL): the segment's true final state.  y and h_final
+ * may not alias an input, the workspace or each other. */
+ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
+                          const float *decays, const float *finals, const float *dt,
+                          const float *A, const void *C, void *y, float *h_final,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /* Allocation-free variant of ssd_fwd.  The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc at the point
  * where they run the layer -- code working under a fixed device-memory plan

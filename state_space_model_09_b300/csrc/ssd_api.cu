@@ -23,9 +23,11 @@
 #include <utility>
 
 #include "../../include/ssd.h"
+#include "ssd_cp.cuh"
 #include "ssd_kernels.cuh"
 #include "ssd_scan.cuh"
 #include "ssd_scan_hb.cuh"
+#include "ssd_selftest.cuh"
 #include "ssd_state_hb.cuh"
 #include "ssd_state.cuh"
 #include "ssd_tc.cuh"
@@ -948,6 +950,170 @@ ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
                   : launch_verify<__nv_bfloat16, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
   return K <= 8 ? launch_verify<float, 8>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
                 : launch_verify<float, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
+}
+
+// ---------------------------------------------------------------------------
+// Context parallelism: per-segment decay, and the correction of a segment's
+// outputs and final state once the states of the segments before it are known.
+// Workspace: the running log2 decays a [b, H, T] and H_in [b, H, N, P], float32.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct CpPlan {
+  int64_t b, T, H, P, N, GC;
+  size_t a_bytes, hin_off, total;
+};
+
+ssd_status make_cp_plan(const ssd_dims *d, CpPlan *cp) {
+  ssd_status st = check_dims(d);
+  if (st != SSD_OK) return st;
+  cp->b = d->batch;
+  cp->T = d->seqlen;
+  cp->H = d->nheads;
+  cp->P = d->headdim;
+  cp->N = d->dstate;
+  cp->GC = d->ngroups_c;
+  if (cp->b * cp->H > (int64_t(1) << 31) - 1 || cp->b > 65535) return SSD_ERR_UNSUPPORTED;
+  cp->a_bytes = align_up(static_cast<size_t>(cp->b * cp->H * cp->T) * 4);
+  cp->hin_off = cp->a_bytes;
+  cp->total = cp->hin_off + align_up(static_cast<size_t>(cp->b * cp->H * cp->N * cp->P) * 4);
+  return SSD_OK;
+}
+
+// a[b, h, t] = running log2 decay from the segment's start (inclusive); the
+// segment's total decay 2^(a[b, h, T - 1]) into decay[b H] when given.
+ssd_status cp_running_decay(const CpPlan &cp, const float *dt, const float *A, int softplus,
+                            float *a, float *decay, cudaStream_t s) {
+  dim3 g((cp.T + 31) / 32, static_cast<unsigned>((cp.H + 31) / 32), static_cast<unsigned>(cp.b));
+  if (g.x > 2147483647ll) return SSD_ERR_UNSUPPORTED;
+  ssd::dt_decay_kernel<<<g, 256, 0, s>>>(dt, A, a, cp.T, static_cast<int>(cp.H), softplus);
+  ssd_status st = launch_status();
+  if (st != SSD_OK) return st;
+  ssd::row_cumsum_kernel<<<static_cast<unsigned>(cp.b * cp.H), 256, 0, s>>>(a, cp.T, decay);
+  return launch_status();
+}
+
+// Heads per CTA of cp_correct_tc: a divisor of the heads per C group, the
+// largest that still gives two CTAs per SM.
+int cp_heads_per_cta(const CpPlan &cp) {
+  const int64_t per_group = cp.H / cp.GC, tiles = (cp.T + 127) / 128;
+  for (int64_t hpc = per_group; hpc > 1; --hpc)
+    if (per_group % hpc == 0 && tiles * cp.b * (cp.H / hpc) >= 2 * num_sms())
+      return static_cast<int>(hpc);
+  return 1;
+}
+
+}  // namespace
+
+size_t ssd_cp_workspace_size(const ssd_dims *dims) {
+  CpPlan cp;
+  return make_cp_plan(dims, &cp) == SSD_OK ? cp.total : 0;
+}
+
+ssd_status ssd_cp_segment_decay(const ssd_dims *dims, const float *dt, const float *A,
+                                float *decay, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  CpPlan cp;
+  ssd_status st = make_cp_plan(dims, &cp);
+  if (st != SSD_OK) return st;
+  if (!dt || !A || !decay || !workspace) return SSD_ERR_INVALID_ARG;
+  const void *ptrs[] = {dt, A, decay, workspace};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if (workspace_bytes < cp.a_bytes) return SSD_ERR_INVALID_ARG;
+  const size_t ndt = static_cast<size_t>(cp.b * cp.T * cp.H) * 4, nh = cp.H * 4,
+               nd = static_cast<size_t>(cp.b * cp.H) * 4;
+  if (overlaps(decay, nd, dt, ndt) || overlaps(decay, nd, A, nh) ||
+      overlaps(decay, nd, workspace, cp.a_bytes) || overlaps(workspace, cp.a_bytes, dt, ndt) ||
+      overlaps(workspace, cp.a_bytes, A, nh))
+    return SSD_ERR_INVALID_ARG;
+  return cp_running_decay(cp, dt, A, dims->dt_softplus, static_cast<float *>(workspace), decay,
+                          static_cast<cudaStream_t>(stream));
+}
+
+ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
+                          const float *decays, const float *finals, const float *dt,
+                          const float *A, const void *C, void *y, float *h_final,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  CpPlan cp;
+  ssd_status st = make_cp_plan(dims, &cp);
+  if (st != SSD_OK) return st;
+  if (nranks < 1 || rank < 0 || rank >= nranks) return SSD_ERR_INVALID_ARG;
+  if (!decays || !finals || !dt || !A || !C || !y || !workspace) return SSD_ERR_INVALID_ARG;
+  const void *ptrs[] = {decays, finals, dt, A, C, y, h_final, workspace};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if (workspace_bytes < cp.total) return SSD_ERR_INVALID_ARG;
+  const size_t io = dims->io_dtype == SSD_BF16 ? 2 : 4;
+  const size_t BH = static_cast<size_t>(cp.b * cp.H), NP = static_cast<size_t>(cp.N * cp.P);
+  struct Buf { const void *p; size_t n; };
+  const Buf ins[] = {{decays, nranks * BH * 4}, {finals, nranks * BH * NP * 4},
+                     {dt, static_cast<size_t>(cp.b * cp.T * cp.H) * 4}, {A, cp.H * 4},
+                     {C, static_cast<size_t>(cp.b * cp.T * cp.GC * cp.N) * io}};
+  const Buf outs[] = {{y, static_cast<size_t>(cp.b * cp.T * cp.H * cp.P) * io},
+                      {h_final, BH * NP * 4}, {workspace, cp.total}};
+  for (const Buf &o : outs)
+    for (const Buf &i : ins)
+      if (overlaps(o.p, o.n, i.p, i.n)) return SSD_ERR_INVALID_ARG;
+  if (overlaps(outs[0].p, outs[0].n, h_final, outs[1].n) ||
+      overlaps(outs[0].p, outs[0].n, workspace, cp.total) ||
+      overlaps(h_final, outs[1].n, workspace, cp.total))
+    return SSD_ERR_INVALID_ARG;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *a = reinterpret_cast<float *>(ws);
+  float *hin = reinterpret_cast<float *>(ws + cp.hin_off);
+  const int64_t n4 = static_cast<int64_t>(BH * NP / 4);
+  const unsigned blocks = static_cast<unsigned>((n4 + 255) / 256);
+  // H_in of this rank and its true final state (rank 0: its own final state)
+  ssd::cp_combine_kernel<<<blocks, 256, 0, s>>>(decays, finals, rank,
+                                                static_cast<int64_t>(BH), static_cast<int>(NP),
+                                                rank > 0 ? hin : nullptr, h_final);
+  if ((st = launch_status()) != SSD_OK) return st;
+  if (rank == 0) return SSD_OK;  // the first segment started from the true h0
+  if ((st = cp_running_decay(cp, dt, A, dims->dt_softplus, a, nullptr, s)) != SSD_OK) return st;
+  const bool tc = dims->io_dtype == SSD_BF16 && cp.N == kTcN && (cp.P == 64 || cp.P == 128);
+  if (tc) {
+    CUtensorMap mC;
+    if (!encode_btgw(&mC, C, cp.b, cp.T, cp.GC, cp.N, 128)) return SSD_ERR_CUDA;
+    const int hpc = cp_heads_per_cta(cp);
+    dim3 grid(static_cast<unsigned>((cp.T + 127) / 128), static_cast<unsigned>((cp.H + hpc - 1) / hpc),
+              static_cast<unsigned>(cp.b));
+    if (cp.T > 2147483647ll - 128 || grid.y > 65535) return SSD_ERR_UNSUPPORTED;
+    if (cp.P == 64) {
+      if (!ensure_smem<ssd::cp_correct_tc<64>>(ssd::CpTc<64>::kBytes)) return SSD_ERR_CUDA;
+      ssd::cp_correct_tc<64><<<grid, 128, ssd::CpTc<64>::kBytes, s>>>(
+          mC, hin, a, static_cast<__nv_bfloat16 *>(y), cp.T, static_cast<int>(cp.H),
+          static_cast<int>(cp.GC), hpc);
+    } else {
+      if (!ensure_smem<ssd::cp_correct_tc<128>>(ssd::CpTc<128>::kBytes)) return SSD_ERR_CUDA;
+      ssd::cp_correct_tc<128><<<grid, 128, ssd::CpTc<128>::kBytes, s>>>(
+          mC, hin, a, static_cast<__nv_bfloat16 *>(y), cp.T, static_cast<int>(cp.H),
+          static_cast<int>(cp.GC), hpc);
+    }
+    return launch_status();
+  }
+  const int PS = cp.P % 64 == 0 ? 64 : cp.P % 32 == 0 ? 32 : 16;
+  const int smem = static_cast<int>((32 * cp.N + cp.N * PS) * 4);
+  dim3 grid(static_cast<unsigned>((cp.T + 31) / 32), static_cast<unsigned>(cp.P / PS),
+            static_cast<unsigned>(BH));
+  if (grid.y > 65535 || BH > 65535) return SSD_ERR_UNSUPPORTED;
+  if (dims->io_dtype == SSD_BF16) {
+    if (!ensure_smem<ssd::cp_correct_simt<__nv_bfloat16>>((32 * 256 + 256 * 64) * 4))
+      return SSD_ERR_CUDA;
+    ssd::cp_correct_simt<__nv_bfloat16><<<grid, 256, smem, s>>>(
+        static_cast<const __nv_bfloat16 *>(C), hin, a, static_cast<__nv_bfloat16 *>(y), cp.T,
+        static_cast<int>(cp.H), static_cast<int>(cp.GC), static_cast<int>(cp.N),
+        static_cast<int>(cp.P), PS);
+  } else {
+    if (!ensure_smem<ssd::cp_correct_simt<float>>((32 * 256 + 256 * 64) * 4)) return SSD_ERR_CUDA;
+    ssd::cp_correct_simt<float><<<grid, 256, smem, s>>>(
+        static_cast<const float *>(C), hin, a, static_cast<float *>(y), cp.T,
+        static_cast<int>(cp.H), static_cast<int>(cp.GC), static_cast<int>(cp.N),
+        static_cast<int>(cp.P), PS);
+  }
+  return launch_status();
 }
 
 ssd_status ssd_check_device_error(void *stream) {

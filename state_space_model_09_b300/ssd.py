@@ -67,6 +67,13 @@ _lib.ssd_multistep.argtypes = [_P] + [_vp] * 11 + [_vp]
 _lib.ssd_multistep.restype = ctypes.c_int
 _lib.ssd_check_device_error.argtypes = [_vp]
 _lib.ssd_check_device_error.restype = ctypes.c_int
+_lib.ssd_cp_workspace_size.argtypes = [_P]
+_lib.ssd_cp_workspace_size.restype = ctypes.c_size_t
+_lib.ssd_cp_segment_decay.argtypes = [_P, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.ssd_cp_segment_decay.restype = ctypes.c_int
+_lib.ssd_cp_correct.argtypes = [_P, ctypes.c_int32, ctypes.c_int32] + [_vp] * 8 + \
+    [ctypes.c_size_t, _vp]
+_lib.ssd_cp_correct.restype = ctypes.c_int
 _lib.ssd_selftest_timeout.argtypes = [ctypes.c_int64, _vp]
 _lib.ssd_selftest_timeout.restype = ctypes.c_int
 _lib.ssd_status_string.argtypes = [ctypes.c_int]
@@ -206,6 +213,28 @@ def ssd_multistep(x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, dt_softplus: bool 
                                                                       y, h_j, h_K)],
                             _stream(stream))
     _check(st, "ssd_multistep")
+
+
+def ssd_cp_workspace_size(dims: ssd_dims) -> int:
+    return int(_lib.ssd_cp_workspace_size(ctypes.byref(dims)))
+
+
+def ssd_cp_segment_decay(dt, A, decay, workspace, dims: ssd_dims, stream=None) -> None:
+    """Enqueue the segment-decay kernels (see ssd.h): decay [b, H] float32."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.ssd_cp_segment_decay(ctypes.byref(dims), _ptr(dt), _ptr(A), _ptr(decay),
+                                   _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ssd_cp_segment_decay")
+
+
+def ssd_cp_correct(nranks: int, rank: int, decays, finals, dt, A, C, y, h_final, workspace,
+                   dims: ssd_dims, stream=None) -> None:
+    """Enqueue the correction of this rank's segment (see ssd.h)."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = _lib.ssd_cp_correct(ctypes.byref(dims), int(nranks), int(rank), _ptr(decays),
+                             _ptr(finals), _ptr(dt), _ptr(A), _ptr(C), _ptr(y), _ptr(h_final),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "ssd_cp_correct")
 
 
 def ssd_selftest_timeout(limit_ns: int, stream=None) -> None:

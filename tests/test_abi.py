@@ -216,6 +216,41 @@ def test_sequential_stages_dt_windows_that_would_break_alignment():
     assert d250 - fwd250 > d256 - fwd256
 
 
+def test_cp_calls_reject_bad_arguments_on_host():
+    """Context-parallel calls: rank outside 0..nranks-1, NULL or misaligned
+    pointers and aliasing are reported before anything is launched (fake,
+    never dereferenced pointers)."""
+    lib = S.library_handle()
+    d = _dims(batch=2, seqlen=1000)
+    n = S.ssd_cp_workspace_size(d)
+    assert n >= 2 * 1000 * 80 * 4 + 2 * 80 * 128 * 64 * 4
+    assert S.ssd_cp_workspace_size(_dims(headdim=24)) == 0
+    # decays finals dt A C y h_final workspace
+    ptr = [ctypes.c_void_p((i + 1) << 36) for i in range(8)]
+
+    def correct(nranks, rank, p, ws=n):
+        return lib.ssd_cp_correct(ctypes.byref(d), nranks, rank, *p[:7], p[7], ws, None)
+
+    assert correct(2, 2, ptr) == S.SSD_ERR_INVALID_ARG      # rank >= nranks
+    assert correct(2, -1, ptr) == S.SSD_ERR_INVALID_ARG     # rank < 0
+    assert correct(0, 0, ptr) == S.SSD_ERR_INVALID_ARG      # no ranks
+    assert correct(2, 1, ptr, n - 1) == S.SSD_ERR_INVALID_ARG  # short workspace
+    alias = list(ptr); alias[5] = alias[4]                   # y aliases C
+    assert correct(2, 1, alias) == S.SSD_ERR_INVALID_ARG
+    alias = list(ptr); alias[6] = ctypes.c_void_p(ptr[1].value + 256)  # h_final inside finals
+    assert correct(2, 1, alias) == S.SSD_ERR_INVALID_ARG
+    odd = list(ptr); odd[2] = ctypes.c_void_p(ptr[2].value + 4)
+    assert correct(2, 1, odd) == S.SSD_ERR_INVALID_ARG      # dt misaligned
+    null = list(ptr); null[4] = None
+    assert correct(2, 1, null) == S.SSD_ERR_INVALID_ARG     # NULL C
+    # segment decay: dt A decay workspace
+    dec = [ctypes.c_void_p((i + 1) << 36) for i in range(4)]
+    seg = lambda p, ws=n: lib.ssd_cp_segment_decay(ctypes.byref(d), *p, ws, None)
+    assert seg(dec, 16) == S.SSD_ERR_INVALID_ARG            # short workspace
+    alias = list(dec); alias[2] = alias[0]                   # decay aliases dt
+    assert seg(alias) == S.SSD_ERR_INVALID_ARG
+
+
 def test_verify_rejects_bad_arguments_on_host():
     """Host-side checks only: every case returns before anything touches the
     (fake, never dereferenced) device pointers."""
