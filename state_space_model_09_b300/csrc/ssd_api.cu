@@ -24,6 +24,7 @@
 
 #include "../../include/ssd.h"
 #include "ssd_cp.cuh"
+#include "ssd_fused_hb.cuh"
 #include "ssd_kernels.cuh"
 #include "ssd_scan.cuh"
 #include "ssd_scan_hb.cuh"
@@ -64,6 +65,11 @@ struct Plan {
   // dt_decay_kernel has written the per-token log2 decays [b, H, T] (u_off)
   bool state_hb = false;
   size_t u_off = 0;
+  // the same shapes, by default: the one-pass kernel (chunk_fused_hb), with
+  // its prepass when items are split (nseg > 1; whole, cps, seg_bh0, seg_rows,
+  // Fseg_off, Lseg_off as above) and the flagged-head pass after it; Hin,
+  // flags and u then hold the flagged (chunk, head) units only
+  bool fused = false;
 };
 
 int num_sms();
@@ -103,6 +109,34 @@ void plan_segments(Plan *pl) {
   } else {
     pl->seg_bh0 = 0;
   }
+  pl->seg_rows = pl->b * pl->H - pl->seg_bh0;
+}
+
+// Segments of the one-pass kernel: one CTA per SM, one per (batch row, head
+// pair).  With more items than SMs the items of a last, partly filled wave
+// are split (the full waves' items run whole); with fewer, every item is; a
+// split item's nseg segments of cps chunks start from the states the prepass
+// computes.  E.g. 8 x 40 head pairs on 148 SMs: two full waves + 24 items in
+// four segments of two chunks; 1 x 40 pairs of 64 chunks: three segments.
+void plan_fused(Plan *pl) {
+  const int64_t npairs = (pl->H + 1) / 2, items = pl->b * npairs;
+  const int64_t slots = num_sms();
+  int64_t nseg = 1, whole = items;
+  if (items < slots) {
+    nseg = std::min<int64_t>(slots / items, pl->nc);
+    whole = 0;
+  } else if (items % slots) {
+    whole = items / slots * slots;
+    nseg = std::min<int64_t>(slots / (items - whole), pl->nc);
+  }
+  if (nseg <= 1) {
+    nseg = 1;
+    whole = items;
+  }
+  pl->cps = static_cast<int>((pl->nc + nseg - 1) / nseg);
+  pl->nseg = (pl->nc + pl->cps - 1) / pl->cps;
+  pl->whole = pl->nseg > 1 ? whole : items;
+  pl->seg_bh0 = pl->whole / npairs * pl->H + 2 * (pl->whole % npairs);
   pl->seg_rows = pl->b * pl->H - pl->seg_bh0;
 }
 
@@ -152,8 +186,15 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     pl->Hin_off = 0;
     pl->total = align_up(states * 2);
     const bool hb_shape = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
-    pl->state_hb = hb_shape;
-    plan_segments(pl);
+    // SSD_FUSED=0, or a forced chunk-scan form (SSD_CHUNK_SCAN), selects the
+    // two-pass head-pair kernels instead of the one-pass kernel (for tests
+    // and comparisons; the results agree within the tolerance)
+    const char *fz = std::getenv("SSD_FUSED");
+    const char *force = std::getenv("SSD_CHUNK_SCAN");
+    pl->fused = hb_shape && !(fz && std::strcmp(fz, "0") == 0) && !(force && *force);
+    pl->state_hb = hb_shape && !pl->fused;
+    if (pl->fused) plan_fused(pl);
+    else plan_segments(pl);
     if (pl->nseg > 1) {
       if (pl->b * pl->nseg > 65535 || pl->seg_rows > 65535) return SSD_ERR_UNSUPPORTED;
       const size_t bh = static_cast<size_t>(pl->seg_rows);
@@ -162,12 +203,16 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
       pl->Dc_off = pl->Lseg_off + align_up(bh * pl->nseg * sizeof(float));
       pl->total = pl->Dc_off + align_up(bh * pl->nc * sizeof(float));
     }
-    if (hb_shape) {  // the flags are reserved for every such shape
+    if (pl->fused) {
+      pl->flags_off = pl->total;
+      pl->total += align_up(static_cast<size_t>(pl->b) * pl->nc * pl->H);
+      pl->u_off = pl->total;
+      pl->total += align_up(static_cast<size_t>(pl->b) * pl->H * pl->T * sizeof(float));
+    } else if (hb_shape) {  // the flags are reserved for every such shape
       pl->flags_off = pl->total;
       pl->total += align_up(static_cast<size_t>(pl->b) * pl->nc * pl->H);
       // SSD_CHUNK_SCAN=pair / =head forces the choice (the same result either
       // way, within the tolerance; for tests and tuning)
-      const char *force = std::getenv("SSD_CHUNK_SCAN");
       if (force && std::strcmp(force, "pair") == 0) pl->hb = true;
       else if (force && std::strcmp(force, "head") == 0) pl->hb = false;
       else pl->hb = scan_pairs_per_cta(*pl, num_sms()) >= kHbMinPairs;
@@ -498,6 +543,77 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
                           flagged_sets, pl.softplus);
 }
 
+// The one-pass path: [prepass of split items] -> chunk_fused_hb -> the
+// flagged (chunk, head) units by the per-head body (chunk_scan_hb's flagged
+// items alone).  Each kernel after the first is a programmatic dependent of
+// the one before (pdl); the first waits for everything before it.
+ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D, const float *h0, void *y,
+                        float *h_final, uint8_t *ws, void *const *events, cudaStream_t s) {
+  CUtensorMap mX, mB, mC, mY, mC32, mBQ, mXQ, mH, mYQ;
+  const cuuint64_t hdims[3] = {static_cast<cuuint64_t>(pl.P), static_cast<cuuint64_t>(pl.N),
+                               static_cast<cuuint64_t>(pl.b * pl.nc * pl.H)};
+  const cuuint64_t hstr[2] = {static_cast<cuuint64_t>(pl.P * 2),
+                              static_cast<cuuint64_t>(pl.N * pl.P * 2)};
+  const cuuint32_t hbox[3] = {64, static_cast<cuuint32_t>(pl.N), 1};
+  __nv_bfloat16 *Hin = reinterpret_cast<__nv_bfloat16 *>(ws + pl.Hin_off);
+  if (!encode_btgw(&mX, x, pl.b, pl.T, pl.H, pl.P, 128) ||
+      !encode_btgw(&mB, B, pl.b, pl.T, 1, pl.N, 128) ||
+      !encode_btgw(&mC, C, pl.b, pl.T, 1, pl.N, 128) ||
+      !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, 128) ||
+      !encode_btgw(&mC32, C, pl.b, pl.T, 1, pl.N, 32) ||
+      !encode_btgw(&mBQ, B, pl.b, pl.T, 1, pl.N, pl.Q) ||
+      !encode_btgw(&mXQ, x, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
+      !encode_btgw(&mYQ, y, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
+      !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
+    return SSD_ERR_CUDA;
+  uint8_t *flags = ws + pl.flags_off;
+  float *u = reinterpret_cast<float *>(ws + pl.u_off);
+  float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
+  float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
+  const int64_t items = pl.b * ((pl.H + 1) / 2);
+  const int64_t split = items - pl.whole;
+  const int H = static_cast<int>(pl.H);
+  using L = ssd::FusedHB;
+  if (!ensure_smem<ssd::chunk_fused_hb<true>>(L::kBytes) ||
+      !ensure_smem<ssd::chunk_fused_hb<false>>(L::kBytes))
+    return SSD_ERR_CUDA;
+  int ev = 0;
+  record(events, ev, s);
+  ssd_status st;
+  bool pdl = false;
+  if (pl.nseg > 1) {
+    const int64_t ctas = split * (pl.nseg - 1);
+    st = launch_dependent(false, ssd::chunk_fused_hb<false>, dim3(static_cast<unsigned>(ctas)),
+                          dim3(ssd::kFuThreads), L::kBytes, s, mX, mB, mC, mY, dt, A, D, h0,
+                          h_final, Hin, flags, u, pl.T, H, pl.nc, pl.softplus ? 1 : 0,
+                          static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg);
+    if (st != SSD_OK) return st;
+    record(events, ++ev, s);
+    pdl = pdl_on(events);
+  }
+  const int64_t ctas = pl.whole + split * (pl.nseg > 1 ? pl.nseg : 0);
+  st = launch_dependent(pdl, ssd::chunk_fused_hb<true>, dim3(static_cast<unsigned>(ctas)),
+                        dim3(ssd::kFuThreads), L::kBytes, s, mX, mB, mC, mY, dt, A, D, h0, h_final,
+                        Hin, flags, u, pl.T, H, pl.nc, pl.softplus ? 1 : 0,
+                        static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg);
+  if (st != SSD_OK) return st;
+  record(events, ++ev, s);
+  // the flagged (chunk, head) units, head by head (blocks that find none exit)
+  if (!ensure_smem<ssd::chunk_scan_hb>(ssd::kHbLaunchBytes)) return SSD_ERR_CUDA;
+  const int64_t kmax = ssd::ScanHL<256, 64>::kMaxFlaggedHeads;
+  const int flagged_sets =
+      static_cast<int>(std::max<int64_t>(kFlaggedSets, (pl.H + kmax - 1) / kmax));
+  const int64_t blocks = static_cast<int64_t>(flagged_sets) * pl.nc * pl.b;
+  st = launch_dependent(pdl_on(events), ssd::chunk_scan_hb, dim3(static_cast<unsigned>(blocks)),
+                        dim3(ssd::kHbThreads), ssd::kHbLaunchBytes, s, mC32, mBQ, mXQ, mH, mYQ, mY,
+                        dt, A, D, u, static_cast<const uint8_t *>(flags), pl.T,
+                        static_cast<int>(pl.b), H, pl.nc, 1, 0, flagged_sets, pl.softplus ? 1 : 0);
+  if (st != SSD_OK) return st;
+  record(events, ++ev, s);
+  return SSD_OK;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   if (!a || !b) return false;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -554,6 +670,9 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
   float *S = reinterpret_cast<float *>(ws + pl.S_off);
   void *Hin = ws + pl.Hin_off;
 
+  if (pl.fused)
+    return launch_fused(pl, x, dt, A, B, C, D, h0, y, h_final, ws, events,
+                        static_cast<cudaStream_t>(stream));
   if (pl.tc) {
     CUtensorMap mX, mB, mC32, mH, mY;
     const cuuint64_t hdims[3] = {static_cast<cuuint64_t>(pl.P), static_cast<cuuint64_t>(pl.N),
@@ -622,6 +741,7 @@ ssd_status fwd_impl(const ssd_dims *dims, const void *x, const float *dt, const 
 }
 
 int num_stages(const Plan &pl) {
+  if (pl.fused) return pl.nseg > 1 ? 3 : 2;
   return pl.tc ? (pl.nseg > 1 ? 3 : 2) + (pl.state_hb ? 1 : 0) : 4;
 }
 const char *const kStageNamesSimt[] = {"dt_cumsum", "chunk_state_simt", "state_passing",
@@ -676,6 +796,10 @@ const char *ssd_fwd_stage_name(const ssd_dims *dims, int32_t chunk, int32_t i) {
   Plan pl;
   if (make_plan(dims, chunk, &pl) != SSD_OK || i < 0 || i >= num_stages(pl)) return nullptr;
   if (!pl.tc) return kStageNamesSimt[i];
+  if (pl.fused) {
+    if (pl.nseg > 1 && i-- == 0) return "chunk_fused_prepass";
+    return i == 0 ? "chunk_fused_hb" : "chunk_scan_flagged";
+  }
   if (pl.state_hb && i-- == 0) return "dt_decay";
   if (i == 0) return pl.state_hb ? "chunk_state_hb" : "chunk_state_pass_tc";
   if (i == 1 && pl.nseg > 1) return "state_fixup";

@@ -57,28 +57,32 @@ def test_workspace_size_layout():
     assert S.ssd_fwd_workspace_size(d2, 256) > S.ssd_fwd_workspace_size(d, 256)
 
 
-def test_stage_names_follow_the_path():
-    # the last wave's chunk-state items split into segments: a fix-up stage
-    assert [S.ssd_fwd_stage_name(_dims(), 256, i) for i in range(4)] == \
-        ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
-    # 37 x 40 head pairs = ten full waves of 148: no split, no fix-up
-    assert [S.ssd_fwd_stage_name(_dims(batch=37), 256, i) for i in range(4)] == \
-        ["dt_decay", "chunk_state_hb", "chunk_scan_hb", None]
-    assert [S.ssd_fwd_stage_name(_dims(ngroups_c=2), 256, i) for i in range(2)] == \
-        ["chunk_state_pass_tc", "chunk_scan_hl"]
-    assert [S.ssd_fwd_stage_name(_dims(io_dtype=S.SSD_F32), 64, i) for i in range(4)] == \
+def test_stage_names_follow_the_path(monkeypatch):
+    monkeypatch.delenv("SSD_FUSED", raising=False)
+    monkeypatch.delenv("SSD_CHUNK_SCAN", raising=False)
+    names = lambda d, q=256: [S.ssd_fwd_stage_name(d, q, i) for i in range(S.ssd_fwd_num_stages(d, q))]
+    # 256-token chunks of 64-wide heads, one (B, C) group: the one-pass kernel;
+    # the last wave's items split into segments need its prepass
+    assert names(_dims()) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
+    # 37 x 40 head pairs = ten full waves of 148: no split, no prepass
+    assert names(_dims(batch=37)) == ["chunk_fused_hb", "chunk_scan_flagged"]
+    # one long sequence over 80 heads: every item split
+    long = _dims(batch=1, seqlen=16384)
+    assert names(long) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
+    assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
+    assert names(_dims(ngroups_c=2)) == ["chunk_state_pass_tc", "chunk_scan_hl"]
+    assert names(_dims(io_dtype=S.SSD_F32), 64) == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
     assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"
-    assert S.ssd_fwd_stage_name(_dims(), 256, 4) is None
-    assert S.ssd_fwd_num_stages(_dims(), 256) == 4
+    assert S.ssd_fwd_stage_name(_dims(), 256, 3) is None
     assert S.ssd_fwd_num_stages(_dims(), 128) == 2
     assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
-    # one long sequence over 80 heads: the state pass is split into sequence
-    # segments, joined by a fix-up stage
-    long = _dims(batch=1, seqlen=16384)
-    assert [S.ssd_fwd_stage_name(long, 256, i) for i in range(S.ssd_fwd_num_stages(long, 256))] == \
-        ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
-    assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
+    # SSD_FUSED=0: the two-pass head-pair kernels; the last wave's chunk-state
+    # items split into segments joined by a fix-up stage
+    monkeypatch.setenv("SSD_FUSED", "0")
+    assert names(_dims()) == ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
+    assert names(_dims(batch=37)) == ["dt_decay", "chunk_state_hb", "chunk_scan_hb"]
+    assert names(long) == ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
 
 
 def _scan_stage(d, chunk=256):
@@ -87,6 +91,7 @@ def _scan_stage(d, chunk=256):
 
 def test_chunk_scan_form_follows_work_per_cta_and_override(monkeypatch):
     monkeypatch.delenv("SSD_CHUNK_SCAN", raising=False)
+    monkeypatch.setenv("SSD_FUSED", "0")  # the two-pass kernels choose a chunk-scan form
     d = _dims()  # 64 (batch, chunk) items x 40 head pairs: head pairs
     window = _dims(batch=1, seqlen=4096)  # 16 items: too few pairs per CTA
     assert _scan_stage(d) == "chunk_scan_hb"

@@ -144,7 +144,17 @@ def chunk_log2_decays(inp, Q):
     return a.reshape(b, nc, Q, H).sum(axis=2)
 
 
-@pytest.mark.parametrize("form", ["pair", "head"])
+def set_form(monkeypatch, form):
+    """fused: the one-pass kernel (the default); pair / head: the two-pass
+    head-pair kernels with the chunk-scan form forced."""
+    if form == "fused":
+        monkeypatch.delenv("SSD_CHUNK_SCAN", raising=False)
+        monkeypatch.delenv("SSD_FUSED", raising=False)
+    else:
+        monkeypatch.setenv("SSD_CHUNK_SCAN", form)
+
+
+@pytest.mark.parametrize("form", ["fused", "pair", "head"])
 @pytest.mark.parametrize("a_scale,window", [
     ((30.0, 1.0, 30.0, 1.0, 1.0), None),       # heads 0 and 2 decay past the scaled form's range
     ((30.0, 30.0, 30.0, 30.0, 30.0), None),    # every head does
@@ -158,8 +168,10 @@ def test_fwd_q256_long_decay_heads(a_scale, window, form, monkeypatch):
     flagged by the chunk-state kernel and computed one by one in the head-pair
     launch; either way, and with the head-by-head kernel throughout, every
     head's y and state match the oracle (odd head count, so one pair has a
-    single head; ragged last chunk; random h0)."""
-    monkeypatch.setenv("SSD_CHUNK_SCAN", form)
+    single head; ragged last chunk; random h0).  The one-pass kernel applies
+    the same range test to each 128-token half of a chunk and leaves the
+    chunks that fail it to the per-head body."""
+    set_form(monkeypatch, form)
     shape = F(2, 700, 5, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 41)
     inp["A"] = (inp["A"] * np.asarray(a_scale, dtype=np.float32)).astype(np.float32)
@@ -196,6 +208,47 @@ def test_fwd_q256_last_wave_split_into_segments(form, monkeypatch):
     check_fwd(shape, 29, pairs=pairs)
 
 
+def test_fwd_fused_last_wave_split_into_segments(monkeypatch):
+    """One-pass kernel, 4 x 40 head pairs on 148 SMs: 148 items run whole, the
+    last 12 in four one-chunk segments whose entering states come from the
+    prepass; heads on both sides of the boundary match the oracle."""
+    set_form(monkeypatch, "fused")
+    shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = S.make_dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate)
+    names = [S.ssd_fwd_stage_name(d, 256, i) for i in range(S.ssd_fwd_num_stages(d, 256))]
+    assert names == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
+    H = shape.nheads
+    pairs = [0, 1, 2 * H + 79, 3 * H + 54, 3 * H + 55, 3 * H + 56, 3 * H + 57, 3 * H + 70,
+             3 * H + 79]
+    check_fwd(shape, 29, pairs=pairs)
+
+
+@pytest.mark.parametrize("shape,seed", [
+    (F(1, 3000, 3, 64, 128, 1, 1, 256, synth.BF16, "all"), 30),   # 12 one-chunk segments
+    (F(3, 1000, 37, 64, 128, 1, 1, 256, synth.BF16, "half"), 31),  # odd H, 2 segments
+    (F(2, 129, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 32),    # one token in the second stage
+])
+def test_fwd_fused_segments_and_ragged(shape, seed, monkeypatch):
+    set_form(monkeypatch, "fused")
+    check_fwd(shape, seed)
+
+
+def test_fwd_fused_matches_two_pass():
+    """The one-pass kernel and the two-pass head-pair kernels agree within the
+    tolerance on the same inputs (both are compared with the oracle elsewhere)."""
+    shape = F(2, 1500, 6, 64, 128, 1, 1, 256, synth.BF16, "all")
+    d = to_dev(synth.make_fwd_inputs(shape, 33), shape.io)
+    y1, h1 = run_fwd(d, 256)
+    import os
+    os.environ["SSD_FUSED"] = "0"
+    try:
+        y2, h2 = run_fwd(d, 256)
+    finally:
+        del os.environ["SSD_FUSED"]
+    assert (y1.float() - y2.float()).abs().max() / y2.float().abs().max() < 1e-2
+    assert (h1 - h2).abs().max() / h2.abs().max() < 1e-2
+
+
 def test_fwd_tc_without_softplus_and_D():
     check_fwd(F(1, 300, 2, 64, 128, 1, 1, 256, synth.BF16, "all"), 41, dt_softplus=False,
               D_none=True)
@@ -219,7 +272,8 @@ def test_fwd_f32_without_softplus_and_D():
 
 def test_fwd_stage_path_matches_dtype():
     d = S.make_dims(8, 2048, 80, 64, 128)
-    assert S.ssd_fwd_stage_name(d, 256, S.ssd_fwd_num_stages(d, 256) - 1) == "chunk_scan_hb"
+    assert [S.ssd_fwd_stage_name(d, 256, i) for i in range(S.ssd_fwd_num_stages(d, 256))] == \
+        ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
     assert S.ssd_fwd_stage_name(d, 128, 1) == "chunk_scan_hl"
 
 
@@ -301,6 +355,45 @@ def test_fwd_head_pair_path_graph_and_serial_launch_agree(monkeypatch):
     monkeypatch.setenv("SSD_CHUNK_SCAN", "pair")
     shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")
     d = to_dev(synth.make_fwd_inputs(shape, 56), shape.io)
+    y_ref, h_ref = run_fwd(d, 256)
+    monkeypatch.setenv("SSD_PDL", "0")
+    y_ser, h_ser = run_fwd(d, 256)
+    assert torch.equal(y_ser, y_ref) and torch.equal(h_ser, h_ref)
+    monkeypatch.delenv("SSD_PDL")
+    b, T, H, P = d["x"].shape
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    ws = S.workspace_for(dims, 256)
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((b, H, d["B"].shape[3], P), device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], 256, y, hf, ws,
+                  stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], 256, y, hf, ws,
+                  stream=stream)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        hf.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        S.ssd_check_device_error()
+        assert torch.equal(y, y_ref) and torch.equal(hf, h_ref)
+
+
+def test_fwd_fused_graph_and_serial_launch_agree(monkeypatch):
+    """The one-pass path with a prepass (dt -> prepass -> one-pass kernel ->
+    flagged-head pass, each after the first a programmatic dependent of the
+    one before): eager, replayed from a CUDA graph, and launched one after
+    another (SSD_PDL=0) give the same bits; long-decay heads make the flagged
+    pass do work."""
+    set_form(monkeypatch, "fused")
+    shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")
+    inp = synth.make_fwd_inputs(shape, 57)
+    inp["A"] = (inp["A"] * np.float32(12.0)).astype(np.float32)
+    d = to_dev(inp, shape.io)
     y_ref, h_ref = run_fwd(d, 256)
     monkeypatch.setenv("SSD_PDL", "0")
     y_ser, h_ser = run_fwd(d, 256)
