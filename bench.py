@@ -164,6 +164,12 @@ def fwd_work(s: synth.FwdShape):
     # the head-pair kernels: the same inputs and outputs
     stages["chunk_scan_hb"] = stages["chunk_scan_hl"]
     stages["chunk_state_hb"] = stages["chunk_state_pass_tc"]
+    # the one-pass kernel moves the layer's whole mandatory I/O (its prepass
+    # re-reads x, B and dt of the split items' segments, and the flagged pass
+    # the few long-decay (chunk, head) units: bounded above by these)
+    stages["chunk_fused_hb"] = stage(layer_bytes, layer_bytes, flops)
+    stages["chunk_fused_prepass"] = stage(0, x + Bb + dt, f_state)
+    stages["chunk_scan_flagged"] = stage(0, 2 * x + Bb + Cb + dt + hin16, f_scan)
     return dict(layer_bytes=layer_bytes, flops=flops, stages=stages, tok_heads=b * T * H)
 
 
