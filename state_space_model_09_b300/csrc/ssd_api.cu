@@ -186,12 +186,18 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     pl->Hin_off = 0;
     pl->total = align_up(states * 2);
     const bool hb_shape = pl->Q == 256 && pl->P == 64 && pl->GB == 1 && pl->GC == 1;
-    // SSD_FUSED=0, or a forced chunk-scan form (SSD_CHUNK_SCAN), selects the
-    // two-pass head-pair kernels instead of the one-pass kernel (for tests
-    // and comparisons; the results agree within the tolerance)
+    // The one-pass kernel when the (batch row, head pair) items fill at least
+    // one wave of the SMs; with fewer (a long sequence over few heads) every
+    // item would be split, and the two-pass kernels, whose chunk scan runs
+    // over all chunks in parallel, are faster.  SSD_FUSED=1 / =0 forces one
+    // or the other, as does a forced chunk-scan form (SSD_CHUNK_SCAN) the
+    // two-pass kernels (for tests and comparisons; the results agree within
+    // the tolerance).
     const char *fz = std::getenv("SSD_FUSED");
     const char *force = std::getenv("SSD_CHUNK_SCAN");
-    pl->fused = hb_shape && !(fz && std::strcmp(fz, "0") == 0) && !(force && *force);
+    const bool fill = pl->b * ((pl->H + 1) / 2) >= num_sms();
+    pl->fused = hb_shape && !(force && *force) &&
+                (fz && *fz ? std::strcmp(fz, "0") != 0 : fill);
     pl->state_hb = hb_shape && !pl->fused;
     if (pl->fused) plan_fused(pl);
     else plan_segments(pl);

@@ -114,10 +114,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// The same test, letting the hardware suspend the thread until the phase
+// completes or about suspend_ns have passed, so that a waiting warp does not
+// keep taking issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return done != 0;
+}
 
 // Time limit of every device-side wait.  A correct launch waits microseconds;
 // the limit only bounds a broken one.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Longest hardware suspension of one test inside a wait (the thread resumes
+// as soon as the phase completes); the time limit is checked between tests.
+constexpr uint32_t kWaitSuspendNs = 20000;
 
 // Waits for phase `parity` of `bar`.  Returns false, after recording
 // kDevTimeout, if the phase has not completed within limit_ns, or at once
@@ -128,8 +146,8 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
+    if ((it & 7u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
         report_error(kDevTimeout);

@@ -66,10 +66,14 @@ def test_stage_names_follow_the_path(monkeypatch):
     assert names(_dims()) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
     # 37 x 40 head pairs = ten full waves of 148: no split, no prepass
     assert names(_dims(batch=37)) == ["chunk_fused_hb", "chunk_scan_flagged"]
-    # one long sequence over 80 heads: every item split
+    # one long sequence over 80 heads: 40 items, fewer than the SMs, so the
+    # two-pass kernels (the one-pass kernel on request)
     long = _dims(batch=1, seqlen=16384)
-    assert names(long) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
+    assert names(long) == ["dt_decay", "chunk_state_hb", "state_fixup", "chunk_scan_hb"]
     assert S.ssd_fwd_workspace_size(long, 256) > 1 * 64 * 80 * 128 * 64 * 2
+    monkeypatch.setenv("SSD_FUSED", "1")
+    assert names(long) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
+    monkeypatch.delenv("SSD_FUSED")
     assert names(_dims(ngroups_c=2)) == ["chunk_state_pass_tc", "chunk_scan_hl"]
     assert names(_dims(io_dtype=S.SSD_F32), 64) == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]

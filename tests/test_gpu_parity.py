@@ -145,11 +145,12 @@ def chunk_log2_decays(inp, Q):
 
 
 def set_form(monkeypatch, form):
-    """fused: the one-pass kernel (the default); pair / head: the two-pass
-    head-pair kernels with the chunk-scan form forced."""
+    """fused: the one-pass kernel (forced; the default when the items fill a
+    wave of the SMs); pair / head: the two-pass head-pair kernels with the
+    chunk-scan form forced."""
     if form == "fused":
         monkeypatch.delenv("SSD_CHUNK_SCAN", raising=False)
-        monkeypatch.delenv("SSD_FUSED", raising=False)
+        monkeypatch.setenv("SSD_FUSED", "1")
     else:
         monkeypatch.setenv("SSD_CHUNK_SCAN", form)
 
@@ -233,18 +234,15 @@ def test_fwd_fused_segments_and_ragged(shape, seed, monkeypatch):
     check_fwd(shape, seed)
 
 
-def test_fwd_fused_matches_two_pass():
+def test_fwd_fused_matches_two_pass(monkeypatch):
     """The one-pass kernel and the two-pass head-pair kernels agree within the
     tolerance on the same inputs (both are compared with the oracle elsewhere)."""
     shape = F(2, 1500, 6, 64, 128, 1, 1, 256, synth.BF16, "all")
     d = to_dev(synth.make_fwd_inputs(shape, 33), shape.io)
+    monkeypatch.setenv("SSD_FUSED", "1")
     y1, h1 = run_fwd(d, 256)
-    import os
-    os.environ["SSD_FUSED"] = "0"
-    try:
-        y2, h2 = run_fwd(d, 256)
-    finally:
-        del os.environ["SSD_FUSED"]
+    monkeypatch.setenv("SSD_FUSED", "0")
+    y2, h2 = run_fwd(d, 256)
     assert (y1.float() - y2.float()).abs().max() / y2.float().abs().max() < 1e-2
     assert (h1 - h2).abs().max() / h2.abs().max() < 1e-2
 
