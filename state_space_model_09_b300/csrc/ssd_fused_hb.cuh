@@ -62,6 +62,15 @@
 
 namespace ssd {
 
+// Multiplies the 8 bf16 values of a 16-byte chunk by s with packed bf16
+// multiplies (s rounded to bf16 once; each product rounded to nearest even).
+__device__ __forceinline__ uint4 scale_bf16x8_packed(uint4 v, __nv_bfloat162 s2) {
+  __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = __hmul2(p[i], s2);
+  return v;
+}
+
 constexpr int kFuWarps = 20;
 constexpr int kFuThreads = 32 * kFuWarps;
 constexpr int kFuCompute = 16;
@@ -409,9 +418,11 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         }
       }
     }
+    // a wait for the whole warp: every lane waits on the same phase, so they
+    // agree unless one ran out of time (which sets the abort flag for all)
     auto wait_all = [&](uint64_t *bar, uint32_t par) -> bool {
       const bool w = mbar_wait(bar, par, abort_flag);
-      return __all_sync(0xffffffffu, w) && !*abort_flag;
+      return __all_sync(0xffffffffu, w);
     };
     auto tables_ready = [&](int g) {
       return wait_all(&bars[kFuTabFull0 + g % L::kTabBufs], (g >> 2) & 1);
@@ -420,7 +431,9 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     // stage g's x rows *= t_j in place (16-byte chunks, four per thread)
     auto scale = [&](int g) -> bool {
       const int xk = g % L::kXSlots;
-      if (!tables_ready(g) || !wait_all(&bars[kFuXfull0 + xk], (g / L::kXSlots) & 1)) return false;
+      // (the full pass calls it right after enter(g), which waited for the tables)
+      if ((!FULL && !tables_ready(g)) || !wait_all(&bars[kFuXfull0 + xk], (g / L::kXSlots) & 1))
+        return false;
       const float *tb = tab + (g % L::kTabBufs) * L::kTabFloats;
       uint8_t *xb = Xs + xk * L::kTile;
 #pragma unroll
@@ -428,7 +441,8 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const int uu = tid + kFuCompute * 32 * m;
         const int x_h = uu >> 10, j = (uu >> 3) & (S - 1), cc = uu & 7;
         uint4 *ptr = reinterpret_cast<uint4 *>(xb + x_h * S * 128 + sw128_offset(j, 8 * cc));
-        *ptr = scale_bf16x8(*ptr, tb[x_h * S + j]);
+        *ptr = FULL ? scale_bf16x8_packed(*ptr, __float2bfloat162_rn(tb[x_h * S + j]))
+                    : scale_bf16x8(*ptr, tb[x_h * S + j]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -485,13 +499,23 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     // P of stage g -> masked bf16 pairs (j <= i) in tensor memory
     auto mask = [&](int g) -> bool {
       if (!wait_all(&bars[kFuPready], g & 1)) return false;
-      tc_fence_after_sync();
-      float v[32];
-      uint32_t pk[16];
-      tmem_ld32(tmem + lane_base + L::kP + 32 * hs, v);
-      hb_mask_pack(v, n - 32 * hs, pk);
-      tmem_st16_u32(tmem + lane_base + L::kM + 16 * hs, pk);
-      tmem_st_wait();
+      // (row quarter q, column block hs): below the diagonal block (q > hs)
+      // nothing is masked, on it (q == hs) columns j <= i are kept, and above
+      // it (q < hs) the block stays zero from the start
+      if (q >= hs) {
+        tc_fence_after_sync();
+        float v[32];
+        uint32_t pk[16];
+        tmem_ld32(tmem + lane_base + L::kP + 32 * hs, v);
+        if (q > hs) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+        } else {
+          hb_mask_pack(v, lane, pk);
+        }
+        tmem_st16_u32(tmem + lane_base + L::kM + 16 * hs, pk);
+        tmem_st_wait();
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kFuMready]);
@@ -525,9 +549,10 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const float d = sc[kScD];
         uint8_t *xrow = Xs + xk * L::kTile + hh * S * 128;
 #pragma unroll
+        float v32[32];
+        tmem_ld32(tmem + lane_base + L::kY + 32 * hs, v32);
         for (int half = 0; half < 2; ++half) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + L::kY + 32 * hs + 16 * half, v);
+          const float *v = v32 + 16 * half;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             uint4 *ptr =
@@ -561,6 +586,11 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     };
 
     if (FULL) {
+      if (q < hs) {  // the masked C B^T's blocks above the diagonal: zero throughout
+        const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+        tmem_st16_u32(tmem + lane_base + L::kM + 16 * hs, z);
+        tmem_st_wait();
+      }
       ok = ok && enter(0) && scale(0);
       for (int g = 0; g < nstages && ok; ++g) {
         if (g > 0 && !(ok = epilogue(g - 1))) break;
