@@ -527,10 +527,17 @@ __global__ void __launch_bounds__(kHbThreads, 1)
   } else {
     grid_dep_wait();  // the flags, u and the chunk states of the kernels before
     const int64_t j = i - n_hb;
-    scan_hl_body<256, 64, true>(
-        static_cast<int>(j % flagged_sets), static_cast<int>((j / flagged_sets) % nc),
-        static_cast<int>(j / (static_cast<int64_t>(flagged_sets) * nc)), mapC32, mapB, mapX,
-        mapH, mapY, dt, A, D, T, H, 1, 1, nc, flagged_sets, softplus, flags, u);
+    const int set = static_cast<int>(j % flagged_sets), c = static_cast<int>((j / flagged_sets) % nc);
+    const int bb = static_cast<int>(j / (static_cast<int64_t>(flagged_sets) * nc));
+    // a block whose heads were all computed by the pass before leaves at once,
+    // before any set-up (usually all of them: long-decay chunks are rare)
+    int any = 0;
+    for (int h = set + static_cast<int>(threadIdx.x) * flagged_sets; h < H;
+         h += static_cast<int>(blockDim.x) * flagged_sets)
+      any |= flags[(static_cast<int64_t>(bb) * nc + c) * H + h] == 0;
+    if (!__syncthreads_or(any)) return;
+    scan_hl_body<256, 64, true>(set, c, bb, mapC32, mapB, mapX, mapH, mapY, dt, A, D, T, H, 1, 1,
+                                nc, flagged_sets, softplus, flags, u);
   }
 }
 
