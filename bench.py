@@ -50,18 +50,23 @@ L2_BYTES = 126 * 1024 * 1024
 MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
-    ("chunk_scan_hb", "mamba2_2p7b"):
-        (416_868_864, ("state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
+    ("chunk_fused_hb", "mamba2_2p7b"):
+        (349_817_088, ("state_space_model_09_b300/csrc/ssd_fused_hb.cuh",
                        "state_space_model_09_b300/csrc/ssd_scan.cuh",
+                       "state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
                        "state_space_model_09_b300/csrc/ssd_tc.cuh",
                        "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "f24fd1932ca4eee3cbb093f1d28f1136a52d4a55"),
-    ("chunk_state_hb", "mamba2_2p7b"):
-        (267_968_000, ("state_space_model_09_b300/csrc/ssd_state_hb.cuh",
-                       "state_space_model_09_b300/csrc/ssd_state.cuh",
+         "32b3b9ec303f21d9e4d6a3e8753647c193e7b56c"),
+    ("chunk_scan_hl", "hybrid_llama3_8b"):
+        (552_532_224, ("state_space_model_09_b300/csrc/ssd_scan.cuh",
                        "state_space_model_09_b300/csrc/ssd_tc.cuh",
                        "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "22cac97fdd2d9cfda95adf1a30d34cbaae2c66ea"),
+         "611043699da0318b501de1671ce8377c1a5da7a6"),
+    ("chunk_state_pass_tc", "hybrid_llama3_8b"):
+        (267_524_352, ("state_space_model_09_b300/csrc/ssd_state.cuh",
+                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
+                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
+         "35cf10d8ea7510bc28882c75765d47427529ac49"),
     ("multistep_kernel", "multistep_k8"):
         (70_129_920, ("state_space_model_09_b300/csrc/ssd_kernels.cuh",),
          "f1267a2133217f991f16eac81edf77c2e16126eb"),
