@@ -65,11 +65,14 @@ struct Plan {
   // dt_decay_kernel has written the per-token log2 decays [b, H, T] (u_off)
   bool state_hb = false;
   size_t u_off = 0;
-  // the same shapes, by default: the one-pass kernel (chunk_fused_hb), with
-  // its prepass when items are split (nseg > 1; whole, cps, seg_bh0, seg_rows,
-  // Fseg_off, Lseg_off as above) and the flagged-head pass after it; Hin,
-  // flags and u then hold the flagged (chunk, head) units only
+  // the one-pass kernel (chunk_fused_hb) for the same shapes and for 128-token
+  // chunks of 128-wide heads: items of fused_hp heads (2: two 64-wide heads
+  // of one (B, C) group; 1: one 128-wide head), fused_spc 128-token stages
+  // per chunk; with its prepass when items are split (nseg > 1; whole, cps,
+  // seg_bh0, seg_rows, Fseg_off, Lseg_off as above) and the flagged-head pass
+  // after it; Hin, flags and u then hold the flagged (chunk, head) units only
   bool fused = false;
+  int fused_hp = 2, fused_spc = 2;
 };
 
 int num_sms();
@@ -112,14 +115,15 @@ void plan_segments(Plan *pl) {
   pl->seg_rows = pl->b * pl->H - pl->seg_bh0;
 }
 
-// Segments of the one-pass kernel: one CTA per SM, one per (batch row, head
-// pair).  With more items than SMs the items of a last, partly filled wave
-// are split (the full waves' items run whole); with fewer, every item is; a
-// split item's nseg segments of cps chunks start from the states the prepass
-// computes.  E.g. 8 x 40 head pairs on 148 SMs: two full waves + 24 items in
-// four segments of two chunks; 1 x 40 pairs of 64 chunks: three segments.
+// Segments of the one-pass kernel: one CTA per SM, one per item (batch row,
+// head pair or 128-wide head).  With more items than SMs the items of a last,
+// partly filled wave are split (the full waves' items run whole); with fewer,
+// every item is, when at least two segments fit; a split item's nseg segments
+// of cps chunks start from the states the prepass computes.  E.g. 8 x 40 head
+// pairs on 148 SMs: two full waves + 24 items in four segments of two chunks;
+// 4 x 32 heads: one wave of 128 whole items.
 void plan_fused(Plan *pl) {
-  const int64_t npairs = (pl->H + 1) / 2, items = pl->b * npairs;
+  const int64_t ipb = (pl->H + pl->fused_hp - 1) / pl->fused_hp, items = pl->b * ipb;
   const int64_t slots = num_sms();
   int64_t nseg = 1, whole = items;
   if (items < slots) {
@@ -136,7 +140,7 @@ void plan_fused(Plan *pl) {
   pl->cps = static_cast<int>((pl->nc + nseg - 1) / nseg);
   pl->nseg = (pl->nc + pl->cps - 1) / pl->cps;
   pl->whole = pl->nseg > 1 ? whole : items;
-  pl->seg_bh0 = pl->whole / npairs * pl->H + 2 * (pl->whole % npairs);
+  pl->seg_bh0 = pl->whole / ipb * pl->H + pl->fused_hp * (pl->whole % ipb);
   pl->seg_rows = pl->b * pl->H - pl->seg_bh0;
 }
 
@@ -193,10 +197,16 @@ ssd_status make_plan(const ssd_dims *d, int32_t chunk, Plan *pl) {
     // or the other, as does a forced chunk-scan form (SSD_CHUNK_SCAN) the
     // two-pass kernels (for tests and comparisons; the results agree within
     // the tolerance).
+    // 128-token chunks of 128-wide heads (any groups) take it, one head per
+    // item, as soon as the items fill half the SMs.
     const char *fz = std::getenv("SSD_FUSED");
     const char *force = std::getenv("SSD_CHUNK_SCAN");
-    const bool fill = pl->b * ((pl->H + 1) / 2) >= num_sms();
-    pl->fused = hb_shape && !(force && *force) &&
+    const bool wide_shape = pl->Q == 128 && pl->P == 128;
+    pl->fused_hp = hb_shape ? 2 : 1;
+    pl->fused_spc = pl->Q / 128;
+    const int64_t items = pl->b * ((pl->H + pl->fused_hp - 1) / pl->fused_hp);
+    const bool fill = hb_shape ? items >= num_sms() : 2 * items >= num_sms();
+    pl->fused = (hb_shape || wide_shape) && !(force && *force) &&
                 (fz && *fz ? std::strcmp(fz, "0") != 0 : fill);
     pl->state_hb = hb_shape && !pl->fused;
     if (pl->fused) plan_fused(pl);
@@ -553,9 +563,10 @@ ssd_status launch_scan_hb(const Plan &pl, const CUtensorMap &mC32, const CUtenso
 // flagged (chunk, head) units by the per-head body (chunk_scan_hb's flagged
 // items alone).  Each kernel after the first is a programmatic dependent of
 // the one before (pdl); the first waits for everything before it.
-ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const float *A,
-                        const void *B, const void *C, const float *D, const float *h0, void *y,
-                        float *h_final, uint8_t *ws, void *const *events, cudaStream_t s) {
+template <int HP, int SPC, int Q, int P>
+ssd_status launch_fused_t(const Plan &pl, const void *x, const float *dt, const float *A,
+                          const void *B, const void *C, const float *D, const float *h0, void *y,
+                          float *h_final, uint8_t *ws, void *const *events, cudaStream_t s) {
   CUtensorMap mX, mB, mC, mY, mC32, mBQ, mXQ, mH, mYQ;
   const cuuint64_t hdims[3] = {static_cast<cuuint64_t>(pl.P), static_cast<cuuint64_t>(pl.N),
                                static_cast<cuuint64_t>(pl.b * pl.nc * pl.H)};
@@ -564,11 +575,11 @@ ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const fl
   const cuuint32_t hbox[3] = {64, static_cast<cuuint32_t>(pl.N), 1};
   __nv_bfloat16 *Hin = reinterpret_cast<__nv_bfloat16 *>(ws + pl.Hin_off);
   if (!encode_btgw(&mX, x, pl.b, pl.T, pl.H, pl.P, 128) ||
-      !encode_btgw(&mB, B, pl.b, pl.T, 1, pl.N, 128) ||
-      !encode_btgw(&mC, C, pl.b, pl.T, 1, pl.N, 128) ||
+      !encode_btgw(&mB, B, pl.b, pl.T, pl.GB, pl.N, 128) ||
+      !encode_btgw(&mC, C, pl.b, pl.T, pl.GC, pl.N, 128) ||
       !encode_btgw(&mY, y, pl.b, pl.T, pl.H, pl.P, 128) ||
-      !encode_btgw(&mC32, C, pl.b, pl.T, 1, pl.N, 32) ||
-      !encode_btgw(&mBQ, B, pl.b, pl.T, 1, pl.N, pl.Q) ||
+      !encode_btgw(&mC32, C, pl.b, pl.T, pl.GC, pl.N, 32) ||
+      !encode_btgw(&mBQ, B, pl.b, pl.T, pl.GB, pl.N, pl.Q) ||
       !encode_btgw(&mXQ, x, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
       !encode_btgw(&mYQ, y, pl.b, pl.T, pl.H, pl.P, pl.Q) ||
       !encode_bf16(&mH, Hin, 3, hdims, hstr, hbox))
@@ -577,12 +588,12 @@ ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const fl
   float *u = reinterpret_cast<float *>(ws + pl.u_off);
   float *Fseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Fseg_off) : nullptr;
   float *Lseg = pl.nseg > 1 ? reinterpret_cast<float *>(ws + pl.Lseg_off) : nullptr;
-  const int64_t items = pl.b * ((pl.H + 1) / 2);
+  const int64_t items = pl.b * ((pl.H + HP - 1) / HP);
   const int64_t split = items - pl.whole;
-  const int H = static_cast<int>(pl.H);
+  const int H = static_cast<int>(pl.H), GB = static_cast<int>(pl.GB), GC = static_cast<int>(pl.GC);
   using L = ssd::FusedHB;
-  if (!ensure_smem<ssd::chunk_fused_hb<true>>(L::kBytes) ||
-      !ensure_smem<ssd::chunk_fused_hb<false>>(L::kBytes))
+  if (!ensure_smem<ssd::chunk_fused_hb<true, HP, SPC>>(L::kBytes) ||
+      !ensure_smem<ssd::chunk_fused_hb<false, HP, SPC>>(L::kBytes))
     return SSD_ERR_CUDA;
   int ev = 0;
   record(events, ev, s);
@@ -590,34 +601,45 @@ ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const fl
   bool pdl = false;
   if (pl.nseg > 1) {
     const int64_t ctas = split * (pl.nseg - 1);
-    st = launch_dependent(false, ssd::chunk_fused_hb<false>, dim3(static_cast<unsigned>(ctas)),
-                          dim3(ssd::kFuThreads), L::kBytes, s, mX, mB, mC, mY, dt, A, D, h0,
-                          h_final, Hin, flags, u, pl.T, H, pl.nc, pl.softplus ? 1 : 0,
-                          static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg);
+    st = launch_dependent(false, ssd::chunk_fused_hb<false, HP, SPC>,
+                          dim3(static_cast<unsigned>(ctas)), dim3(ssd::kFuThreads), L::kBytes, s,
+                          mX, mB, mC, mY, dt, A, D, h0, h_final, Hin, flags, u, pl.T, H, GB, GC,
+                          pl.nc, pl.softplus ? 1 : 0, static_cast<int>(pl.whole), pl.nseg, pl.cps,
+                          pl.seg_bh0, Fseg, Lseg);
     if (st != SSD_OK) return st;
     record(events, ++ev, s);
     pdl = pdl_on(events);
   }
   const int64_t ctas = pl.whole + split * (pl.nseg > 1 ? pl.nseg : 0);
-  st = launch_dependent(pdl, ssd::chunk_fused_hb<true>, dim3(static_cast<unsigned>(ctas)),
+  st = launch_dependent(pdl, ssd::chunk_fused_hb<true, HP, SPC>, dim3(static_cast<unsigned>(ctas)),
                         dim3(ssd::kFuThreads), L::kBytes, s, mX, mB, mC, mY, dt, A, D, h0, h_final,
-                        Hin, flags, u, pl.T, H, pl.nc, pl.softplus ? 1 : 0,
+                        Hin, flags, u, pl.T, H, GB, GC, pl.nc, pl.softplus ? 1 : 0,
                         static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg);
   if (st != SSD_OK) return st;
   record(events, ++ev, s);
   // the flagged (chunk, head) units, head by head (blocks that find none exit)
-  if (!ensure_smem<ssd::chunk_scan_hb>(ssd::kHbLaunchBytes)) return SSD_ERR_CUDA;
-  const int64_t kmax = ssd::ScanHL<256, 64>::kMaxFlaggedHeads;
-  const int flagged_sets =
-      static_cast<int>(std::max<int64_t>(kFlaggedSets, (pl.H + kmax - 1) / kmax));
-  const int64_t blocks = static_cast<int64_t>(flagged_sets) * pl.nc * pl.b;
-  st = launch_dependent(pdl_on(events), ssd::chunk_scan_hb, dim3(static_cast<unsigned>(blocks)),
-                        dim3(ssd::kHbThreads), ssd::kHbLaunchBytes, s, mC32, mBQ, mXQ, mH, mYQ, mY,
-                        dt, A, D, u, static_cast<const uint8_t *>(flags), pl.T,
-                        static_cast<int>(pl.b), H, pl.nc, 1, 0, flagged_sets, pl.softplus ? 1 : 0);
+  using LH = ssd::ScanHL<Q, P>;
+  if (!ensure_smem<ssd::chunk_scan_flagged<Q, P>>(LH::kBytes)) return SSD_ERR_CUDA;
+  const int64_t kmax = LH::kMaxFlaggedHeads;
+  const int sets = static_cast<int>(std::max<int64_t>(kFlaggedSets, (pl.H + kmax - 1) / kmax));
+  const int64_t blocks = static_cast<int64_t>(sets) * pl.nc * pl.b;
+  if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
+  st = launch_dependent(pdl_on(events), ssd::chunk_scan_flagged<Q, P>,
+                        dim3(static_cast<unsigned>(blocks)), dim3(LH::kThreads), LH::kBytes, s,
+                        mC32, mBQ, mXQ, mH, mYQ, dt, A, D, static_cast<const float *>(u),
+                        static_cast<const uint8_t *>(flags), pl.T, H, GB, GC, pl.nc, sets,
+                        pl.softplus ? 1 : 0);
   if (st != SSD_OK) return st;
   record(events, ++ev, s);
   return SSD_OK;
+}
+
+ssd_status launch_fused(const Plan &pl, const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D, const float *h0, void *y,
+                        float *h_final, uint8_t *ws, void *const *events, cudaStream_t s) {
+  if (pl.fused_hp == 2)
+    return launch_fused_t<2, 2, 256, 64>(pl, x, dt, A, B, C, D, h0, y, h_final, ws, events, s);
+  return launch_fused_t<1, 1, 128, 128>(pl, x, dt, A, B, C, D, h0, y, h_final, ws, events, s);
 }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {

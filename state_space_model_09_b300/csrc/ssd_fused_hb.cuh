@@ -108,18 +108,26 @@ static_assert(kNumFuBars <= FusedHB::kBars, "barrier slots");
 
 // FULL: the whole layer for items whole.. and split segments; otherwise the
 // prepass of the split items' segments 0 .. nseg - 2 (final states, decays).
-template <bool FULL>
+// HP: heads per item -- 2 (two 64-wide heads sharing one (B, C) group, their
+// 128 columns side by side) or 1 (one 128-wide head, its two 64-column
+// halves side by side; B and C of its own groups).  SPC: 128-token stages per
+// chunk (2: 256-token chunks, 1: 128-token chunks); the flags, the flagged
+// units' states and u are kept per chunk.
+template <bool FULL, int HP, int SPC>
 __global__ void __launch_bounds__(kFuThreads, 1)
     chunk_fused_hb(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapY,
                    const float *__restrict__ dt, const float *__restrict__ A,
                    const float *__restrict__ D, const float *__restrict__ h0,
                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ Hin,
-                   uint8_t *__restrict__ flags, float *__restrict__ u, int64_t T, int H, int nc,
-                   int softplus, int whole, int nseg, int cps, int64_t bh0,
+                   uint8_t *__restrict__ flags, float *__restrict__ u, int64_t T, int H, int GB,
+                   int GC, int nc, int softplus, int whole, int nseg, int cps, int64_t bh0,
                    float *__restrict__ Fseg, float *__restrict__ Lseg) {
   using L = FusedHB;
-  constexpr int S = L::S, P = L::P, N = L::N;
+  constexpr int S = L::S, N = L::N;
+  constexpr int P = 128 / HP;  // the width of one head
+  static_assert(HP == 1 || HP == 2, "heads per item");
+  static_assert(SPC == 1 || SPC == 2, "stages per chunk");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *Xs = smem;                            // [slot][head][S rows][128 B]
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + L::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tslot + 1);
 
-  const int npairs = (H + 1) / 2;
+  const int ipb = (H + HP - 1) / HP;  // items per batch row
   const int cta = blockIdx.x;
   bool split;
   int item, seg;
@@ -146,13 +154,18 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     item = whole + cta / (nseg - 1);
     seg = cta % (nseg - 1);
   }
-  const int b = item / npairs, pair = item % npairs;
-  const int hb0 = 2 * pair, nh = min(2, H - hb0);
+  const int b = item / ipb;
+  const int hb0 = HP * (item % ipb), nh = min(HP, H - hb0);
+  const int gb = hb0 / (H / GB), gc = hb0 / (H / GC);  // the item's B and C groups
   const int c_begin = split ? seg * cps : 0;
   const int ncl = split ? min(nc, c_begin + cps) - c_begin : nc;
-  const int nstages = 2 * ncl;
+  const int nstages = SPC * ncl;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  auto stage_t0 = [&](int g) { return (2 * c_begin + g) * S; };
+  auto stage_t0 = [&](int g) { return (SPC * c_begin + g) * S; };
+  // column atom a (64 columns) of the item's 128: which head, which columns
+  auto atom_head = [&](int a) { return HP == 2 ? hb0 + a : hb0; };
+  auto atom_col = [&](int a) { return HP == 2 ? 0 : 64 * a; };
+  const int natoms = HP == 2 ? nh : 2;
 
   if (tid == 0) {
     for (int i = 0; i < L::kBars; ++i) {
@@ -177,30 +190,34 @@ __global__ void __launch_bounds__(kFuThreads, 1)
 
   if (warp == kFuTables || warp == kFuTables + 1) {
     // ================================================================ tables
-    // One head per warp, one chunk (two stages) at a time: lane owns 8
-    // consecutive tokens (lanes 0-15 the first stage, 16-31 the second);
-    // z = softplus(dt) A log2(e), running sums, a scan within each half-warp.
+    // One head per warp (the second warp idles when an item has one head),
+    // two stages at a time: lane owns 8 consecutive tokens (lanes 0-15 the
+    // first stage, 16-31 the second); z = softplus(dt) A log2(e), running
+    // sums, a scan within each half-warp.
     const int hh = warp - kFuTables;
     const bool mine = hh < nh;
     const int h = hb0 + min(hh, nh - 1);
     constexpr float kLog2e = 1.4426950408889634f;
     const float Ah = A[h] * kLog2e, Dh = D ? D[h] : 0.f;
     const int st = lane >> 4, sl = lane & 15;
+    const int npair = (nstages + 1) / 2;
     float raw[8], rawn[8];
-    auto fetch = [&](int lc, float (&rr)[8]) {
-      const int64_t t0 = static_cast<int64_t>(c_begin + lc) * L::Q + lane * 8;
+    auto fetch = [&](int lp, float (&rr)[8]) {
+      const int64_t t0 = static_cast<int64_t>(stage_t0(2 * lp)) + lane * 8;
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         rr[e] = t0 + e < T ? dt[(static_cast<int64_t>(b) * T + t0 + e) * H + h] : 0.f;
     };
     float prod = 1.f;  // prepass: the segment's total decay
-    if (ncl > 0) fetch(0, rawn);
-    for (int lc = 0; lc < ncl; ++lc) {
-      const int c = c_begin + lc;
-      const int64_t t0 = static_cast<int64_t>(c) * L::Q + lane * 8;
+    if (npair > 0) fetch(0, rawn);
+    for (int lp = 0; lp < npair; ++lp) {
+      const int g0 = 2 * lp, gs = g0 + st;  // this half-warp's stage
+      const bool have = gs < nstages;
+      const int c = c_begin + gs / SPC;     // and its chunk
+      const int64_t t0 = static_cast<int64_t>(stage_t0(g0)) + lane * 8;
 #pragma unroll
       for (int e = 0; e < 8; ++e) raw[e] = rawn[e];
-      if (lc + 1 < ncl) fetch(lc + 1, rawn);
+      if (lp + 1 < npair) fetch(lp + 1, rawn);
       float z[8], v[8];
       float run = 0.f;
 #pragma unroll
@@ -218,19 +235,20 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       const float base = incl - run;
       const float last0 = __shfl_sync(0xffffffffu, incl, 15);
       const float last1 = __shfl_sync(0xffffffffu, incl, 31);
-      const bool fast = FULL && scaled_form_ok(last0) && scaled_form_ok(last1);
+      // the scaled form holds for a chunk when it holds for each of its stages
+      const bool ok0 = scaled_form_ok(last0), ok1 = scaled_form_ok(last1);
+      const bool fast = FULL && (SPC == 2 ? ok0 && ok1 : (st ? ok1 : ok0));
       const float a_last = st ? last1 : last0;
       const float r = fast ? scaled_form_ref(a_last) : a_last;
-      const int g0 = 2 * lc;
       bool ok = true;
-      for (int s = 0; s < 2 && ok; ++s) {
-        const int g = g0 + s;
+      for (int s2 = 0; s2 < 2 && ok; ++s2) {
+        const int g = g0 + s2;
         if (g >= L::kTabBufs)
           ok = mbar_wait(&bars[kFuTabEmpty0 + g % L::kTabBufs], ((g >> 2) - 1) & 1, abort_flag);
       }
       if (!ok) break;
-      if (mine) {
-        float *tb = tab + ((g0 + st) % L::kTabBufs) * L::kTabFloats;
+      if (mine && have) {
+        float *tb = tab + (gs % L::kTabBufs) * L::kTabFloats;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float av = v[e] + base;
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
           tb[2 * S + hh * S + sl * 8 + e] = fast ? ex2_approx(av - r) : 0.f;
         }
         if (sl == 0) {
-          float *sc = scal + ((g0 + st) % L::kTabBufs) * L::kScal + hh * 8;
+          float *sc = scal + (gs % L::kTabBufs) * L::kScal + hh * 8;
           sc[kScSfac] = ex2_approx(a_last - r);
           sc[kScDec] = ex2_approx(a_last);
           sc[kScHsc] = ex2_approx(r);
@@ -247,15 +265,16 @@ __global__ void __launch_bounds__(kFuThreads, 1)
           sc[kScHin] = fast ? 0.f : 1.f;
         }
         if (FULL) {
-          if (lane == 0) flags[(static_cast<int64_t>(b) * nc + c) * H + h] = fast ? 1 : 0;
+          if (sl == 0 && (SPC == 1 || st == 0))
+            flags[(static_cast<int64_t>(b) * nc + c) * H + h] = fast ? 1 : 0;
           if (!fast) {  // the per-token log2 decays, for the per-head body
             float *uh = u + (static_cast<int64_t>(b) * H + h) * T;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               if (t0 + e < T) uh[t0 + e] = z[e];
           }
-        } else if (lane == 0) {
-          prod *= ex2_approx(last0) * ex2_approx(last1);
+        } else if (sl == 0) {
+          prod *= ex2_approx(a_last);
         }
       }
       __syncwarp();
@@ -264,6 +283,8 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         mbar_arrive(&bars[kFuTabFull0 + (g0 + 1) % L::kTabBufs]);
       }
     }
+    // the prepass: the segment's total decay, the two half-warps' products
+    prod *= __shfl_sync(0xffffffffu, prod, 16);
     if (!FULL && mine && lane == 0)
       Lseg[(static_cast<int64_t>(b) * H + h - bh0) * nseg + seg] = prod;
   } else if (warp == kFuControl) {
@@ -276,20 +297,21 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         uint8_t *dst = FULL ? Bs : (k ? Cl : Bs);
         uint64_t *bar = &bars[kFuBfull0 + k];
         mbar_arrive_expect_tx(bar, L::kTile);
-        tma_load_4d(dst, &mapB, bar, 0, 0, stage_t0(g), b);
-        tma_load_4d(dst + S * 128, &mapB, bar, 64, 0, stage_t0(g), b);
+        tma_load_4d(dst, &mapB, bar, 0, gb, stage_t0(g), b);
+        tma_load_4d(dst + S * 128, &mapB, bar, 64, gb, stage_t0(g), b);
       };
       auto load_C = [&](int g) {
         mbar_arrive_expect_tx(&bars[kFuCfull], L::kTile);
-        tma_load_4d(Cl, &mapC, &bars[kFuCfull], 0, 0, stage_t0(g), b);
-        tma_load_4d(Cl + S * 128, &mapC, &bars[kFuCfull], 64, 0, stage_t0(g), b);
+        tma_load_4d(Cl, &mapC, &bars[kFuCfull], 0, gc, stage_t0(g), b);
+        tma_load_4d(Cl + S * 128, &mapC, &bars[kFuCfull], 64, gc, stage_t0(g), b);
       };
       load_B(0);
       if (FULL) load_C(0);
       else if (nstages > 1) load_B(1);
       constexpr uint32_t id_p = idesc_bf16(128, 128, false, false);  // C (TMEM) B^T (smem, K-major)
-      constexpr uint32_t id_s = idesc_bf16(128, 2 * P, true, true);  // B^T (MN-major) x~ (MN-major)
-      constexpr uint32_t id_y = idesc_bf16(128, 2 * P, false, true); // C or P (TMEM) H~ / x~ (MN-major)
+      // N = the item's 128 columns (two heads, or one 128-wide head)
+      constexpr uint32_t id_s = idesc_bf16(128, 128, true, true);    // B^T (MN-major) x~ (MN-major)
+      constexpr uint32_t id_y = idesc_bf16(128, 128, false, true);   // C or P (TMEM) H~ / x~ (MN-major)
       const uint32_t hs_ = smem_u32(Ht);
       for (int g = 0; g < nstages && !*abort_flag; ++g) {
         const int xk = g % L::kXSlots, bk = FULL ? 0 : (g & 1);
@@ -361,9 +383,10 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       auto load_x = [&](int g) {
         const int xk = g % L::kXSlots;
         uint64_t *bar = &bars[kFuXfull0 + xk];
-        mbar_arrive_expect_tx(bar, nh * S * 128);
-        for (int hh = 0; hh < nh; ++hh)
-          tma_load_4d(Xs + xk * L::kTile + hh * S * 128, &mapX, bar, 0, hb0 + hh, stage_t0(g), b);
+        mbar_arrive_expect_tx(bar, natoms * S * 128);
+        for (int a = 0; a < natoms; ++a)
+          tma_load_4d(Xs + xk * L::kTile + a * S * 128, &mapX, bar, atom_col(a), atom_head(a),
+                      stage_t0(g), b);
       };
       for (int g = 0; g < min(L::kXSlots, nstages); ++g) load_x(g);
       for (int g = 0; g < nstages; ++g) {
@@ -371,9 +394,10 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const uint32_t par = (g / L::kXSlots) & 1;
         if (FULL) {
           if (!mbar_wait(&bars[kFuYstaged0 + xk], par, abort_flag) || *abort_flag) break;
-          for (int hh = 0; hh < nh; ++hh)
-            if (ystore[2 * xk + hh])
-              tma_store_4d(&mapY, Xs + xk * L::kTile + hh * S * 128, 0, hb0 + hh, stage_t0(g), b);
+          for (int a = 0; a < natoms; ++a)
+            if (ystore[2 * xk + a])
+              tma_store_4d(&mapY, Xs + xk * L::kTile + a * S * 128, atom_col(a), atom_head(a),
+                           stage_t0(g), b);
           bulk_commit();
           bulk_wait_read0();  // the slot's y has been read
         } else if (!mbar_wait(&bars[kFuXfree0 + xk], par, abort_flag)) {
@@ -387,7 +411,10 @@ __global__ void __launch_bounds__(kFuThreads, 1)
   } else {
     // ================================================================ compute
     const int q = warp & 3, hs = warp >> 2;       // TMEM lane quarter; 32-column block
-    const int hh = hs >> 1, p0 = 32 * (hs & 1);   // head and first column (Y, S, H~)
+    // the block's 64-column atom and its columns inside it (shared memory),
+    // its head (tables) and its first column inside that head (global memory)
+    const int atom = hs >> 1, pa = 32 * (hs & 1);
+    const int hh = HP == 2 ? atom : 0, p0 = HP == 2 ? pa : 32 * hs;
     const int n = 32 * q + lane;                  // state row (S), token row (Y, P)
     const bool valid = hh < nh;
     const int h = hb0 + min(hh, nh - 1);
@@ -441,8 +468,8 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const int uu = tid + kFuCompute * 32 * m;
         const int x_h = uu >> 10, j = (uu >> 3) & (S - 1), cc = uu & 7;
         uint4 *ptr = reinterpret_cast<uint4 *>(xb + x_h * S * 128 + sw128_offset(j, 8 * cc));
-        *ptr = FULL ? scale_bf16x8_packed(*ptr, __float2bfloat162_rn(tb[x_h * S + j]))
-                    : scale_bf16x8(*ptr, tb[x_h * S + j]);
+        const float t = tb[(HP == 2 ? x_h : 0) * S + j];
+        *ptr = FULL ? scale_bf16x8_packed(*ptr, __float2bfloat162_rn(t)) : scale_bf16x8(*ptr, t);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -456,19 +483,19 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       if (!tables_ready(g) || !wait_all(&bars[kFuCfull], g & 1)) return false;
       const float *sc = sc_of(g);
       const float f = sc[kScHsc];
-      uint8_t *hrow = Ht + hh * N * 128;
+      uint8_t *hrow = Ht + atom * N * 128;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t w4[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           w4[i] = pack_bf16x2(f * st[8 * k + 2 * i], f * st[8 * k + 2 * i + 1]);
-        *reinterpret_cast<uint4 *>(hrow + sw128_offset(n, p0 + 8 * k)) =
+        *reinterpret_cast<uint4 *>(hrow + sw128_offset(n, pa + 8 * k)) =
             make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      if ((g & 1) == 0 && valid && sc[kScHin] != 0.f) {
+      if (g % SPC == 0 && valid && sc[kScHin] != 0.f) {  // a flagged chunk's start
         __nv_bfloat16 *dst =
-            Hin + (((static_cast<int64_t>(b) * nc + c_begin + (g >> 1)) * H + h) * N + n) * P + p0;
+            Hin + (((static_cast<int64_t>(b) * nc + c_begin + g / SPC) * H + h) * N + n) * P + p0;
 #pragma unroll
         for (int e = 0; e < 32; e += 16) {
           uint32_t w8[8];
@@ -547,16 +574,16 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       if (yw) {
         const float f = tab[(g % L::kTabBufs) * L::kTabFloats + 2 * S + hh * S + n];
         const float d = sc[kScD];
-        uint8_t *xrow = Xs + xk * L::kTile + hh * S * 128;
-#pragma unroll
+        uint8_t *xrow = Xs + xk * L::kTile + atom * S * 128;
         float v32[32];
         tmem_ld32(tmem + lane_base + L::kY + 32 * hs, v32);
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
           const float *v = v32 + 16 * half;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             uint4 *ptr =
-                reinterpret_cast<uint4 *>(xrow + sw128_offset(n, p0 + 16 * half + 8 * k));
+                reinterpret_cast<uint4 *>(xrow + sw128_offset(n, pa + 16 * half + 8 * k));
             const uint4 xv = *ptr;
             const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
             uint32_t o[4];
@@ -570,9 +597,9 @@ __global__ void __launch_bounds__(kFuThreads, 1)
           }
         }
       }
-      if (warp == 0 && lane < 2) {  // which heads' y the loader stores
+      if (warp == 0 && lane < 2) {  // which atoms' y the loader stores
         const float *s0 = scal + (g % L::kTabBufs) * L::kScal;
-        ystore[2 * xk + lane] = lane < nh && s0[8 * lane + kScYw] != 0.f;
+        ystore[2 * xk + lane] = lane < natoms && s0[8 * (HP == 2 ? lane : 0) + kScYw] != 0.f;
       }
       tc_fence_before_sync();
       fence_proxy_async_smem();
@@ -628,6 +655,34 @@ __global__ void __launch_bounds__(kFuThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kFuControl) tmem_dealloc(tmem, L::kAlloc);
+}
+
+// The (chunk, head) units the one-pass kernel left to the per-head chunk-scan
+// body (their decay falls outside its scaled form's range): one block per
+// (head set, chunk, batch row) -- set r of `sets` holds heads r, r + sets,
+// ... -- computing the set's flagged heads; a block with none leaves before
+// any set-up (usually all of them: such chunks are rare).
+template <int Q, int P>
+__global__ void __launch_bounds__(kScanThreads, 1)
+    chunk_scan_flagged(const __grid_constant__ CUtensorMap mapC32,
+                       const __grid_constant__ CUtensorMap mapB,
+                       const __grid_constant__ CUtensorMap mapX,
+                       const __grid_constant__ CUtensorMap mapH,
+                       const __grid_constant__ CUtensorMap mapY, const float *__restrict__ dt,
+                       const float *__restrict__ A, const float *__restrict__ D,
+                       const float *__restrict__ u, const uint8_t *__restrict__ flags, int64_t T,
+                       int H, int GB, int GC, int nc, int sets, int softplus) {
+  grid_dep_wait();  // the flags, u and the states of the one-pass kernel
+  const int64_t j = blockIdx.x;
+  const int set = static_cast<int>(j % sets), c = static_cast<int>((j / sets) % nc);
+  const int bb = static_cast<int>(j / (static_cast<int64_t>(sets) * nc));
+  int any = 0;
+  for (int h = set + static_cast<int>(threadIdx.x) * sets; h < H;
+       h += static_cast<int>(blockDim.x) * sets)
+    any |= flags[(static_cast<int64_t>(bb) * nc + c) * H + h] == 0;
+  if (!__syncthreads_or(any)) return;
+  scan_hl_body<Q, P, true>(set, c, bb, mapC32, mapB, mapX, mapH, mapY, dt, A, D, T, H, GB, GC, nc,
+                           sets, softplus, flags, u);
 }
 
 }  // namespace ssd

@@ -75,6 +75,13 @@ def test_stage_names_follow_the_path(monkeypatch):
     assert names(long) == ["chunk_fused_prepass", "chunk_fused_hb", "chunk_scan_flagged"]
     monkeypatch.delenv("SSD_FUSED")
     assert names(_dims(ngroups_c=2)) == ["chunk_state_pass_tc", "chunk_scan_hl"]
+    # the hybrid shape (128-token chunks of 128-wide heads, grouped B and C):
+    # 4 x 32 one-head items fill more than half the SMs -> the one-pass kernel
+    hyb = _dims(batch=4, seqlen=4096, nheads=32, headdim=128, ngroups_b=8, ngroups_c=32)
+    assert names(hyb, 128) == ["chunk_fused_hb", "chunk_scan_flagged"]
+    # one batch row: 32 items, too few -> the two-pass kernels
+    assert "chunk_fused_hb" not in names(_dims(batch=1, seqlen=4096, nheads=32, headdim=128,
+                                               ngroups_b=8, ngroups_c=32), 128)
     assert names(_dims(io_dtype=S.SSD_F32), 64) == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
     assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"

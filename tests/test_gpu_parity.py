@@ -234,6 +234,53 @@ def test_fwd_fused_segments_and_ragged(shape, seed, monkeypatch):
     check_fwd(shape, seed)
 
 
+def check_fwd_scaled_A(shape, seed, a_scale):
+    """check_fwd with A multiplied by a_scale (longer decays)."""
+    inp = synth.make_fwd_inputs(shape, seed)
+    inp["A"] = (inp["A"] * np.float32(a_scale)).astype(np.float32)
+    d = to_dev(inp, shape.io)
+    y, hf = run_fwd(d, shape.chunk)
+    pairs = list(range(shape.batch * shape.nheads))
+    y_ref, h_ref = oracle.ssd_seq(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["h0"], pairs=pairs)
+    ey = rel_err(y_pairs(y, pairs, shape.nheads), y_ref)
+    eh = rel_err(h_pairs(hf, pairs, shape.nheads), h_ref)
+    assert np.isfinite(ey) and ey <= TOL[synth.BF16], ey
+    assert np.isfinite(eh) and eh <= TOL[synth.BF16], eh
+
+
+@pytest.mark.parametrize("shape,seed,a_scale", [
+    # 128-token chunks of 128-wide heads, B in groups of heads, C per head;
+    # few items, so the prepass and segments run too
+    (F(2, 600, 8, 128, 128, 2, 8, 128, synth.BF16, "all"), 34, 1.0),
+    (F(1, 1000, 4, 128, 128, 1, 4, 128, synth.BF16, "half"), 35, 1.0),
+    (F(2, 129, 2, 128, 128, 1, 2, 128, synth.BF16, "all"), 37, 1.0),
+    # chunks decaying past the scaled form's range: left to the per-head body
+    (F(2, 700, 8, 128, 128, 2, 8, 128, synth.BF16, "all"), 36, 30.0),
+    (F(1, 900, 6, 128, 128, 3, 6, 128, synth.BF16, "all"), 38, 3.0),
+])
+def test_fwd_fused_wide_heads(shape, seed, a_scale, monkeypatch):
+    """The one-pass kernel with one 128-wide head per item (the Llama-3-8B
+    hybrid's head shape) matches the oracle."""
+    set_form(monkeypatch, "fused")
+    d = S.make_dims(shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                    shape.ngroups_b, shape.ngroups_c)
+    names = [S.ssd_fwd_stage_name(d, 128, i) for i in range(S.ssd_fwd_num_stages(d, 128))]
+    assert names[-2:] == ["chunk_fused_hb", "chunk_scan_flagged"], names
+    check_fwd_scaled_A(shape, seed, a_scale)
+
+
+def test_fwd_fused_wide_heads_matches_two_pass(monkeypatch):
+    shape = F(2, 1000, 8, 128, 128, 2, 8, 128, synth.BF16, "all")
+    d = to_dev(synth.make_fwd_inputs(shape, 39), shape.io)
+    monkeypatch.setenv("SSD_FUSED", "1")
+    y1, h1 = run_fwd(d, 128)
+    monkeypatch.setenv("SSD_FUSED", "0")
+    y2, h2 = run_fwd(d, 128)
+    assert (y1.float() - y2.float()).abs().max() / y2.float().abs().max() < 1e-2
+    assert (h1 - h2).abs().max() / h2.abs().max() < 1e-2
+
+
 def test_fwd_fused_matches_two_pass(monkeypatch):
     """The one-pass kernel and the two-pass head-pair kernels agree within the
     tolerance on the same inputs (both are compared with the oracle elsewhere)."""
