@@ -84,7 +84,8 @@ def test_stage_names_follow_the_path(monkeypatch):
                                                ngroups_b=8, ngroups_c=32), 128)
     assert names(_dims(io_dtype=S.SSD_F32), 64) == \
         ["dt_cumsum", "chunk_state_simt", "state_passing", "chunk_scan_simt"]
-    assert S.ssd_fwd_stage_name(_dims(headdim=128), 128, 1) == "chunk_scan_hl"
+    assert names(_dims(headdim=128), 128)[-2:] == ["chunk_fused_hb", "chunk_scan_flagged"]
+    assert names(_dims(headdim=128, batch=1, nheads=32), 128)[-1] == "chunk_scan_hl"
     assert S.ssd_fwd_stage_name(_dims(), 256, 3) is None
     assert S.ssd_fwd_num_stages(_dims(), 128) == 2
     assert S.ssd_fwd_num_stages(_dims(io_dtype=S.SSD_F32), 256) == 4
