@@ -62,15 +62,6 @@
 
 namespace ssd {
 
-// Multiplies the 8 bf16 values of a 16-byte chunk by s with packed bf16
-// multiplies (s rounded to bf16 once; each product rounded to nearest even).
-__device__ __forceinline__ uint4 scale_bf16x8_packed(uint4 v, __nv_bfloat162 s2) {
-  __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = __hmul2(p[i], s2);
-  return v;
-}
-
 constexpr int kFuWarps = 20;
 constexpr int kFuThreads = 32 * kFuWarps;
 constexpr int kFuCompute = 16;
@@ -469,7 +460,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
         const int x_h = uu >> 10, j = (uu >> 3) & (S - 1), cc = uu & 7;
         uint4 *ptr = reinterpret_cast<uint4 *>(xb + x_h * S * 128 + sw128_offset(j, 8 * cc));
         const float t = tb[(HP == 2 ? x_h : 0) * S + j];
-        *ptr = FULL ? scale_bf16x8_packed(*ptr, __float2bfloat162_rn(t)) : scale_bf16x8(*ptr, t);
+        *ptr = scale_bf16x8(*ptr, t);
       }
       fence_proxy_async_smem();
       __syncwarp();
