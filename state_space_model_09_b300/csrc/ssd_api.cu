@@ -446,37 +446,48 @@ ssd_status launch_state_pass(const Plan &pl, const CUtensorMap &mB, const CUtens
                           pl.cps, pl.nseg, NP, pl.seg_bh0);
 }
 
-template <typename IO, int KT, int NC = 0, int PSC = 0>
-ssd_status launch_multistep(dim3 grid, int64_t smem, const ssd_dims *d, const void *x,
-                            const float *dt, const float *A, const void *B, const void *C,
-                            const float *D, const float *h_cache, const int32_t *j, void *y,
-                            float *h_j, float *h_K, int PS, cudaStream_t s) {
-  auto k = ssd::multistep_kernel<IO, KT, NC, PSC>;
-  if (!ensure_smem<ssd::multistep_kernel<IO, KT, NC, PSC>>(227 * 1024)) return SSD_ERR_CUDA;
+// One instance of multistep_kernel: KT bounds K (and k_prev in verify mode);
+// the shared memory is sized for those bounds.
+template <typename IO, int KT, int NC = 0, bool KX = false, bool VF = false>
+ssd_status launch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, const float *dtp,
+                     const void *Bp, const int32_t *j, const void *x, const float *dt,
+                     const float *A, const void *B, const void *C, const float *D,
+                     const float *h_cache, void *y, float *h_j, float *h_K, float *h_next,
+                     int PS, cudaStream_t s) {
+  auto k = ssd::multistep_kernel<IO, KT, KT, NC, KX, VF>;
+  const int64_t smem = ssd::ms_smem_bytes(KT, KT, static_cast<int>(d->dstate), PS, VF,
+                                          static_cast<int>(sizeof(IO)));
+  if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
+  if (!ensure_smem<ssd::multistep_kernel<IO, KT, KT, NC, KX, VF>>(227 * 1024)) return SSD_ERR_CUDA;
   k<<<grid, ssd::kMsThreads, static_cast<size_t>(smem), s>>>(
       static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
-      static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus, nullptr,
-      nullptr, nullptr, nullptr, 0);
-  return launch_status();
-}
-
-template <typename IO, int KT, int NC = 0, int PSC = 0>
-ssd_status launch_verify(dim3 grid, int64_t smem, const ssd_dims *d, int KP, const void *xp,
-                         const float *dtp, const void *Bp, const int32_t *jp, const void *x,
-                         const float *dt, const float *A, const void *B, const void *C,
-                         const float *D, const float *h_cache, void *y, float *h_next, int PS,
-                         cudaStream_t s) {
-  auto k = ssd::multistep_kernel<IO, KT, NC, PSC, true>;
-  if (!ensure_smem<ssd::multistep_kernel<IO, KT, NC, PSC, true>>(227 * 1024)) return SSD_ERR_CUDA;
-  k<<<grid, ssd::kMsThreads, static_cast<size_t>(smem), s>>>(
-      static_cast<const IO *>(x), dt, A, static_cast<const IO *>(B), static_cast<const IO *>(C),
-      D, h_cache, jp, static_cast<IO *>(y), nullptr, nullptr, static_cast<int>(d->seqlen),
-      static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
       static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus,
       static_cast<const IO *>(xp), dtp, static_cast<const IO *>(Bp), h_next, KP);
   return launch_status();
+}
+
+// The instance for a shape: the decode shape of the Mamba-2 layers (bf16,
+// N = 128, K = 8, k_prev <= 8) with N and K fixed at compile time, else a
+// generic one.
+template <bool VF>
+ssd_status dispatch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, const float *dtp,
+                       const void *Bp, const int32_t *j, const void *x, const float *dt,
+                       const float *A, const void *B, const void *C, const float *D,
+                       const float *h_cache, void *y, float *h_j, float *h_K, float *h_next,
+                       int PS, cudaStream_t s) {
+  const bool bf16 = d->io_dtype == SSD_BF16;
+  const bool small = d->seqlen <= 8 && (!VF || KP <= 8);
+#define SSD_MS_ARGS grid, d, KP, xp, dtp, Bp, j, x, dt, A, B, C, D, h_cache, y, h_j, h_K, h_next, PS, s
+  if (bf16 && small && d->seqlen == 8 && d->dstate == 128)
+    return launch_ms<__nv_bfloat16, 8, 128, true, VF>(SSD_MS_ARGS);
+  if (bf16)
+    return small ? launch_ms<__nv_bfloat16, 8, 0, false, VF>(SSD_MS_ARGS)
+                 : launch_ms<__nv_bfloat16, 16, 0, false, VF>(SSD_MS_ARGS);
+  return small ? launch_ms<float, 8, 0, false, VF>(SSD_MS_ARGS)
+               : launch_ms<float, 16, 0, false, VF>(SSD_MS_ARGS);
+#undef SSD_MS_ARGS
 }
 
 // Heads per CTA of chunk_scan_hl: trades the per-group C B^T product (paid
@@ -1032,23 +1043,13 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
 
   // column slice per block: the largest of 128, 64, 32, 16 that divides P
   const int PS = P % 128 == 0 ? 128 : P % 64 == 0 ? 64 : P % 32 == 0 ? 32 : 16;
-  const int R = ssd::kMsItemThreads / (PS / 4);
-  if (N % R) return SSD_ERR_UNSUPPORTED;
-  const int64_t smem = 2 * (2 * K * N + K * PS + ssd::kMsMaxK + K * 2 * PS) * 4;
-  if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
+  const int R = ssd::kMsThreads / (PS / 4);
+  // raw rows of B move in 16-byte granules
+  if (N % R || (N * (dims->io_dtype == SSD_BF16 ? 2 : 4)) % 16) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(static_cast<unsigned>((H + 1) / 2), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
-  if (bf16 && K <= 8 && N == 128 && PS == 64) {
-    // the decode shape of the Mamba-2 layers: compile-time N and column slice
-    st = launch_multistep<__nv_bfloat16, 8, 128, 64>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
-  } else if (bf16) {
-    st = K <= 8 ? launch_multistep<__nv_bfloat16, 8>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
-                : launch_multistep<__nv_bfloat16, 16>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
-  } else {
-    st = K <= 8 ? launch_multistep<float, 8>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s)
-                : launch_multistep<float, 16>(grid, smem, dims, x, dt, A, B, C, D, h_cache, j, y, h_j, h_K, PS, s);
-  }
-  return st;
+  dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
+  return dispatch_ms<false>(grid, dims, 0, nullptr, nullptr, nullptr, j, x, dt, A, B, C, D, h_cache,
+                            y, h_j, h_K, nullptr, PS, s);
 }
 
 ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
@@ -1089,19 +1090,13 @@ ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
   if (overlaps(y, nx, h_next, nst)) return SSD_ERR_INVALID_ARG;
 
   const int PS = P % 128 == 0 ? 128 : P % 64 == 0 ? 64 : P % 32 == 0 ? 32 : 16;
-  const int R = ssd::kMsItemThreads / (PS / 4);
-  if (N % R) return SSD_ERR_UNSUPPORTED;
-  const int64_t smem = 2 * static_cast<int64_t>(ssd::ms_item_floats(static_cast<int>(K), static_cast<int>(N), PS, true, static_cast<int>(KP))) * 4;
-  if (smem > 227 * 1024) return SSD_ERR_UNSUPPORTED;
+  const int R = ssd::kMsThreads / (PS / 4);
+  // raw rows of B move in 16-byte granules
+  if (N % R || (N * (dims->io_dtype == SSD_BF16 ? 2 : 4)) % 16) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(static_cast<unsigned>((H + 1) / 2), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
-  if (bf16 && K <= 8 && N == 128 && PS == 64)
-    return launch_verify<__nv_bfloat16, 8, 128, 64>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
-  if (bf16)
-    return K <= 8 ? launch_verify<__nv_bfloat16, 8>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
-                  : launch_verify<__nv_bfloat16, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
-  return K <= 8 ? launch_verify<float, 8>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s)
-                : launch_verify<float, 16>(grid, smem, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt, A, B, C, D, h_cache, y, h_next, PS, s);
+  dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
+  return dispatch_ms<true>(grid, dims, static_cast<int>(KP), x_prev, dt_prev, B_prev, j_prev, x, dt,
+                           A, B, C, D, h_cache, y, nullptr, nullptr, h_next, PS, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -1200,7 +1195,7 @@ ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
   const size_t BH = static_cast<size_t>(cp.b * cp.H), NP = static_cast<size_t>(cp.N * cp.P);
   struct Buf { const void *p; size_t n; };
   const Buf ins[] = {{decays, nranks * BH * 4}, {finals, nranks * BH * NP * 4},
-                     {dt, static_cast<size_t>(cp.b * cp.T * cp.H) * 4}, {A, cp.H * 4},
+                     {dt, static_cast<size_t>(cp.b * cp.T * cp.H) * 4}, {A, static_cast<size_t>(cp.H) * 4},
                      {C, static_cast<size_t>(cp.b * cp.T * cp.GC * cp.N) * io}};
   const Buf outs[] = {{y, static_cast<size_t>(cp.b * cp.T * cp.H * cp.P) * io},
                       {h_final, BH * NP * 4}, {workspace, cp.total}};

@@ -4,8 +4,11 @@
 //   chunk_state_simt / chunk_scan_simt
 //                         float32-accurate chunk kernels (the fp32 I/O path and
 //                         shapes outside the tensor-core kernels' envelope)
-//   multistep_kernel      K-token verification decode from a cached state
+//   multistep_kernel      K-token verification decode from a cached state, and
+//                         the fused recompute + verify + cache step
 #pragma once
+
+#include <type_traits>
 
 #include "ssd_device.cuh"
 
@@ -297,189 +300,407 @@ __global__ void __launch_bounds__(256) chunk_scan_simt(
 }
 
 // ----------------------------------------------------------------------------
-// K-token multi-step decode ("Mamba in the Llama", 推测解码, MultiStep).
-// A block of 128 threads serves two items (heads 2 blockIdx.x and +1 of batch
-// row b, p-slice of PS columns); 64 threads per item.  Thread (r, q) of an item
-// handles the 4 columns 4q..4q+3 of state rows r, r + R, r + 2R, ...
-// (R = 64 / (PS/4) row groups) and streams them: a row's 4 values are
-// advanced through the K tokens (h = a h + B x^T; written to h_j after j
-// tokens and to h_K after K) and add C_k[n] h to the thread's y partials,
-// which stay in registers; loads run four rows ahead.  y = sum over rows
-// (warp shuffles + shared memory) + D x.  The state is never held whole
-// (42 MB of state would not fit the register file), so the whole grid is
-// resident at once.
-// dynamic smem per item: B[K][N], C[K][N], x[K][PS], a[16], y partials [K][2][PS].
+// K-token multi-step decode ("Mamba in the Llama", 推测解码, MultiStep) and the
+// fused verifier step (same page, 硬件特定优化).
+// One warp serves one item (head blockIdx.x of batch row b, p-slice of PS
+// columns).  Lane (r, q) owns the 4 columns 4q..4q+3 of state rows r, r + R,
+// r + 2R, ... (R = 32 / (PS/4) row groups).  Its rows stream through a
+// lane-private ring of D float4 slots in shared memory filled by cp.async
+// (D - 1 rows in flight without holding registers); the small per-call
+// operands (B, C, x of the new tokens; B, x of the previous drafts) arrive
+// the same way, raw, as one group ahead of them.
+//
+// The recurrence h_k = a_k h_{k-1} + B_k x_k^T is not stepped token by token:
+// over a run of tokens lo..hi-1 it collapses to
+//     h_hi = (prod_{lo<=m<hi} a_m) h_lo + sum_k (prod_{k<m<hi} a_m) B_k x_k^T,
+// one scale and one rank-1 term per token, with the decay products folded
+// into per-row coefficients W[n][k] = w_k B_k[n] once per item.  The outputs
+// split the same way,
+//     y_k = e_k C_k^T h_0 + sum_{m<=k} G[k][m] x_m + D x_k,
+//     e_k = prod_{m<=k} a_m,  G[k][m] = (prod_{m<l<=k} a_l) C_k . B_m,
+// so a state row only feeds K dot-product partials (coefficients e_k C_k[n])
+// and the K x K matrix G is formed once per item from B and C.  Per state
+// element that is 1 + (tokens folded) + K multiply-adds; the coefficients
+// are float4 rows of shared memory, the lane's x columns sit in registers.
+// For the decode instance (K fixed) the row loop is compiled once per
+// accepted count, so each fold runs exactly its tokens with no predicates.
+//
+// Both modes fold with one routine (ms_fold) and form y with one routine, so
+// a verifier chain (cache = the state before the previous drafts) and a
+// multistep chain continuing from h_j produce identical bits.
 // ----------------------------------------------------------------------------
-constexpr int kMsThreads = 128;
-// floats of shared memory per item: B, C [K][N], x [K][PS], decays, y partials
-// [K][2][PS]; verify adds the previous drafts' B [KP][N], x [KP][PS], decays.
-__host__ __device__ constexpr int ms_item_floats(int K, int N, int PS, bool verify, int KP = 0) {
-  return 2 * K * N + K * PS + 16 + K * 2 * PS + (verify ? KP * N + KP * PS + 16 : 0);
-}
-constexpr int kMsItemThreads = 64;
+constexpr int kMsThreads = 32;
 constexpr int kMsMaxK = 16;
 
-// KT: compile-time bound on K (8 or 16), K <= KT.  NC / PSC: the state size N
-// and the column slice PS when fixed at compile time (0: taken from the
-// arguments); with both fixed every shared-memory index of the row loop is a
-// constant offset, which removes most of its integer work.
+// ring of the state stream: DEPTH row slots per lane, filled two row steps
+// per cp.async group (at most DEPTH / 2 groups outstanding)
+__host__ __device__ constexpr int ms_depth(bool verify) { return verify ? 12 : 16; }
+
+// dynamic shared memory per item (bytes).  float32: e C [N][KT], W [N][KW],
+// G [KT][KT], decays [2][16], ring [DEPTH][32] float4.  io dtype, raw: B, C of
+// the new tokens [KT][N + 16 B] (rows padded so that reads across tokens fall
+// in distinct banks), x [KT][PS]; verify adds B_prev [KPT][N + 16 B] and
+// x_prev [KPT][PS].
+__host__ __device__ constexpr int ms_smem_bytes(int KT, int KPT, int N, int PS, bool verify,
+                                                int io_bytes) {
+  return 4 * (N * KT + N * (verify ? KPT : KT) + KT * KT + 2 * kMsMaxK) + 16 * 32 * ms_depth(verify) +
+         io_bytes * (2 * KT * (N + 16 / io_bytes) + KT * PS +
+                     (verify ? KPT * (N + 16 / io_bytes) + KPT * PS : 0));
+}
+
+// four consecutive elements as float (8- or 16-byte aligned; global or shared)
+__device__ __forceinline__ float4 ms_ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ms_ld4(const __nv_bfloat16 *p) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  const float2 a = unpack_bf16x2(v.x), c = unpack_bf16x2(v.y);
+  return make_float4(a.x, a.y, c.x, c.y);
+}
+__device__ __forceinline__ void ms_st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void ms_st4(__nv_bfloat16 *p, float4 v) {
+  *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// asynchronous 16-byte copy global -> shared (cp.async, L2 only), and its
+// group bookkeeping; a group completes in the order it was committed
+__device__ __forceinline__ void ms_cp16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ms_zero16(void *dst) {
+  *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void ms_cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int NW>
+__device__ __forceinline__ void ms_cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(NW) : "memory");
+}
+
+// prod_{lo <= l < hi} a[l], ascending; the one formula every decay product of
+// both modes goes through (bit-identical folds)
+__device__ __forceinline__ float ms_prod(const float *a, int lo, int hi) {
+  float p = 1.f;
+  for (int l = lo; l < hi; ++l) p *= a[l];
+  return p;
+}
+
+// the coefficient w of token k when folding tokens lo..hi-1 (0 outside)
+__device__ __forceinline__ float ms_weight(const float *a, int k, int lo, int hi) {
+  return (k >= lo && k < hi) ? ms_prod(a, k + 1, hi) : 0.f;
+}
+
+__device__ __forceinline__ void ms_fma(float4 &s, float w, float4 v) {
+  s.x = fmaf(w, v.x, s.x);
+  s.y = fmaf(w, v.y, s.y);
+  s.z = fmaf(w, v.z, s.z);
+  s.w = fmaf(w, v.w, s.w);
+}
+
+// s = lam st + sum over tokens k in [lo, hi) of wrow[k] xr[k], ascending k.
+// LO >= 0: the range is [LO, HI), fixed at compile time; LO < 0: [lo, hi).
+template <int KW, int LO, int HI>
+__device__ __forceinline__ float4 ms_fold(float lam, float4 st, const float *wrow,
+                                          const float4 (&xr)[KW], int lo, int hi) {
+  float4 s = make_float4(lam * st.x, lam * st.y, lam * st.z, lam * st.w);
+#pragma unroll
+  for (int k4 = 0; k4 < KW; k4 += 4) {
+    if (LO >= 0 && (k4 + 4 <= LO || k4 >= HI)) continue;
+    const float4 w = *reinterpret_cast<const float4 *>(wrow + k4);
+    const float wk[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k4 + u;
+      if (LO >= 0 ? (k >= LO && k < HI) : (k >= lo && k < hi)) ms_fma(s, wk[u], xr[k]);
+    }
+  }
+  return s;
+}
+
+// y partials: yp[k] += e_k C_k[n] st for the new tokens (crow: row n of e C);
+// KX: K == KT
+template <int KT, bool KX>
+__device__ __forceinline__ void ms_ypart(float4 (&yp)[KT], const float *crow, float4 st, int K) {
+#pragma unroll
+  for (int k4 = 0; k4 < KT; k4 += 4) {
+    const float4 c = *reinterpret_cast<const float4 *>(crow + k4);
+    const float ck[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (KX || k4 + u < K) ms_fma(yp[k4 + u], ck[u], st);
+  }
+}
+
+// KT: compile-time bound on K (8 or 16); KPT: on k_prev (verify).  NC: the
+// state size N when fixed at compile time (0: taken from the arguments).  KX:
+// K == KT exactly (the row loop is then specialised on the accepted count).
 //
-// VF (verify): the fused recompute + multistep + cache step ("Mamba in the
-// Llama", 硬件特定优化: the verifier first recomputes the previous steps from
-// the cache, then decodes the new drafts, then caches, in one kernel).  The
-// cache h_cache then holds the state before the previous call's KP drafts
-// (xp, dtp, Bp); jacc[b] of them were accepted.  Each state row is advanced
-// through those jacc[b] tokens, stored to h_next (the next call's cache),
-// and then through the K new drafts for y; h_j and h_K are not written.  Per
-// row that is one state read and one state write instead of one and two.
-template <typename IO, int KT, int NC = 0, int PSC = 0, bool VF = false>
-__global__ void __launch_bounds__(128, 5) multistep_kernel(
+// Multistep (VF false): each state row yields the y partials, h_j (tokens
+// 0..j-1 folded, ordinary stores: a speculative chain continues from it, so
+// the next call finds it in L2) and h_K (tokens j..K-1 folded onto h_j).
+// Verify (VF true): h_cache holds the state before the previous call's KP
+// drafts (xp, dtp, Bp), jacc[b] of which were accepted; a row is folded
+// through those, stored to h_next (the next call's cache) and then feeds the
+// y partials of the K new drafts; h_j and h_K are not written.  Per state
+// row that is one read and one write (multistep: one read, two writes).
+template <typename IO, int KT, int KPT, int NC = 0, bool KX = false, bool VF = false>
+__global__ void __launch_bounds__(kMsThreads, KT <= 8 ? 12 : 8) multistep_kernel(
     const IO *__restrict__ x, const float *__restrict__ dt, const float *__restrict__ A,
     const IO *__restrict__ Bm, const IO *__restrict__ Cm, const float *__restrict__ D,
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
-    float *__restrict__ h_j, float *__restrict__ h_K, int K, int H, int GB, int GC, int N_arg,
-    int P, int PS_arg, int softplus, const IO *__restrict__ xp, const float *__restrict__ dtp,
+    float *__restrict__ h_j, float *__restrict__ h_K, int K_arg, int H, int GB, int GC, int N_arg,
+    int P, int PS, int softplus, const IO *__restrict__ xp, const float *__restrict__ dtp,
     const IO *__restrict__ Bp, float *__restrict__ h_next, int KP) {
+  static_assert(!KX || KT == 8, "the specialised row loop covers accepted counts 0..8");
+  constexpr int KW = VF ? KPT : KT;
+  constexpr int DEPTH = ms_depth(VF);
   const int N = NC ? NC : N_arg;
-  const int PS = PSC ? PSC : PS_arg;
-  extern __shared__ float sm_ms[];
-  const int item = threadIdx.x / kMsItemThreads;  // 0 or 1
-  const int h = 2 * blockIdx.x + item, b = blockIdx.y, p0 = blockIdx.z * PS;
-  const int tid = threadIdx.x % kMsItemThreads, lane = threadIdx.x & 31;
-  const int warp = tid >> 5;  // warp within the item: 0 or 1
-  const int item_floats = ms_item_floats(K, N, PS, VF, KP);
-  float *sB = sm_ms + item * item_floats;
-  float *sC = sB + K * N;
-  float *sx = sC + K * N;
-  float *sa = sx + K * PS;
-  float *red = sa + kMsMaxK;
-  float *sBp = red + K * 2 * PS;  // verify: previous drafts' B, x and decays
-  float *sxp = sBp + KP * N;
-  float *sap = sxp + KP * PS;
-  const bool live = h < H;
-  const int hh = live ? h : H - 1;
-  const int gb = hh / (H / GB), gc = hh / (H / GC);
-  const int TP = PS / 4, R = kMsItemThreads / TP;
-  const int q = tid % TP, r = tid / TP;
+  const int K = KX ? KT : K_arg;
+  extern __shared__ float4 sm_ms4[];
+  const int h = blockIdx.x, b = blockIdx.y, p0 = blockIdx.z * PS;
+  const int lane = threadIdx.x;
+  const int NS = N + 16 / static_cast<int>(sizeof(IO));  // padded raw row
+  float *sCe = reinterpret_cast<float *>(sm_ms4);  // e_k C_k [N][KT]
+  float *sW = sCe + N * KT;                         // fold coefficients [N][KW]
+  float *sG = sW + N * KW;                          // [KT][KT]
+  float *sa = sG + KT * KT;                         // decays of the new tokens
+  float *sap = sa + kMsMaxK;                        // verify: decays of the previous drafts
+  float4 *ring = reinterpret_cast<float4 *>(sap + kMsMaxK);  // [DEPTH][32]
+  IO *sBr = reinterpret_cast<IO *>(ring + DEPTH * kMsThreads);  // raw B [KT][NS]
+  IO *sCr = sBr + KT * NS;                          // raw C [KT][NS]
+  IO *sxr = sCr + KT * NS;                          // raw x [KT][PS]
+  IO *sBpr = sxr + KT * PS;                         // verify: raw B_prev [KPT][NS]
+  IO *sxpr = sBpr + KPT * NS;                       // verify: raw x_prev [KPT][PS]
+  const int gb = h / (H / GB), gc = h / (H / GC);
+  const int TP = PS / 4, R = kMsThreads / TP;
+  const int q = lane % TP, r = lane / TP;
+  const int rows = N / R;
+  const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
 
-  for (int i = tid; i < K * N; i += kMsItemThreads) {
-    const int k = i / N, n = i % N;
-    sB[i] = to_f32(Bm[((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n]);
-    sC[i] = to_f32(Cm[((static_cast<int64_t>(b) * K + k) * GC + gc) * N + n]);
+  // group 1: the per-call operands, raw, in 16-byte granules of GR elements;
+  // rows past K (k_prev) zero
+  constexpr int GR = 16 / static_cast<int>(sizeof(IO));
+  const int NGB = N / GR, PG = PS / GR;
+  for (int i = lane; i < KT * NGB; i += kMsThreads) {
+    const int k = i / NGB, n = (i % NGB) * GR;
+    if (k < K) {
+      const int64_t ob = ((static_cast<int64_t>(b) * K + k) * GB + gb) * N + n;
+      const int64_t oc = ((static_cast<int64_t>(b) * K + k) * GC + gc) * N + n;
+      ms_cp16(sBr + k * NS + n, Bm + ob);
+      ms_cp16(sCr + k * NS + n, Cm + oc);
+    } else {
+      ms_zero16(sBr + k * NS + n);
+      ms_zero16(sCr + k * NS + n);
+    }
   }
-  for (int i = tid; i < K * PS; i += kMsItemThreads) {
-    const int k = i / PS, p = i % PS;
-    sx[i] = to_f32(x[((static_cast<int64_t>(b) * K + k) * H + hh) * P + p0 + p]);
-  }
-  if (tid < K) {
-    const float z = dt[(static_cast<int64_t>(b) * K + tid) * H + hh];
-    sa[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
+  for (int i = lane; i < KT * PG; i += kMsThreads) {
+    const int k = i / PG, p = (i % PG) * GR;
+    const int64_t ox = ((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p;
+    if (k < K) {
+      ms_cp16(sxr + k * PS + p, x + ox);
+    } else {
+      ms_zero16(sxr + k * PS + p);
+    }
   }
   if (VF) {
-    for (int i = tid; i < KP * N; i += kMsItemThreads) {
-      const int k = i / N, n = i % N;
-      sBp[i] = to_f32(Bp[((static_cast<int64_t>(b) * KP + k) * GB + gb) * N + n]);
+    for (int i = lane; i < KPT * NGB; i += kMsThreads) {
+      const int k = i / NGB, n = (i % NGB) * GR;
+      const int64_t ob = ((static_cast<int64_t>(b) * KP + k) * GB + gb) * N + n;
+      if (k < KP) {
+        ms_cp16(sBpr + k * NS + n, Bp + ob);
+      } else {
+        ms_zero16(sBpr + k * NS + n);
+      }
     }
-    for (int i = tid; i < KP * PS; i += kMsItemThreads) {
-      const int k = i / PS, p = i % PS;
-      sxp[i] = to_f32(xp[((static_cast<int64_t>(b) * KP + k) * H + hh) * P + p0 + p]);
-    }
-    if (tid < KP) {
-      const float z = dtp[(static_cast<int64_t>(b) * KP + tid) * H + hh];
-      sap[tid] = expf((softplus ? softplus_f32(z) : z) * A[hh]);
+    for (int i = lane; i < KPT * PG; i += kMsThreads) {
+      const int k = i / PG, p = (i % PG) * GR;
+      const int64_t ox = ((static_cast<int64_t>(b) * KP + k) * H + h) * P + p0 + p;
+      if (k < KP) {
+        ms_cp16(sxpr + k * PS + p, xp + ox);
+      } else {
+        ms_zero16(sxpr + k * PS + p);
+      }
     }
   }
+  ms_cp_commit();
+  // groups 2..DEPTH/2: the first DEPTH - 2 row steps of the state stream, two
+  // per group
+  constexpr int NGR = DEPTH / 2;
+#pragma unroll
+  for (int g = 0; g < NGR - 1; ++g) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = 2 * g + u;
+      if (i < rows) ms_cp16(ring + i * kMsThreads + lane, h_cache + base + static_cast<int64_t>(r + R * i) * P);
+    }
+    ms_cp_commit();
+  }
+
   int jb = jacc[b];
   if (jb < 0 || jb > (VF ? KP : K)) {
-    if (tid == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
+    if (lane == 0 && h == 0 && blockIdx.z == 0) report_error(kDevBadJ);
     jb = -1;
   }
-  __syncthreads();
   // verify: a batch row whose accepted count is out of range gets no outputs
   const bool run = !VF || jb >= 0;
+  const int jf = jb < 0 ? 0 : jb;  // tokens folded into h_j (multistep) / h_next (verify)
+  if (lane < kMsMaxK) {
+    float av = 1.f;
+    if (lane < K) {
+      const float z = dt[(static_cast<int64_t>(b) * K + lane) * H + h];
+      av = expf((softplus ? softplus_f32(z) : z) * A[h]);
+    }
+    sa[lane] = av;
+    if (VF) {
+      av = 1.f;
+      if (lane < KP) {
+        const float z = dtp[(static_cast<int64_t>(b) * KP + lane) * H + h];
+        av = expf((softplus ? softplus_f32(z) : z) * A[h]);
+      }
+      sap[lane] = av;
+    }
+  }
+  ms_cp_wait<NGR - 1>();  // group 1 has landed
+  __syncwarp();
+
+  // per-item coefficients, written as float4 rows: element 4i + u of e C
+  // (or W) is token (4i) % KT + u of state index (4i) / KT; since
+  // 128 % KT == 0 a lane keeps the same four tokens on every step
+  {
+    const int k0 = (4 * lane) % KT;
+    float e[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) e[u] = k0 + u < K ? ms_prod(sa, 0, k0 + u + 1) : 0.f;
+    for (int i = lane; i < N * KT / 4; i += kMsThreads) {
+      const int n = (4 * i) / KT;
+      *reinterpret_cast<float4 *>(sCe + 4 * i) =
+          make_float4(e[0] * to_f32(sCr[k0 * NS + n]), e[1] * to_f32(sCr[(k0 + 1) * NS + n]),
+                      e[2] * to_f32(sCr[(k0 + 2) * NS + n]), e[3] * to_f32(sCr[(k0 + 3) * NS + n]));
+    }
+    const int kw0 = (4 * lane) % KW;
+    float w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int kw = kw0 + u;
+      w[u] = VF ? ms_weight(sap, kw, 0, jf)
+                : (kw < jf ? ms_weight(sa, kw, 0, jf) : ms_weight(sa, kw, jf, K));
+    }
+    // raw B times w (verify: of the previous drafts); the product commutes,
+    // so both modes give a token's coefficient the same bits
+    const IO *braw = VF ? sBpr : sBr;
+    for (int i = lane; i < N * KW / 4; i += kMsThreads) {
+      const int n = (4 * i) / KW;
+      *reinterpret_cast<float4 *>(sW + 4 * i) =
+          make_float4(w[0] * to_f32(braw[kw0 * NS + n]), w[1] * to_f32(braw[(kw0 + 1) * NS + n]),
+                      w[2] * to_f32(braw[(kw0 + 2) * NS + n]), w[3] * to_f32(braw[(kw0 + 3) * NS + n]));
+    }
+    for (int t = lane; t < KT * KT; t += kMsThreads) {
+      const int kk = t / KT, m = t % KT;
+      float g = 0.f;
+      if (m <= kk && kk < K) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int n = 0; n < N; n += 4) {
+          const float4 c = ms_ld4(sCr + kk * NS + n), bb = ms_ld4(sBr + m * NS + n);
+          acc.x = fmaf(c.x, bb.x, acc.x);
+          acc.y = fmaf(c.y, bb.y, acc.y);
+          acc.z = fmaf(c.z, bb.z, acc.z);
+          acc.w = fmaf(c.w, bb.w, acc.w);
+        }
+        g = ((acc.x + acc.y) + (acc.z + acc.w)) * ms_prod(sa, m + 1, kk + 1);
+      }
+      sG[t] = g;
+    }
+  }
+  __syncwarp();
+
+  const float lam_j = ms_prod(VF ? sap : sa, 0, jf);  // decay of the folded tokens
+  const float lam_K = VF ? 1.f : ms_prod(sa, jf, K);  // multistep: tokens j..K-1
+  float4 xr[KW];  // the lane's columns of the folded tokens' x
+#pragma unroll
+  for (int k = 0; k < KW; ++k) xr[k] = ms_ld4((VF ? sxpr : sxr) + k * PS + 4 * q);
 
   float4 yp[KT];
 #pragma unroll
   for (int k = 0; k < KT; ++k) yp[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  if (live && run) {
-    const int64_t base = (static_cast<int64_t>(b) * H + h) * N * P + p0 + 4 * q;
-    const int rows = N / R;
-    constexpr int PF = 4;  // rows in flight
-    float4 buf[PF];
+  // the row loop; JF >= 0: compiled for jf == JF (and K == KT)
+  const auto row_loop = [&](auto jf_tag) {
+    constexpr int JF = decltype(jf_tag)::value;
+    constexpr int LO0 = JF >= 0 ? 0 : -1;       // the fold into h_j / h_next
+    constexpr int LO1 = JF >= 0 ? JF : -1;      // multistep: the fold onto h_K
+    for (int i2 = 0; i2 < rows; i2 += 2) {
+      ms_cp_wait<NGR - 2>();  // row steps i2, i2 + 1 have landed (this lane's own copies)
 #pragma unroll
-    for (int u = 0; u < PF; ++u)
-      if (u < rows) buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(r + R * u) * P));
-    for (int i0 = 0; i0 < rows; i0 += PF) {
-#pragma unroll
-      for (int u = 0; u < PF; ++u) {
-        const int i = i0 + u;
+      for (int u = 0; u < 2; ++u) {
+        const int i = i2 + u;
         if (i < rows) {
+          const float4 st = ring[(i % DEPTH) * kMsThreads + lane];
           const int n = r + R * i;
-          float4 st = buf[u];
-          if (i + PF < rows)
-            buf[u] = __ldcs(reinterpret_cast<const float4 *>(h_cache + base + static_cast<int64_t>(n + R * PF) * P));
           const int64_t off = base + static_cast<int64_t>(n) * P;
+          const float *wrow = sW + n * KW;
+          const float *crow = sCe + n * KT;
           if (VF) {
-            // recompute the accepted previous drafts, then cache the result
-#pragma unroll
-            for (int k = 0; k < kMsMaxK; ++k) {
-              if (k < jb) {
-                const float bn = sBp[k * N + n], a = sap[k];
-                const float4 xk = *reinterpret_cast<const float4 *>(sxp + k * PS + 4 * q);
-                st.x = fmaf(a, st.x, bn * xk.x);
-                st.y = fmaf(a, st.y, bn * xk.y);
-                st.z = fmaf(a, st.z, bn * xk.z);
-                st.w = fmaf(a, st.w, bn * xk.w);
-              }
-            }
-            *reinterpret_cast<float4 *>(h_next + off) = st;
+            const float4 s = ms_fold<KW, LO0, JF>(lam_j, st, wrow, xr, 0, jf);
+            *reinterpret_cast<float4 *>(h_next + off) = s;
+            ms_ypart<KT, KX>(yp, crow, s, K);
+          } else {
+            ms_ypart<KT, KX>(yp, crow, st, K);
+            const float4 sj = ms_fold<KW, LO0, JF>(lam_j, st, wrow, xr, 0, jf);
+            if (jb >= 0) *reinterpret_cast<float4 *>(h_j + off) = sj;
+            __stcs(reinterpret_cast<float4 *>(h_K + off), ms_fold<KW, LO1, KT>(lam_K, sj, wrow, xr, jf, K));
           }
-          // h_j with ordinary (L2-resident) stores: a speculative decode step
-          // usually continues from it, so the next call finds it in L2
-          if (!VF && jb == 0) *reinterpret_cast<float4 *>(h_j + off) = st;
-#pragma unroll
-          for (int k = 0; k < KT; ++k) {
-            if (k < K) {
-              const float bn = sB[k * N + n], cn = sC[k * N + n], a = sa[k];
-              const float4 xk = *reinterpret_cast<const float4 *>(sx + k * PS + 4 * q);
-              st.x = fmaf(a, st.x, bn * xk.x);
-              st.y = fmaf(a, st.y, bn * xk.y);
-              st.z = fmaf(a, st.z, bn * xk.z);
-              st.w = fmaf(a, st.w, bn * xk.w);
-              yp[k].x = fmaf(cn, st.x, yp[k].x);
-              yp[k].y = fmaf(cn, st.y, yp[k].y);
-              yp[k].z = fmaf(cn, st.z, yp[k].z);
-              yp[k].w = fmaf(cn, st.w, yp[k].w);
-              if (!VF && k + 1 == jb) *reinterpret_cast<float4 *>(h_j + off) = st;
-            }
-          }
-          if (!VF) __stcs(reinterpret_cast<float4 *>(h_K + off), st);
         }
       }
+      // refill the two slots read one step ago (their values are long consumed)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int nx = i2 + DEPTH - 2 + u;
+        if (nx < rows) ms_cp16(ring + (nx % DEPTH) * kMsThreads + lane, h_cache + base + static_cast<int64_t>(r + R * nx) * P);
+      }
+      ms_cp_commit();
+    }
+  };
+  if (run) {
+    if constexpr (KX) {
+      switch (jf) {
+        case 0: row_loop(std::integral_constant<int, 0>{}); break;
+        case 1: row_loop(std::integral_constant<int, 1>{}); break;
+        case 2: row_loop(std::integral_constant<int, 2>{}); break;
+        case 3: row_loop(std::integral_constant<int, 3>{}); break;
+        case 4: row_loop(std::integral_constant<int, 4>{}); break;
+        case 5: row_loop(std::integral_constant<int, 5>{}); break;
+        case 6: row_loop(std::integral_constant<int, 6>{}); break;
+        case 7: row_loop(std::integral_constant<int, 7>{}); break;
+        default: row_loop(std::integral_constant<int, 8>{}); break;
+      }
+    } else {
+      row_loop(std::integral_constant<int, -1>{});
     }
   }
-  // reduce the y partials over row groups: lanes q, q + TP, ... of a warp, then 2 warps
+  ms_cp_wait<0>();  // no copy may outlive the block (a skipped row loop leaves some)
+  if (!run) return;
+  // sum the partials over the row groups (lanes q, q + TP, ...); lane (r, q)
+  // then writes tokens k = r, r + R, ... of its four columns
+  const float Dh = D ? D[h] : 0.f;
 #pragma unroll
   for (int k = 0; k < KT; ++k) {
     if (k < K) {
       float4 v = yp[k];
-      for (int off = TP; off < 32; off <<= 1) {
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
-        v.z += __shfl_xor_sync(0xffffffffu, v.z, off);
-        v.w += __shfl_xor_sync(0xffffffffu, v.w, off);
+      for (int o = TP; o < kMsThreads; o <<= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+        v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
       }
-      if (lane < TP) *reinterpret_cast<float4 *>(red + (k * 2 + warp) * PS + 4 * lane) = v;
+      if (k % R == r) {
+        // sum_{m<=k} G[k][m] x_m: the part of y_k that does not see the state
+        float4 loc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m <= k; ++m) ms_fma(loc, sG[k * KT + m], ms_ld4(sxr + m * PS + 4 * q));
+        const float4 xk = ms_ld4(sxr + k * PS + 4 * q);
+        ms_st4(y + ((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + 4 * q,
+               make_float4(v.x + loc.x + Dh * xk.x, v.y + loc.y + Dh * xk.y,
+                           v.z + loc.z + Dh * xk.z, v.w + loc.w + Dh * xk.w));
+      }
     }
-  }
-  __syncthreads();
-  if (!live || !run) return;
-  const float Dh = D ? D[h] : 0.f;
-  for (int i = tid; i < K * PS; i += kMsItemThreads) {
-    const int k = i / PS, p = i % PS;
-    const float acc = red[(k * 2) * PS + p] + red[(k * 2 + 1) * PS + p];
-    y[((static_cast<int64_t>(b) * K + k) * H + h) * P + p0 + p] = from_f32<IO>(acc + Dh * sx[i]);
   }
 }
 
