@@ -591,22 +591,66 @@ __global__ void __launch_bounds__(kMsThreads, KT <= 8 ? 12 : 8) multistep_kernel
           make_float4(w[0] * to_f32(braw[kw0 * NS + n]), w[1] * to_f32(braw[(kw0 + 1) * NS + n]),
                       w[2] * to_f32(braw[(kw0 + 2) * NS + n]), w[3] * to_f32(braw[(kw0 + 3) * NS + n]));
     }
-    for (int t = lane; t < KT * KT; t += kMsThreads) {
-      const int kk = t / KT, m = t % KT;
-      float g = 0.f;
-      if (m <= kk && kk < K) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int n = 0; n < N; n += 4) {
-          const float4 c = ms_ld4(sCr + kk * NS + n), bb = ms_ld4(sBr + m * NS + n);
-          acc.x = fmaf(c.x, bb.x, acc.x);
-          acc.y = fmaf(c.y, bb.y, acc.y);
-          acc.z = fmaf(c.z, bb.z, acc.z);
-          acc.w = fmaf(c.w, bb.w, acc.w);
+    if constexpr (KT == 8) {
+      // lane-split: the lane's partial C_k . B_m over its granules of four
+      // state indices for all 64 (k, m), then a transposing butterfly: at
+      // each level a lane keeps half of its values plus its partner's copy
+      // of that half, so lane l ends with entries 2l and 2l + 1, summed
+      // over the warp
+      float pv[64];
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pv[e] = 0.f;
+      for (int n = 4 * lane; n < N; n += 4 * kMsThreads) {
+        float4 bv[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) bv[m] = ms_ld4(sBr + m * NS + n);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const float4 cv = ms_ld4(sCr + kk * NS + n);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            float &a = pv[kk * 8 + m];
+            a = fmaf(cv.x, bv[m].x, a);
+            a = fmaf(cv.y, bv[m].y, a);
+            a = fmaf(cv.z, bv[m].z, a);
+            a = fmaf(cv.w, bv[m].w, a);
+          }
         }
-        g = ((acc.x + acc.y) + (acc.z + acc.w)) * ms_prod(sa, m + 1, kk + 1);
       }
-      sG[t] = g;
+#pragma unroll
+      for (int lv = 0; lv < 5; ++lv) {
+        const int o = 16 >> lv, half = 32 >> lv;
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int e = 0; e < half; ++e) {
+          const float lo_v = pv[e], hi_v = pv[e + half];
+          const float recv = __shfl_xor_sync(0xffffffffu, hi ? lo_v : hi_v, o);
+          pv[e] = (hi ? hi_v : lo_v) + recv;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = 2 * lane + u, kk = t / 8, m = t % 8;
+        sG[t] = (m <= kk && kk < K) ? pv[u] * ms_prod(sa, m + 1, kk + 1) : 0.f;
+      }
+    } else {
+      for (int t = lane; t < KT * KT; t += kMsThreads) {
+        const int kk = t / KT, m = t % KT;
+        float g = 0.f;
+        if (m <= kk && kk < K) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int n = 0; n < N; n += 4) {
+            const float4 c = ms_ld4(sCr + kk * NS + n), bb = ms_ld4(sBr + m * NS + n);
+            acc.x = fmaf(c.x, bb.x, acc.x);
+            acc.y = fmaf(c.y, bb.y, acc.y);
+            acc.z = fmaf(c.z, bb.z, acc.z);
+            acc.w = fmaf(c.w, bb.w, acc.w);
+          }
+          g = ((acc.x + acc.y) + (acc.z + acc.w)) * ms_prod(sa, m + 1, kk + 1);
+        }
+        sG[t] = g;
+      }
     }
   }
   __syncwarp();
@@ -626,36 +670,46 @@ __global__ void __launch_bounds__(kMsThreads, KT <= 8 ? 12 : 8) multistep_kernel
     constexpr int JF = decltype(jf_tag)::value;
     constexpr int LO0 = JF >= 0 ? 0 : -1;       // the fold into h_j / h_next
     constexpr int LO1 = JF >= 0 ? JF : -1;      // multistep: the fold onto h_K
+    const int64_t rstep = static_cast<int64_t>(R) * P;  // one row step in the state
+    const float4 *rd = ring + lane;                                // slot of row step i2
+    float4 *wr = ring + (DEPTH - 2) * kMsThreads + lane;           // slot of row step i2 + DEPTH - 2
+    const float *src = h_cache + base + (DEPTH - 2) * rstep + static_cast<int64_t>(r) * P;
+    float *out_a = (VF ? h_next : h_j) + base + static_cast<int64_t>(r) * P;
+    float *out_b = h_K + base + static_cast<int64_t>(r) * P;     // multistep only
+    const float *wrow = sW + r * KW, *crow = sCe + r * KT;
     for (int i2 = 0; i2 < rows; i2 += 2) {
       ms_cp_wait<NGR - 2>();  // row steps i2, i2 + 1 have landed (this lane's own copies)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int i = i2 + u;
-        if (i < rows) {
-          const float4 st = ring[(i % DEPTH) * kMsThreads + lane];
-          const int n = r + R * i;
-          const int64_t off = base + static_cast<int64_t>(n) * P;
-          const float *wrow = sW + n * KW;
-          const float *crow = sCe + n * KT;
+        if (i2 + u < rows) {
+          const float4 st = rd[u * kMsThreads];
+          const float *wr_u = wrow + u * R * KW, *cr_u = crow + u * R * KT;
           if (VF) {
-            const float4 s = ms_fold<KW, LO0, JF>(lam_j, st, wrow, xr, 0, jf);
-            *reinterpret_cast<float4 *>(h_next + off) = s;
-            ms_ypart<KT, KX>(yp, crow, s, K);
+            const float4 s = ms_fold<KW, LO0, JF>(lam_j, st, wr_u, xr, 0, jf);
+            *reinterpret_cast<float4 *>(out_a + u * rstep) = s;
+            ms_ypart<KT, KX>(yp, cr_u, s, K);
           } else {
-            ms_ypart<KT, KX>(yp, crow, st, K);
-            const float4 sj = ms_fold<KW, LO0, JF>(lam_j, st, wrow, xr, 0, jf);
-            if (jb >= 0) *reinterpret_cast<float4 *>(h_j + off) = sj;
-            __stcs(reinterpret_cast<float4 *>(h_K + off), ms_fold<KW, LO1, KT>(lam_K, sj, wrow, xr, jf, K));
+            ms_ypart<KT, KX>(yp, cr_u, st, K);
+            const float4 sj = ms_fold<KW, LO0, JF>(lam_j, st, wr_u, xr, 0, jf);
+            if (jb >= 0) *reinterpret_cast<float4 *>(out_a + u * rstep) = sj;
+            __stcs(reinterpret_cast<float4 *>(out_b + u * rstep), ms_fold<KW, LO1, KT>(lam_K, sj, wr_u, xr, jf, K));
           }
         }
       }
       // refill the two slots read one step ago (their values are long consumed)
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int nx = i2 + DEPTH - 2 + u;
-        if (nx < rows) ms_cp16(ring + (nx % DEPTH) * kMsThreads + lane, h_cache + base + static_cast<int64_t>(r + R * nx) * P);
-      }
+      for (int u = 0; u < 2; ++u)
+        if (i2 + DEPTH - 2 + u < rows) ms_cp16(wr + u * kMsThreads, src + u * rstep);
       ms_cp_commit();
+      rd += 2 * kMsThreads;
+      if (rd == ring + DEPTH * kMsThreads + lane) rd = ring + lane;
+      wr += 2 * kMsThreads;
+      if (wr == ring + DEPTH * kMsThreads + lane) wr = ring + lane;
+      src += 2 * rstep;
+      out_a += 2 * rstep;
+      out_b += 2 * rstep;
+      wrow += 2 * R * KW;
+      crow += 2 * R * KT;
     }
   };
   if (run) {
