@@ -47,16 +47,22 @@ L2_BYTES = 126 * 1024 * 1024
 # DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) of
 # the dominant kernels, with the sha1 of the kernel's source at capture time;
 # the summaries are in profiles/.  A changed source reports null.
+FUSED_SRCS = ("state_space_model_09_b300/csrc/ssd_fused_hb.cuh",
+              "state_space_model_09_b300/csrc/ssd_scan.cuh",
+              "state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
+              "state_space_model_09_b300/csrc/ssd_tc.cuh",
+              "state_space_model_09_b300/csrc/ssd_device.cuh")
+MS_SRCS = ("state_space_model_09_b300/csrc/ssd_kernels.cuh",
+           "state_space_model_09_b300/csrc/ssd_device.cuh")
 MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_fused_hb", "mamba2_2p7b"):
-        (349_817_088, ("state_space_model_09_b300/csrc/ssd_fused_hb.cuh",
-                       "state_space_model_09_b300/csrc/ssd_scan.cuh",
-                       "state_space_model_09_b300/csrc/ssd_scan_hb.cuh",
-                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
-                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "32b3b9ec303f21d9e4d6a3e8753647c193e7b56c"),
+        (346_560_512, FUSED_SRCS,
+         "d2a0ba6387b973cb9fd08b502e16f468ce712412"),
+    ("chunk_fused_hb", "hybrid_llama3_8b"):
+        (406_920_832, FUSED_SRCS,
+         "d2a0ba6387b973cb9fd08b502e16f468ce712412"),
     ("chunk_scan_hl", "hybrid_llama3_8b"):
         (552_532_224, ("state_space_model_09_b300/csrc/ssd_scan.cuh",
                        "state_space_model_09_b300/csrc/ssd_tc.cuh",
@@ -68,8 +74,11 @@ MEASURED_TRAFFIC = {
                        "state_space_model_09_b300/csrc/ssd_device.cuh"),
          "35cf10d8ea7510bc28882c75765d47427529ac49"),
     ("multistep_kernel", "multistep_k8"):
-        (70_129_920, ("state_space_model_09_b300/csrc/ssd_kernels.cuh",),
-         "f1267a2133217f991f16eac81edf77c2e16126eb"),
+        (71_768_832, MS_SRCS,
+         "b99058203500c94bdbee37385ef005c3797dc64a"),
+    ("multistep_kernel_verify", "multistep_k8"):
+        (48_279_552, MS_SRCS,
+         "b99058203500c94bdbee37385ef005c3797dc64a"),
 }
 
 
@@ -986,7 +995,9 @@ def multistep_summary(args, world, rank, local):
                                      "state was written three calls (~385 MB) earlier")
     torch.cuda.empty_cache()
     mv = measure_multistep(args, world, rank, dev, verify=True, min_s=args.min_seconds, e2e=False)
-    out["verify"] = dict(multistep_fields(mv, world, pk, None), call="ssd_verify")
+    out["verify"] = dict(multistep_fields(mv, world, pk,
+                                          measured_traffic("multistep_kernel_verify", "multistep_k8")),
+                         call="ssd_verify")
     out["verify"]["roofline"]["kernel"] = "multistep_kernel (verify mode)"
     if not args.no_cpu_baseline:
         value, _, cores, sample = oracle_multistep_chain(12, 6.0)
@@ -1006,8 +1017,8 @@ def run_multistep(args, world, rank, local):
     if rank != 0:
         return
     pk = peaks()
-    f = multistep_fields(m, world, pk, None if (args.verify or args.chains > 1)
-                         else measured_traffic("multistep_kernel", "multistep_k8"))
+    f = multistep_fields(m, world, pk, None if args.chains > 1 else measured_traffic(
+        "multistep_kernel_verify" if args.verify else "multistep_kernel", "multistep_k8"))
     metric = ("SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
               "1000-step speculative chain)" if args.verify else MULTISTEP_METRIC)
     line = {"metric": metric, "value": f.pop("value"), "unit": UNIT, "n_gpus": world,
