@@ -255,10 +255,15 @@ ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
  * this library, which every GPU that loads the library holds until the
  * process exits.  Shapes whose ssd_fwd_workspace_size() exceeds that return
  * SSD_ERR_UNSUPPORTED before anything is launched.  The call allocates and
- * frees nothing.
+ * frees nothing itself, but the array's 64 MiB are claimed on a device when
+ * the library's device code is loaded there -- under CUDA's lazy module
+ * loading, at the first libssd call on that device, which may be this one;
+ * if the device is full by then, that call returns SSD_ERR_CUDA.  Make one
+ * warm-up call per device at start-up, before a memory plan or a caching
+ * allocator takes the rest of the device.
  *   - The first call on a device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture.
+ *     array's device address once and keeps it for the life of the process,
+ *     so a device reset (cudaDeviceReset) is unsupported after that call.
  *   - All calls on a device share the one array and it keeps the previous
  *     call's contents; nothing in it needs to start at zero (every byte the
  *     kernels read is written earlier in the same call).  Calls that overlap
