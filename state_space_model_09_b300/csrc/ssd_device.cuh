@@ -63,6 +63,44 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+// 256-bit global accesses of eight floats (32-byte aligned): a thread that
+// owns a 128-byte row moves it in four instructions, one full sector each
+// (ld_row32 / st_row32 fall back to 16-byte accesses for a row that is only
+// 16-byte aligned)
+__device__ __forceinline__ void ld_global_v8f(const float *p, float *v) {
+  asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_global_v8f(float *p, const float *v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void ld_row32(const float *p, float *v) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) ld_global_v8f(p + e, v + e);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 t = *reinterpret_cast<const float4 *>(p + e);
+      v[e] = t.x; v[e + 1] = t.y; v[e + 2] = t.z; v[e + 3] = t.w;
+    }
+  }
+}
+__device__ __forceinline__ void st_row32(float *p, const float *v) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) st_global_v8f(p + e, v + e);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4)
+      *reinterpret_cast<float4 *>(p + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+  }
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

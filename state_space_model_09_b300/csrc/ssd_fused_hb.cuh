@@ -415,25 +415,18 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     float st[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) st[e] = 0.f;
+    // (a thread's 32 columns of a state row are one 128-byte line)
     if (seg == 0 && h0 && valid) {
-      const float *src = h0 + ((static_cast<int64_t>(b) * H + h) * N + n) * P + p0;
-#pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src + e);
-        st[e] = v.x; st[e + 1] = v.y; st[e + 2] = v.z; st[e + 3] = v.w;
-      }
+      ld_row32(h0 + ((static_cast<int64_t>(b) * H + h) * N + n) * P + p0, st);
     } else if (FULL && split && seg > 0 && valid) {
       // the true entering state from the prepass: T = Lambda T + F over s' < seg
       grid_dep_wait();
       for (int s2 = 0; s2 < seg; ++s2) {
         const float Ls = Lseg[rel * nseg + s2];
-        const float *F = Fseg + (rel * nseg + s2) * N * P + static_cast<int64_t>(n) * P + p0;
+        float v[32];
+        ld_row32(Fseg + (rel * nseg + s2) * N * P + static_cast<int64_t>(n) * P + p0, v);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(F + e);
-          st[e] = fmaf(Ls, st[e], v.x); st[e + 1] = fmaf(Ls, st[e + 1], v.y);
-          st[e + 2] = fmaf(Ls, st[e + 2], v.z); st[e + 3] = fmaf(Ls, st[e + 3], v.w);
-        }
+        for (int e = 0; e < 32; ++e) st[e] = fmaf(Ls, st[e], v[e]);
       }
     }
     // a wait for the whole warp: every lane waits on the same phase, so they
@@ -636,11 +629,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       if (!FULL) fin = Fseg + (rel * nseg + seg) * N * P + static_cast<int64_t>(n) * P + p0;
       else if (h_final && (!split || seg == nseg - 1))
         fin = h_final + ((static_cast<int64_t>(b) * H + h) * N + n) * P + p0;
-      if (fin) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4 *>(fin + e) = make_float4(st[e], st[e + 1], st[e + 2], st[e + 3]);
-      }
+      if (fin) st_row32(fin, st);
     }
   }
   tc_fence_before_sync();
