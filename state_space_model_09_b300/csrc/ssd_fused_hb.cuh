@@ -63,6 +63,11 @@
 namespace ssd {
 
 constexpr int kFuWarps = 20;
+constexpr int kFuComputeThreads = 32 * 16;
+// a barrier among the sixteen compute warps only (threads 0..511)
+__device__ __forceinline__ void compute_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFuComputeThreads) : "memory");
+}
 constexpr int kFuThreads = 32 * kFuWarps;
 constexpr int kFuCompute = 16;
 constexpr int kFuControl = 16;
@@ -415,11 +420,104 @@ __global__ void __launch_bounds__(kFuThreads, 1)
     float st[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) st[e] = 0.f;
-    // (a thread's 32 columns of a state row are one 128-byte line)
-    if (seg == 0 && h0 && valid) {
-      ld_row32(h0 + ((static_cast<int64_t>(b) * H + h) * N + n) * P + p0, st);
+    // The item's state moves between global memory and the threads' rows
+    // through the H~ buffer (idle before the first stage and after the
+    // last): one 64-column half of the item's 128 columns (a head of a pair,
+    // or half of a wide head) at a time, fully coalesced on the global side,
+    // 16-byte chunks XOR-swizzled by row on the shared side; round r serves
+    // the warps whose columns lie in that half (hs / 2 == r).
+    float *stage_f = reinterpret_cast<float *>(Ht);  // [128 rows][64 floats]
+    auto half_base = [&](float *base, int r) {       // the half's [128][64] block
+      return HP == 2 ? base + ((static_cast<int64_t>(b) * H + hb0 + r) * N) * P
+                     : base + (static_cast<int64_t>(b) * H + hb0) * N * P + 64 * r;
+    };
+    const int nhalves = HP == 2 ? nh : 2;
+    // both halves' global loads are issued first (one memory latency): the
+    // first half lands in ta, the second in st[16..31], whose owners fill st
+    // last; the first half's owners park their row's second 16 floats in ta
+    auto load_state_staged = [&](const float *base) {
+      float ta[16];
+      auto gload = [&](int r, float *dst) {
+        const float *src = half_base(const_cast<float *>(base), r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int f = i * 32 * kFuCompute + tid, row = f >> 4, c = f & 15;
+          const float4 v = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(row) * P + 4 * c);
+          dst[4 * i] = v.x; dst[4 * i + 1] = v.y; dst[4 * i + 2] = v.z; dst[4 * i + 3] = v.w;
+        }
+      };
+      auto sstore = [&](const float *src) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int f = i * 32 * kFuCompute + tid, row = f >> 4, c = f & 15;
+          *reinterpret_cast<float4 *>(stage_f + row * 64 + 4 * (c ^ (row & 7))) =
+              make_float4(src[4 * i], src[4 * i + 1], src[4 * i + 2], src[4 * i + 3]);
+        }
+      };
+      // own row, 16-byte chunks j0 .. j0 + 3 of the thread's eight, into dst
+      auto sread = [&](int j0, float *dst) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 8 * (hs & 1) + j0 + j;
+          const float4 v = *reinterpret_cast<const float4 *>(stage_f + n * 64 + 4 * (c ^ (n & 7)));
+          dst[4 * j] = v.x; dst[4 * j + 1] = v.y; dst[4 * j + 2] = v.z; dst[4 * j + 3] = v.w;
+        }
+      };
+      gload(0, ta);
+      if (nhalves > 1) gload(1, st + 16);
+      sstore(ta);
+      compute_bar_sync();
+      if ((hs >> 1) == 0) {
+        sread(0, st);
+        sread(4, ta);
+      }
+      compute_bar_sync();
+      if (nhalves > 1) {
+        sstore(st + 16);
+        compute_bar_sync();
+        if ((hs >> 1) == 1) {
+          sread(0, st);
+          sread(4, st + 16);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) st[16 + e] = ta[e];
+        }
+        compute_bar_sync();  // every row read before the first H~ is written
+      } else if ((hs >> 1) == 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) st[16 + e] = ta[e];
+      }
+    };
+    // half(r): the global [128][64] block of round r (row stride P)
+    auto store_state_staged = [&](auto half, bool write) {
+#pragma unroll 1
+      for (int r = 0; r < nhalves; ++r) {
+        float *dst = half(r);
+        compute_bar_sync();  // the buffer is free
+        if ((hs >> 1) == r) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = 8 * (hs & 1) + j;
+            *reinterpret_cast<float4 *>(stage_f + n * 64 + 4 * (c ^ (n & 7))) =
+                make_float4(st[4 * j], st[4 * j + 1], st[4 * j + 2], st[4 * j + 3]);
+          }
+        }
+        compute_bar_sync();
+        if (write) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int f = i * 32 * kFuCompute + tid, row = f >> 4, c = f & 15;
+            *reinterpret_cast<float4 *>(dst + static_cast<int64_t>(row) * P + 4 * c) =
+                *reinterpret_cast<const float4 *>(stage_f + row * 64 + 4 * (c ^ (row & 7)));
+          }
+        }
+      }
+    };
+    if (seg == 0 && h0) {
+      load_state_staged(h0);
     } else if (FULL && split && seg > 0 && valid) {
       // the true entering state from the prepass: T = Lambda T + F over s' < seg
+      // (a thread's 32 columns of a state row, one 128-byte line, at a time)
       grid_dep_wait();
       for (int s2 = 0; s2 < seg; ++s2) {
         const float Ls = Lseg[rel * nseg + s2];
@@ -623,13 +721,18 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       }
     }
     // the final state: the sequence's (whole items, last segments) or, in the
-    // prepass, the segment's from its own start
-    if (ok && valid) {
-      float *fin = nullptr;
-      if (!FULL) fin = Fseg + (rel * nseg + seg) * N * P + static_cast<int64_t>(n) * P + p0;
-      else if (h_final && (!split || seg == nseg - 1))
-        fin = h_final + ((static_cast<int64_t>(b) * H + h) * N + n) * P + p0;
-      if (fin) st_row32(fin, st);
+    // prepass, the segment's from its own start (the H~ buffer is free once
+    // the last C H~ product is done)
+    if (FULL && nstages > 0) ok = ok && wait_all(&bars[kFuHfree], (nstages - 1) & 1);
+    if (!FULL) {  // segment states: [(row - bh0) nseg + seg][N][P]
+      store_state_staged(
+          [&](int r) {
+            const int64_t row = static_cast<int64_t>(b) * H + hb0 + (HP == 2 ? r : 0) - bh0;
+            return Fseg + (row * nseg + seg) * N * P + (HP == 2 ? 0 : 64 * r);
+          },
+          ok);
+    } else if (h_final && (!split || seg == nseg - 1)) {
+      store_state_staged([&](int r) { return half_base(h_final, r); }, ok);
     }
   }
   tc_fence_before_sync();
