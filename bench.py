@@ -58,27 +58,17 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_fused_hb", "mamba2_2p7b"):
-        (346_560_512, FUSED_SRCS,
-         "d2a0ba6387b973cb9fd08b502e16f468ce712412"),
+        (346_760_960, FUSED_SRCS,
+         "1f87a04b5f475f5e15b6311efe1af2bcbe4e899e"),
     ("chunk_fused_hb", "hybrid_llama3_8b"):
-        (406_920_832, FUSED_SRCS,
-         "d2a0ba6387b973cb9fd08b502e16f468ce712412"),
-    ("chunk_scan_hl", "hybrid_llama3_8b"):
-        (552_532_224, ("state_space_model_09_b300/csrc/ssd_scan.cuh",
-                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
-                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "611043699da0318b501de1671ce8377c1a5da7a6"),
-    ("chunk_state_pass_tc", "hybrid_llama3_8b"):
-        (267_524_352, ("state_space_model_09_b300/csrc/ssd_state.cuh",
-                       "state_space_model_09_b300/csrc/ssd_tc.cuh",
-                       "state_space_model_09_b300/csrc/ssd_device.cuh"),
-         "35cf10d8ea7510bc28882c75765d47427529ac49"),
+        (406_927_232, FUSED_SRCS,
+         "1f87a04b5f475f5e15b6311efe1af2bcbe4e899e"),
     ("multistep_kernel", "multistep_k8"):
-        (71_768_832, MS_SRCS,
-         "b99058203500c94bdbee37385ef005c3797dc64a"),
+        (68_567_808, MS_SRCS,
+         "2247f085a6f25de83d9e138dde25a79199608cd8"),
     ("multistep_kernel_verify", "multistep_k8"):
-        (48_279_552, MS_SRCS,
-         "b99058203500c94bdbee37385ef005c3797dc64a"),
+        (46_689_792, MS_SRCS,
+         "2247f085a6f25de83d9e138dde25a79199608cd8"),
 }
 
 
