@@ -867,15 +867,18 @@ def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0,
     del g
     if e2e:
         out["e2e"] = e2e_multistep(S, inp, A, D, h0, dims, stream, world, dev, verify,
-                                   max(3, min(args.steps, 200)))
+                                   100)
     return out
 
 
 def e2e_multistep(S, inp, A, D, h0, dims, stream, world, dev, verify, ke):
-    """End to end through the public API: each call's drafts (x, dt, B, C) and
-    accepted count j copied in from pinned host memory (one stream, a call
-    ahead), y read back (another stream); the recurrent state stays resident
-    on the device, as a decoder's cache does."""
+    """End to end through the public API, as a decoder's serving loop runs it:
+    each call's drafts (x, dt, B, C) and accepted count j are copied in from
+    pinned host memory on one stream, the call runs on another and its y is
+    read back to pinned host memory on a third; the recurrent state stays
+    resident on the device, as a decoder's cache does.  The ke calls with all
+    their copies are captured once in a CUDA graph (as a decoder captures its
+    step) and the graph is replayed; ms per call = replay time / ke."""
     import torch
     bf = torch.bfloat16
     hx = {k: torch.from_numpy(inp[k][:ke]).pin_memory() for k in ("dt", "j")}
@@ -890,55 +893,72 @@ def e2e_multistep(S, inp, A, D, h0, dims, stream, world, dev, verify, ke):
     hK = torch.empty_like(h0)
     J0 = torch.zeros(h0.shape[0], dtype=torch.int32, device=dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    fork = torch.cuda.Event()
     ev_in = [torch.cuda.Event() for _ in range(ns)]
     ev_used = [torch.cuda.Event() for _ in range(ns)]
     ev_y = [torch.cuda.Event() for _ in range(2)]
     ev_ydone = [torch.cuda.Event() for _ in range(2)]
 
-    def call(i, cur, nxt):
-        k, kp = i % ns, (i - 1) % ns
-        dx, dp = dxs[k], dxs[kp]
-        s_in.wait_event(ev_used[k])  # calls i - 3 and i - 2 are done with this slot
-        with torch.cuda.stream(s_in):
-            for name in ("x", "dt", "B", "C", "j"):
-                dx[name].copy_(hx[name][i], non_blocking=True)
-            ev_in[k].record(s_in)
-        stream.wait_event(ev_in[k])
-        stream.wait_event(ev_ydone[i % 2])
-        yy = ys[i % 2]
-        if verify:
-            S.ssd_verify(dp["x"], dp["dt"], dp["B"], dp["j"] if i > 0 else J0, dx["x"],
-                         dx["dt"], A, dx["B"], dx["C"], D, cur, yy, nxt, stream=stream)
-        else:
-            S.ssd_multistep(dx["x"], dx["dt"], A, dx["B"], dx["C"], D, cur, dx["j"], yy,
-                            nxt, hK, stream=stream, dims=dims)
-        ev_used[k].record(stream)
-        ev_used[kp].record(stream)  # a verify call read the previous call's slot too
-        ev_y[i % 2].record(stream)
-        s_out.wait_event(ev_y[i % 2])
-        with torch.cuda.stream(s_out):
-            hys[i % 2].copy_(yy, non_blocking=True)
-            ev_ydone[i % 2].record(s_out)
+    def chain():
+        # every wait is on an event recorded earlier in the same chain (or
+        # on the fork), so the chain can be captured
+        fork.record(stream)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        cur = h0
+        for i in range(ke):
+            k, kp = i % ns, (i - 1) % ns
+            dx, dp = dxs[k], dxs[kp]
+            if i >= ns:
+                s_in.wait_event(ev_used[k])  # calls i - 3 and i - 2 are done with this slot
+            with torch.cuda.stream(s_in):
+                for name in ("x", "dt", "B", "C", "j"):
+                    dx[name].copy_(hx[name][i], non_blocking=True)
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            if i >= 2:
+                stream.wait_event(ev_ydone[i % 2])  # y buffer read back
+            yy, nxt = ys[i % 2], bufs[i % 2]
+            if verify:
+                S.ssd_verify(dp["x"], dp["dt"], dp["B"], dp["j"] if i > 0 else J0, dx["x"],
+                             dx["dt"], A, dx["B"], dx["C"], D, cur, yy, nxt, stream=stream)
+            else:
+                S.ssd_multistep(dx["x"], dx["dt"], A, dx["B"], dx["C"], D, cur, dx["j"], yy,
+                                nxt, hK, stream=stream, dims=dims)
+            ev_used[k].record(stream)
+            ev_used[kp].record(stream)  # a verify call read the previous call's slot too
+            ev_y[i % 2].record(stream)
+            s_out.wait_event(ev_y[i % 2])
+            with torch.cuda.stream(s_out):
+                hys[i % 2].copy_(yy, non_blocking=True)
+                ev_ydone[i % 2].record(s_out)
+            cur = nxt
+        for k2 in range(2):
+            stream.wait_event(ev_ydone[k2])
 
-    for i in range(3):
-        call(i, h0, bufs[i % 2])
+    with torch.cuda.stream(stream):
+        chain()  # eager once: the library and the copies are warm
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        chain()
+    with torch.cuda.stream(stream):
+        g.replay()
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    s_in.wait_event(f0)
-    cur = h0
-    for i in range(ke):
-        call(i, cur, bufs[i % 2])
-        cur = bufs[i % 2]
-    for k in range(2):
-        stream.wait_event(ev_ydone[k])
-    f1.record(stream)
+    reps = 5
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        f1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / ke, world, dev)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / (reps * ke), world, dev)
     h2d = sum(v[0].numel() * v[0].element_size() for v in hx.values())
     d2h = hys[0].numel() * hys[0].element_size()
+    del g
     return {"ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
