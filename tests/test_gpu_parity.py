@@ -224,6 +224,34 @@ def test_fwd_fused_last_wave_split_into_segments(monkeypatch):
     check_fwd(shape, 29, pairs=pairs)
 
 
+def test_fwd_fused_16_byte_aligned_state_buffers(monkeypatch):
+    """The one-pass kernel moves a state row in 32-byte accesses where the row
+    is 32-byte aligned and in 16-byte ones otherwise: h0, h_final and a
+    workspace (holding the segments' states) that are only 16-byte aligned
+    give the same bits as 256-byte aligned ones."""
+    set_form(monkeypatch, "fused")
+    shape = F(4, 1024, 80, 64, 128, 1, 1, 256, synth.BF16, "all")  # a split last wave
+    d = to_dev(synth.make_fwd_inputs(shape, 45), shape.io)
+    y1, h1 = run_fwd(d, 256)
+    b, T, H, P = d["x"].shape
+    N = d["B"].shape[3]
+    dims = S.dims_of(d["x"], d["B"], d["C"])
+    nws = S.ssd_fwd_workspace_size(dims, 256)
+    ws_big = torch.full((nws + 64,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws = ws_big[16:16 + nws]
+    h0_big = torch.empty(d["h0"].numel() + 4, device="cuda")
+    h0 = h0_big[4:].view_as(d["h0"])
+    h0.copy_(d["h0"])
+    hf_big = torch.full((h1.numel() + 4,), float("nan"), device="cuda")
+    hf = hf_big[4:].view_as(h1)
+    assert h0.data_ptr() % 32 == 16 and hf.data_ptr() % 32 == 16 and ws.data_ptr() % 32 == 16
+    y2 = torch.full_like(y1, float("nan"))
+    S.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], h0, 256, y2, hf, ws)
+    S.ssd_check_device_error()
+    assert torch.equal(y1, y2)
+    assert torch.equal(h1, hf)
+
+
 @pytest.mark.parametrize("shape,seed", [
     (F(1, 3000, 3, 64, 128, 1, 1, 256, synth.BF16, "all"), 30),   # 12 one-chunk segments
     (F(3, 1000, 37, 64, 128, 1, 1, 256, synth.BF16, "half"), 31),  # odd H, 2 segments
