@@ -605,9 +605,11 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       }
       return true;
     };
-    // P of stage g -> masked bf16 pairs (j <= i) in tensor memory
+    // P of stage g -> masked bf16 pairs (j <= i) in tensor memory.  The full
+    // pass waits for S instead: its commit follows P's MMAs (same thread, in
+    // order), so one wait covers mask and fold
     auto mask = [&](int g) -> bool {
-      if (!wait_all(&bars[kFuPready], g & 1)) return false;
+      if (!wait_all(&bars[FULL ? kFuSready : kFuPready], g & 1)) return false;
       // (row quarter q, column block hs): below the diagonal block (q > hs)
       // nothing is masked, on it (q == hs) columns j <= i are kept, and above
       // it (q < hs) the block stays zero from the start
@@ -630,9 +632,9 @@ __global__ void __launch_bounds__(kFuThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kFuMready]);
       return true;
     };
-    // state <- dec state + sfac S (stage g's S)
+    // state <- dec state + sfac S (stage g's S; the full pass has waited in mask)
     auto fold = [&](int g) -> bool {
-      if (!wait_all(&bars[kFuSready], g & 1)) return false;
+      if (!FULL && !wait_all(&bars[kFuSready], g & 1)) return false;
       tc_fence_after_sync();
       float sv[32];
       tmem_ld32(tmem + lane_base + L::kS + 32 * hs, sv);
