@@ -793,6 +793,114 @@ def run_sequential(args, shape, world, rank, local):
         "clocks": clk}), flush=True)
 
 
+def run_cp(args, shape, world, rank, local):
+    """Context parallelism's per-rank compute on one GPU (--cp R): the
+    sequence cut into R contiguous segments on the chunk grid; each rank's
+    phase 1 (ssd_fwd of its segment, rank 0 from h0, then
+    ssd_cp_segment_decay) and phase 2 (ssd_cp_correct once every rank's decay
+    and final state are gathered) are timed as CUDA-graph replays.  The
+    gather itself is done here by device copies and not timed: with one GPU
+    per call the exchange between GPUs is not measured.  The critical path of
+    R concurrent ranks is max(phase 1) + exchange + max(phase 2)."""
+    import torch
+    from state_space_model_09_b300 import ssd as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    R = args.cp
+    inp = synth.make_fwd_inputs(shape, synth.WORKLOAD_SEEDS[args.workload])
+    io_t = torch.bfloat16 if shape.io == synth.BF16 else torch.float32
+    T, Q = shape.seqlen, shape.chunk
+    per = -(-T // R)
+    per = -(-per // Q) * Q
+    cuts = [min(T, r * per) for r in range(R + 1)]
+    if any(cuts[r + 1] <= cuts[r] for r in range(R)):
+        raise SystemExit("--cp %d leaves an empty segment of %d tokens" % (R, T))
+    A = torch.from_numpy(inp["A"]).to(dev)
+    D = None if inp["D"] is None else torch.from_numpy(inp["D"]).to(dev)
+    h0 = None if inp["h0"] is None else torch.from_numpy(inp["h0"]).to(dev)
+    b, H, P, N = shape.batch, shape.nheads, shape.headdim, shape.dstate
+    stream = torch.cuda.Stream(dev)
+    ranks = []
+    for r in range(R):
+        sl = slice(cuts[r], cuts[r + 1])
+        seg = {k: torch.from_numpy(np.ascontiguousarray(inp[k][:, sl])) for k in ("x", "dt", "B", "C")}
+        for k in ("x", "B", "C"):
+            seg[k] = seg[k].to(io_t)
+        seg = {k: v.to(dev) for k, v in seg.items()}
+        dims = S.dims_of(seg["x"], seg["B"], seg["C"])
+        ranks.append(dict(seg=seg, dims=dims, ws=S.workspace_for(dims, Q),
+                          cws=torch.empty(S.ssd_cp_workspace_size(dims), dtype=torch.uint8,
+                                          device=dev),
+                          y=torch.empty_like(seg["x"]),
+                          hl=torch.empty((b, H, N, P), dtype=torch.float32, device=dev),
+                          hf=torch.empty((b, H, N, P), dtype=torch.float32, device=dev),
+                          decay=torch.empty((b, H), dtype=torch.float32, device=dev)))
+    decays = torch.empty((R, b, H), dtype=torch.float32, device=dev)
+    finals = torch.empty((R, b, H, N, P), dtype=torch.float32, device=dev)
+
+    def phase1(r):
+        k = ranks[r]
+        g = k["seg"]
+        S.ssd_fwd(g["x"], g["dt"], A, g["B"], g["C"], D, h0 if r == 0 else None, Q, k["y"],
+                  k["hl"], k["ws"], True, stream, k["dims"])
+        S.ssd_cp_segment_decay(g["dt"], A, k["decay"], k["cws"], k["dims"], stream=stream)
+
+    def gather():
+        with torch.cuda.stream(stream):
+            for r in range(R):
+                decays[r].copy_(ranks[r]["decay"])
+                finals[r].copy_(ranks[r]["hl"])
+
+    def phase2(r):
+        k = ranks[r]
+        g = k["seg"]
+        S.ssd_cp_correct(R, r, decays, finals, g["dt"], A, g["C"], k["y"], k["hf"], k["cws"],
+                         k["dims"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            phase1(r)
+        gather()
+        for r in range(R):
+            phase2(r)
+    torch.cuda.synchronize()
+    S.ssd_check_device_error(stream)
+    reps = 10
+
+    def timed(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+            ms, _ = timed_replays(g.replay, reps, stream, max(0.2, args.min_seconds / 4))
+        torch.cuda.synchronize()
+        return ms
+
+    clocks = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.3)
+    p1 = [timed(lambda r=r: phase1(r)) for r in range(R)]
+    p2 = [timed(lambda r=r: phase2(r)) for r in range(R)]
+    clk = clocks.stop()
+    crit = max(p1) + max(p2)
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": "SSD context-parallel prefill, per-rank compute on one GPU "
+                  "(Mtok·heads/s if the R ranks ran concurrently, exchange excluded)",
+        "value": round(shape.tok_heads / (crit * 1e-3) / 1e6, 2), "unit": UNIT, "n_gpus": 1,
+        "ranks_emulated": R, "higher_is_better": True, "vs_baseline": None,
+        "dtype": "bf16" if shape.io == synth.BF16 else "f32", "data": "synthetic (seeded PCG64)",
+        "config": dict(config_of(args.workload, shape, 1), segments=cuts),
+        "phase1_ms": [round(v, 5) for v in p1], "phase2_ms": [round(v, 5) for v in p2],
+        "critical_path_ms": round(crit, 5),
+        "exchange": "not measured: one GPU per call (per rank: decay [b,H] and final state "
+                    "[b,H,N,P] float32, %d bytes)" % (4 * b * H * (1 + N * P)),
+        "clocks": clk}), flush=True)
+
+
 def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0, e2e=True):
     """The speculative chain: each call continues from the previous call's h_j
     (ssd_multistep) or from the next cache it stored (ssd_verify).  The
@@ -1065,6 +1173,9 @@ def main():
                     help="multistep_k8: independent chains interleaved (3+ keeps states cold)")
     ap.add_argument("--window", type=int, default=0,
                     help="prefill through ssd_fwd_sequential with windows of this many tokens")
+    ap.add_argument("--cp", type=int, default=0,
+                    help="prefill: context parallelism's per-rank compute for this many "
+                         "ranks, emulated one after another on one GPU")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1087,6 +1198,9 @@ def main():
     world, rank, local = dist_setup()
     if args.window > 0:
         run_sequential(args, shape, world, rank, local)
+        return
+    if args.cp > 0:
+        run_cp(args, shape, world, rank, local)
         return
     run_ours(args, shape, world, rank, local)
 
