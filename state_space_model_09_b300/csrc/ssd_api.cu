@@ -1102,13 +1102,16 @@ ssd_status ssd_verify(const ssd_dims *dims, int32_t k_prev, const void *x_prev,
 // ---------------------------------------------------------------------------
 // Context parallelism: per-segment decay, and the correction of a segment's
 // outputs and final state once the states of the segments before it are known.
-// Workspace: the running log2 decays a [b, H, T] and H_in [b, H, N, P], float32.
+// Workspace: the running log2 decays a [b, H, T] (within 128-token tiles) and the
+// tiles' totals [b, H, ceil(T / 128)], H_in [b, H, N, P] float32,
+// then H_in rounded to bf16 in the tensor-core operand image (b H tiles of N P
+// bf16).
 // ---------------------------------------------------------------------------
 namespace {
 
 struct CpPlan {
-  int64_t b, T, H, P, N, GC;
-  size_t a_bytes, hin_off, total;
+  int64_t b, T, H, P, N, GC, ntiles;
+  size_t pre_off, decay_bytes, hin_off, op_off, total;
 };
 
 ssd_status make_cp_plan(const ssd_dims *d, CpPlan *cp) {
@@ -1121,33 +1124,71 @@ ssd_status make_cp_plan(const ssd_dims *d, CpPlan *cp) {
   cp->N = d->dstate;
   cp->GC = d->ngroups_c;
   if (cp->b * cp->H > (int64_t(1) << 31) - 1 || cp->b > 65535) return SSD_ERR_UNSUPPORTED;
-  cp->a_bytes = align_up(static_cast<size_t>(cp->b * cp->H * cp->T) * 4);
-  cp->hin_off = cp->a_bytes;
-  cp->total = cp->hin_off + align_up(static_cast<size_t>(cp->b * cp->H * cp->N * cp->P) * 4);
+  cp->ntiles = (cp->T + ssd::kCpTile - 1) / ssd::kCpTile;
+  cp->pre_off = align_up(static_cast<size_t>(cp->b * cp->H * cp->T) * 4);
+  cp->decay_bytes = cp->pre_off + align_up(static_cast<size_t>(cp->b * cp->H * cp->ntiles) * 4);
+  cp->hin_off = cp->decay_bytes;
+  cp->op_off = cp->hin_off + align_up(static_cast<size_t>(cp->b * cp->H * cp->N * cp->P) * 4);
+  cp->total = cp->op_off + align_up(static_cast<size_t>(cp->b * cp->H * cp->N * cp->P) * 2);
   return SSD_OK;
 }
 
-// a[b, h, t] = running log2 decay from the segment's start (inclusive); the
-// segment's total decay 2^(a[b, h, T - 1]) into decay[b H] when given.
+// a[b, h, t] = running log2 decay from the start of t's 128-token tile
+// (inclusive) and pre[b, h, k] = the decay over the tiles before tile k (the
+// running decay from the segment's start is their sum); the segment's total
+// decay into decay[b H] when given.
 ssd_status cp_running_decay(const CpPlan &cp, const float *dt, const float *A, int softplus,
-                            float *a, float *decay, cudaStream_t s) {
-  dim3 g((cp.T + 31) / 32, static_cast<unsigned>((cp.H + 31) / 32), static_cast<unsigned>(cp.b));
-  if (g.x > 2147483647ll) return SSD_ERR_UNSUPPORTED;
-  ssd::dt_decay_kernel<<<g, 256, 0, s>>>(dt, A, a, cp.T, static_cast<int>(cp.H), softplus);
+                            float *a, float *pre, float *decay, cudaStream_t s) {
+  dim3 g(static_cast<unsigned>(cp.ntiles), static_cast<unsigned>((cp.H + 31) / 32),
+         static_cast<unsigned>(cp.b));
+  if (cp.ntiles > 2147483647ll || g.y > 65535) return SSD_ERR_UNSUPPORTED;
+  ssd::cp_tile_decay_kernel<<<g, 256, 0, s>>>(dt, A, a, pre, cp.T, static_cast<int>(cp.H),
+                                              static_cast<int>(cp.ntiles), softplus);
   ssd_status st = launch_status();
   if (st != SSD_OK) return st;
-  ssd::row_cumsum_kernel<<<static_cast<unsigned>(cp.b * cp.H), 256, 0, s>>>(a, cp.T, decay);
+  const int64_t rows = cp.b * cp.H;
+  ssd::cp_tile_prefix_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
+      pre, static_cast<int>(cp.ntiles), rows, decay);
   return launch_status();
 }
 
-// Heads per CTA of cp_correct_tc: a divisor of the heads per C group, the
-// largest that still gives two CTAs per SM.
-int cp_heads_per_cta(const CpPlan &cp) {
+// Heads per work unit of cp_correct_tc: a divisor of the heads per C group,
+// the largest that still gives each persistent CTA eight units or more (each
+// unit loads one C tile; more units even out the CTAs' shares).
+int cp_heads_per_unit(const CpPlan &cp) {
   const int64_t per_group = cp.H / cp.GC, tiles = (cp.T + 127) / 128;
   for (int64_t hpc = per_group; hpc > 1; --hpc)
-    if (per_group % hpc == 0 && tiles * cp.b * (cp.H / hpc) >= 2 * num_sms())
+    if (per_group % hpc == 0 && tiles * cp.b * (cp.H / hpc) >= 8 * num_sms())
       return static_cast<int>(hpc);
   return 1;
+}
+
+ssd_status launch_cp_correct_tc(const CpPlan &cp, const void *C, void *y, const uint8_t *hin_op,
+                                const float *a, const float *pre, cudaStream_t s) {
+  const int P = static_cast<int>(cp.P);
+  CUtensorMap mC, mYl, mYs;
+  if (!encode_btgw(&mC, C, cp.b, cp.T, cp.GC, cp.N, 128) ||
+      !encode_btgw(&mYl, y, cp.b, cp.T, cp.H, P, 128) ||
+      !encode_btgw(&mYs, y, cp.b, cp.T, cp.H, P, 32))
+    return SSD_ERR_CUDA;
+  const int hpc = cp_heads_per_unit(cp);
+  const int64_t units = cp.ntiles * cp.b * (cp.H / hpc);
+  if (cp.T > 2147483647ll - 128) return SSD_ERR_UNSUPPORTED;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(units, num_sms()));
+  const int nt = static_cast<int>(cp.ntiles), H = static_cast<int>(cp.H),
+            GC = static_cast<int>(cp.GC);
+  if (P == 64) {
+    using L = ssd::CpTc<64>;
+    if (!ensure_smem<ssd::cp_correct_tc<64>>(L::kBytes)) return SSD_ERR_CUDA;
+    ssd::cp_correct_tc<64><<<grid, L::kThreads, L::kBytes, s>>>(mC, mYl, mYs, hin_op, a, pre, nt,
+                                                                cp.T, H, GC, hpc, units);
+  } else {
+    using L = ssd::CpTc<128>;
+    if (!ensure_smem<ssd::cp_correct_tc<128>>(L::kBytes)) return SSD_ERR_CUDA;
+    ssd::cp_correct_tc<128><<<grid, L::kThreads, L::kBytes, s>>>(mC, mYl, mYs, hin_op, a, pre, nt,
+                                                                 cp.T, H, GC, hpc, units);
+  }
+  return launch_status();
 }
 
 }  // namespace
@@ -1167,14 +1208,16 @@ ssd_status ssd_cp_segment_decay(const ssd_dims *dims, const float *dt, const flo
   const void *ptrs[] = {dt, A, decay, workspace};
   for (const void *p : ptrs)
     if (!aligned16(p)) return SSD_ERR_INVALID_ARG;
-  if (workspace_bytes < cp.a_bytes) return SSD_ERR_INVALID_ARG;
+  if (workspace_bytes < cp.decay_bytes) return SSD_ERR_INVALID_ARG;
   const size_t ndt = static_cast<size_t>(cp.b * cp.T * cp.H) * 4, nh = cp.H * 4,
                nd = static_cast<size_t>(cp.b * cp.H) * 4;
   if (overlaps(decay, nd, dt, ndt) || overlaps(decay, nd, A, nh) ||
-      overlaps(decay, nd, workspace, cp.a_bytes) || overlaps(workspace, cp.a_bytes, dt, ndt) ||
-      overlaps(workspace, cp.a_bytes, A, nh))
+      overlaps(decay, nd, workspace, cp.decay_bytes) ||
+      overlaps(workspace, cp.decay_bytes, dt, ndt) || overlaps(workspace, cp.decay_bytes, A, nh))
     return SSD_ERR_INVALID_ARG;
-  return cp_running_decay(cp, dt, A, dims->dt_softplus, static_cast<float *>(workspace), decay,
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  return cp_running_decay(cp, dt, A, dims->dt_softplus, reinterpret_cast<float *>(ws),
+                          reinterpret_cast<float *>(ws + cp.pre_off), decay,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -1210,37 +1253,25 @@ ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *a = reinterpret_cast<float *>(ws);
+  float *pre = reinterpret_cast<float *>(ws + cp.pre_off);
   float *hin = reinterpret_cast<float *>(ws + cp.hin_off);
+  uint8_t *hin_op = ws + cp.op_off;
+  const bool tc = dims->io_dtype == SSD_BF16 && cp.N == kTcN && (cp.P == 64 || cp.P == 128);
   const int64_t n4 = static_cast<int64_t>(BH * NP / 4);
   const unsigned blocks = static_cast<unsigned>((n4 + 255) / 256);
-  // H_in of this rank and its true final state (rank 0: its own final state)
-  ssd::cp_combine_kernel<<<blocks, 256, 0, s>>>(decays, finals, rank,
-                                                static_cast<int64_t>(BH), static_cast<int>(NP),
-                                                rank > 0 ? hin : nullptr, h_final);
+  // H_in of this rank (float32 for the CUDA-core update, the bf16 operand
+  // image for the tensor-core one) and its true final state (rank 0: its own
+  // final state)
+  ssd::cp_combine_kernel<<<blocks, 256, 0, s>>>(
+      decays, finals, rank, static_cast<int64_t>(BH), static_cast<int>(NP),
+      static_cast<int>(cp.P), rank > 0 && !tc ? hin : nullptr, rank > 0 && tc ? hin_op : nullptr,
+      h_final);
   if ((st = launch_status()) != SSD_OK) return st;
   if (rank == 0) return SSD_OK;  // the first segment started from the true h0
-  if ((st = cp_running_decay(cp, dt, A, dims->dt_softplus, a, nullptr, s)) != SSD_OK) return st;
-  const bool tc = dims->io_dtype == SSD_BF16 && cp.N == kTcN && (cp.P == 64 || cp.P == 128);
-  if (tc) {
-    CUtensorMap mC;
-    if (!encode_btgw(&mC, C, cp.b, cp.T, cp.GC, cp.N, 128)) return SSD_ERR_CUDA;
-    const int hpc = cp_heads_per_cta(cp);
-    dim3 grid(static_cast<unsigned>((cp.T + 127) / 128), static_cast<unsigned>((cp.H + hpc - 1) / hpc),
-              static_cast<unsigned>(cp.b));
-    if (cp.T > 2147483647ll - 128 || grid.y > 65535) return SSD_ERR_UNSUPPORTED;
-    if (cp.P == 64) {
-      if (!ensure_smem<ssd::cp_correct_tc<64>>(ssd::CpTc<64>::kBytes)) return SSD_ERR_CUDA;
-      ssd::cp_correct_tc<64><<<grid, 128, ssd::CpTc<64>::kBytes, s>>>(
-          mC, hin, a, static_cast<__nv_bfloat16 *>(y), cp.T, static_cast<int>(cp.H),
-          static_cast<int>(cp.GC), hpc);
-    } else {
-      if (!ensure_smem<ssd::cp_correct_tc<128>>(ssd::CpTc<128>::kBytes)) return SSD_ERR_CUDA;
-      ssd::cp_correct_tc<128><<<grid, 128, ssd::CpTc<128>::kBytes, s>>>(
-          mC, hin, a, static_cast<__nv_bfloat16 *>(y), cp.T, static_cast<int>(cp.H),
-          static_cast<int>(cp.GC), hpc);
-    }
-    return launch_status();
-  }
+  if ((st = cp_running_decay(cp, dt, A, dims->dt_softplus, a, pre, nullptr, s)) != SSD_OK)
+    return st;
+  if (tc)
+    return launch_cp_correct_tc(cp, C, y, hin_op, a, pre, s);
   const int PS = cp.P % 64 == 0 ? 64 : cp.P % 32 == 0 ? 32 : 16;
   const int smem = static_cast<int>((32 * cp.N + cp.N * PS) * 4);
   dim3 grid(static_cast<unsigned>((cp.T + 31) / 32), static_cast<unsigned>(cp.P / PS),
@@ -1250,13 +1281,15 @@ ssd_status ssd_cp_correct(const ssd_dims *dims, int32_t nranks, int32_t rank,
     if (!ensure_smem<ssd::cp_correct_simt<__nv_bfloat16>>((32 * 256 + 256 * 64) * 4))
       return SSD_ERR_CUDA;
     ssd::cp_correct_simt<__nv_bfloat16><<<grid, 256, smem, s>>>(
-        static_cast<const __nv_bfloat16 *>(C), hin, a, static_cast<__nv_bfloat16 *>(y), cp.T,
+        static_cast<const __nv_bfloat16 *>(C), hin, a, pre, static_cast<int>(cp.ntiles),
+        static_cast<__nv_bfloat16 *>(y), cp.T,
         static_cast<int>(cp.H), static_cast<int>(cp.GC), static_cast<int>(cp.N),
         static_cast<int>(cp.P), PS);
   } else {
     if (!ensure_smem<ssd::cp_correct_simt<float>>((32 * 256 + 256 * 64) * 4)) return SSD_ERR_CUDA;
     ssd::cp_correct_simt<float><<<grid, 256, smem, s>>>(
-        static_cast<const float *>(C), hin, a, static_cast<float *>(y), cp.T,
+        static_cast<const float *>(C), hin, a, pre, static_cast<int>(cp.ntiles),
+        static_cast<float *>(y), cp.T,
         static_cast<int>(cp.H), static_cast<int>(cp.GC), static_cast<int>(cp.N),
         static_cast<int>(cp.P), PS);
   }

@@ -357,20 +357,23 @@ __global__ void __launch_bounds__(256) dt_decay_kernel(const float *__restrict__
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   constexpr float kLog2e = 1.4426950408889634f;
   grid_dep_trigger();  // the chunk-state kernel may start loading x and B
+  const int h = h0 + tx;
+  float z[4];
 #pragma unroll
-  for (int r = ty; r < 32; r += 8) {
-    const int64_t t = t0 + r;
-    const int h = h0 + tx;
-    float v = 0.f;
-    if (t < T && h < H) {
-      const float z = dt[(static_cast<int64_t>(b) * T + t) * H + h];
-      v = (softplus ? softplus_f32(z) : z) * A[h] * kLog2e;
-    }
-    tile[r][tx] = v;
+  for (int k = 0; k < 4; ++k) {  // every load first, so that the four are in flight at once
+    const int64_t t = t0 + ty + 8 * k;
+    z[k] = t < T && h < H ? dt[(static_cast<int64_t>(b) * T + t) * H + h] : 0.f;
+  }
+  const float Ah = h < H ? A[h] : 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = ty + 8 * k;
+    tile[r][tx] = t0 + r < T && h < H ? (softplus ? softplus_f32(z[k]) : z[k]) * Ah * kLog2e : 0.f;
   }
   __syncthreads();
 #pragma unroll
-  for (int r = ty; r < 32; r += 8) {
+  for (int k = 0; k < 4; ++k) {
+    const int r = ty + 8 * k;
     const int h = h0 + r;
     const int64_t t = t0 + tx;
     if (h < H && t < T) u[(static_cast<int64_t>(b) * H + h) * T + t] = tile[tx][r];

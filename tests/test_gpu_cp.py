@@ -114,6 +114,14 @@ def test_long_16k_in_two_segments_sampled():
     check(shape, synth.WORKLOAD_SEEDS["long_16k"], (8192,), pairs=[0, 7, 33, 40, 79])
 
 
+def test_long_16k_in_three_uneven_segments_sampled():
+    """Segments of 5000, 6000 and 5384 tokens: the tensor-core correction runs
+    several heads per CTA (its two-deep head pipeline) over ragged last
+    tiles."""
+    shape = synth.WORKLOADS["long_16k"]
+    check(shape, synth.WORKLOAD_SEEDS["long_16k"], (5000, 11000), pairs=[1, 6, 38, 64, 79])
+
+
 def test_rank0_leaves_y_and_copies_its_final_state():
     shape = F(1, 300, 2, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 96)
