@@ -122,6 +122,18 @@ def test_long_16k_in_three_uneven_segments_sampled():
     check(shape, synth.WORKLOAD_SEEDS["long_16k"], (5000, 11000), pairs=[1, 6, 38, 64, 79])
 
 
+@pytest.mark.parametrize("shape,seed,cuts,pairs", [
+    # the 2.7B layer's heads, four batch rows: the correction's units run two
+    # heads each and span batch rows, over ragged last tiles
+    (F(4, 4096, 80, 64, 128, 1, 1, 256, synth.BF16, "half"), 97, (1500, 2900),
+     [3, 81, 170, 259, 319]),
+    # 128-wide heads (P = 128) over a long sequence: two heads per unit
+    (F(1, 8192, 64, 128, 128, 1, 1, 128, synth.BF16, "all"), 98, (3000,), [0, 17, 40, 63]),
+])
+def test_large_segments_sampled(shape, seed, cuts, pairs):
+    check(shape, seed, cuts, pairs=pairs)
+
+
 def test_rank0_leaves_y_and_copies_its_final_state():
     shape = F(1, 300, 2, 64, 128, 1, 1, 256, synth.BF16, "all")
     inp = synth.make_fwd_inputs(shape, 96)
