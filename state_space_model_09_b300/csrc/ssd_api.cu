@@ -631,8 +631,13 @@ ssd_status launch_fused_t(const Plan &pl, const void *x, const float *dt, const 
   // the flagged (chunk, head) units, head by head (blocks that find none exit)
   using LH = ssd::ScanHL<Q, P>;
   if (!ensure_smem<ssd::chunk_scan_flagged<Q, P>>(LH::kBytes)) return SSD_ERR_CUDA;
+  // head sets per (batch row, chunk): as many as still fit the launch in one
+  // round of the SMs (its blocks take an SM each and nearly all of them only
+  // read their flags), at least enough for kMaxFlaggedHeads heads a set
   const int64_t kmax = LH::kMaxFlaggedHeads;
-  const int sets = static_cast<int>(std::max<int64_t>(kFlaggedSets, (pl.H + kmax - 1) / kmax));
+  const int64_t fit = std::max<int64_t>(1, num_sms() / (static_cast<int64_t>(pl.nc) * pl.b));
+  const int sets = static_cast<int>(
+      std::max<int64_t>((pl.H + kmax - 1) / kmax, std::min<int64_t>(kFlaggedSets, fit)));
   const int64_t blocks = static_cast<int64_t>(sets) * pl.nc * pl.b;
   if (blocks > (int64_t(1) << 31) - 1) return SSD_ERR_UNSUPPORTED;
   st = launch_dependent(pdl_on(events), ssd::chunk_scan_flagged<Q, P>,
