@@ -716,15 +716,22 @@ def run_ours(args, shape, world, rank, local):
 
 
 # ----------------------------------------------------------------------------- multistep arm
-def multistep_work(s: synth.MultistepShape, verify: bool = False):
+def multistep_work(s: synth.MultistepShape, verify: bool = False, draft: bool = False):
     """Bytes of one multi-step call: h_cache in, h_j and h_K out (f32), x and y
     (io), B, C (io), dt (f32), j (int32).  A fused verify call moves two states
-    (cache in, next cache out) and also reads the previous drafts' x, B, dt."""
+    (cache in, next cache out) and also reads the previous drafts' x, B, dt.  A
+    draft-model step is a fused verify call with one new token (K = 1) after
+    the K previous drafts."""
     io = 2 if s.io == synth.BF16 else 4
     st = s.batch * s.nheads * s.dstate * s.headdim * 4
     x = s.batch * s.K * s.nheads * s.headdim * io
     bc = s.batch * s.K * (s.ngroups_b + s.ngroups_c) * s.dstate * io
     dt = s.batch * s.K * s.nheads * 4
+    if draft:
+        x1, bc1, dt1 = x // s.K, bc // s.K, dt // s.K
+        bp = s.batch * s.K * s.ngroups_b * s.dstate * io
+        return dict(bytes=2 * st + x + bp + dt + 2 * x1 + bc1 + dt1 + s.batch * 4,
+                    tok_heads=s.batch * s.nheads)
     if verify:
         bp = s.batch * s.K * s.ngroups_b * s.dstate * io
         return dict(bytes=2 * st + 3 * x + bc + bp + 2 * dt + s.batch * 4,
@@ -901,9 +908,12 @@ def run_cp(args, shape, world, rank, local):
         "clocks": clk}), flush=True)
 
 
-def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0, e2e=True):
+def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0, e2e=True,
+                      draft=False):
     """The speculative chain: each call continues from the previous call's h_j
-    (ssd_multistep) or from the next cache it stored (ssd_verify).  The
+    (ssd_multistep) or from the next cache it stored (ssd_verify; with draft,
+    the draft model's step: the previous call's K drafts, j of them accepted,
+    folded into the cache and one new token decoded).  The
     1000-call chain is captured in a CUDA graph and replayed until >= min_s;
     ms per call = median replay time / calls.  With chains > 1, that many
     independent chains (own states, the same drafts) run interleaved, call i of
@@ -914,7 +924,8 @@ def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0,
     from state_space_model_09_b300 import ssd as S
 
     shape = synth.WORKLOADS["multistep_k8"]
-    work = multistep_work(shape, verify)
+    verify = verify or draft
+    work = multistep_work(shape, verify, draft)
     inp = synth.make_multistep_inputs(shape, synth.WORKLOAD_SEEDS["multistep_k8"] + 17 * rank)
     bf = torch.bfloat16
     X = torch.from_numpy(inp["x"]).to(bf).to(dev)
@@ -931,6 +942,10 @@ def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0,
     steps = shape.steps
     stream = torch.cuda.Stream(dev)
     J0 = torch.zeros_like(J[0])
+    if draft:  # the new token of each call: the first of its drafts, contiguous
+        X1, DT1, BB1, CC1 = (t[:, :, :1].contiguous() for t in (X, DT, BB, CC))
+        for c in st:
+            c["Y"] = torch.empty_like(X1[0])
 
     def chain():
         cur = [h0] * chains
@@ -941,8 +956,13 @@ def measure_multistep(args, world, rank, dev, verify=False, chains=1, min_s=1.0,
                     # fused recompute + verify + cache: the cache is the state
                     # before the previous drafts, of which J[i-1] were accepted
                     p = i - 1 if i > 0 else 0
-                    S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X[i], DT[i], A,
-                                 BB[i], CC[i], D, cur[c], st[c]["Y"], nxt, stream=stream)
+                    if draft:
+                        S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X1[i],
+                                     DT1[i], A, BB1[i], CC1[i], D, cur[c], st[c]["Y"], nxt,
+                                     stream=stream)
+                    else:
+                        S.ssd_verify(X[p], DT[p], BB[p], J[i - 1] if i > 0 else J0, X[i], DT[i],
+                                     A, BB[i], CC[i], D, cur[c], st[c]["Y"], nxt, stream=stream)
                 else:
                     S.ssd_multistep(X[i], DT[i], A, BB[i], CC[i], D, cur[c], J[i], st[c]["Y"],
                                     nxt, st[c]["hK"], stream=stream, dims=dims)
@@ -1117,6 +1137,11 @@ def multistep_summary(args, world, rank, local):
                                           measured_traffic("multistep_kernel_verify", "multistep_k8")),
                          call="ssd_verify")
     out["verify"]["roofline"]["kernel"] = "multistep_kernel (verify mode)"
+    torch.cuda.empty_cache()
+    md = measure_multistep(args, world, rank, dev, draft=True, min_s=args.min_seconds, e2e=False)
+    out["draft"] = dict(multistep_fields(md, world, pk, None),
+                        call="ssd_verify, K = 1 after 8 previous drafts (draft-model step)")
+    out["draft"]["roofline"]["kernel"] = "multistep_kernel (verify mode, K = 1)"
     if not args.no_cpu_baseline:
         value, _, cores, sample = oracle_multistep_chain(12, 6.0)
         out["cpu_baseline"] = {"value": round(value, 4), "unit": UNIT, "cores": cores,
@@ -1131,13 +1156,15 @@ def run_multistep(args, world, rank, local):
     torch.cuda.set_device(dev)
     shape = synth.WORKLOADS["multistep_k8"]
     m = measure_multistep(args, world, rank, dev, verify=args.verify, chains=args.chains,
-                          min_s=args.min_seconds)
+                          min_s=args.min_seconds, draft=args.draft, e2e=not args.draft)
     if rank != 0:
         return
     pk = peaks()
-    f = multistep_fields(m, world, pk, None if args.chains > 1 else measured_traffic(
+    f = multistep_fields(m, world, pk, None if args.chains > 1 or args.draft else measured_traffic(
         "multistep_kernel_verify" if args.verify else "multistep_kernel", "multistep_k8"))
-    metric = ("SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
+    metric = ("SSD draft-model step Mtok·heads/s (8 previous drafts folded + 1 new token, "
+              "1000-step chain)" if args.draft else
+              "SSD fused verify decode Mtok·heads/s (recompute + K=8 verify + cache, "
               "1000-step speculative chain)" if args.verify else MULTISTEP_METRIC)
     line = {"metric": metric, "value": f.pop("value"), "unit": UNIT, "n_gpus": world,
             "steps": shape.steps * args.chains, "warmup": args.warmup,
@@ -1145,10 +1172,11 @@ def run_multistep(args, world, rank, local):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded PCG64)",
             "config": config_of("multistep_k8", shape, world),
             "timing": "CUDA graph of the chain (%d interleaved), replayed until >= 1 s; %s"
-                      % (args.chains, "ssd_verify" if args.verify else "ssd_multistep"),
+                      % (args.chains, "ssd_verify (K = 1)" if args.draft else
+                         "ssd_verify" if args.verify else "ssd_multistep"),
             "gpu_launches": m["launches"]}
     line.update(f)
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.draft:
         value, _, cores, sample = oracle_multistep_chain(40, 20.0)
         line["cpu_baseline"] = {"value": round(value, 4), "unit": UNIT, "cores": cores,
                                 "kind": "oracle", "sample": sample}
@@ -1169,6 +1197,8 @@ def main():
                     help="replay the timed block until this much device time is measured")
     ap.add_argument("--verify", action="store_true",
                     help="multistep_k8: time the chain of fused recompute + verify calls")
+    ap.add_argument("--draft", action="store_true",
+                    help="multistep_k8: time the draft-model step (fused verify call, K = 1)")
     ap.add_argument("--chains", type=int, default=1,
                     help="multistep_k8: independent chains interleaved (3+ keeps states cold)")
     ap.add_argument("--window", type=int, default=0,
