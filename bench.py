@@ -58,17 +58,20 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_fused_hb", "mamba2_2p7b"):
-        (346_760_960, FUSED_SRCS,
-         "1f87a04b5f475f5e15b6311efe1af2bcbe4e899e"),
+        (347_219_200, FUSED_SRCS,
+         "bc936592d46e8d97cce5a6a6f3781bd098f950f2"),
     ("chunk_fused_hb", "hybrid_llama3_8b"):
-        (406_927_232, FUSED_SRCS,
-         "1f87a04b5f475f5e15b6311efe1af2bcbe4e899e"),
+        (406_737_408, FUSED_SRCS,
+         "bc936592d46e8d97cce5a6a6f3781bd098f950f2"),
     ("multistep_kernel", "multistep_k8"):
-        (68_567_808, MS_SRCS,
-         "2247f085a6f25de83d9e138dde25a79199608cd8"),
+        (68_773_888, MS_SRCS,
+         "f33363be53b6bef03095edd84f7f3da335fe3838"),
     ("multistep_kernel_verify", "multistep_k8"):
-        (46_689_792, MS_SRCS,
-         "2247f085a6f25de83d9e138dde25a79199608cd8"),
+        (46_773_888, MS_SRCS,
+         "f33363be53b6bef03095edd84f7f3da335fe3838"),
+    ("multistep_kernel_draft", "multistep_k8"):
+        (44_980_992, MS_SRCS,
+         "f33363be53b6bef03095edd84f7f3da335fe3838"),
 }
 
 
@@ -1139,7 +1142,8 @@ def multistep_summary(args, world, rank, local):
     out["verify"]["roofline"]["kernel"] = "multistep_kernel (verify mode)"
     torch.cuda.empty_cache()
     md = measure_multistep(args, world, rank, dev, draft=True, min_s=args.min_seconds, e2e=False)
-    out["draft"] = dict(multistep_fields(md, world, pk, None),
+    out["draft"] = dict(multistep_fields(md, world, pk,
+                                         measured_traffic("multistep_kernel_draft", "multistep_k8")),
                         call="ssd_verify, K = 1 after 8 previous drafts (draft-model step)")
     out["draft"]["roofline"]["kernel"] = "multistep_kernel (verify mode, K = 1)"
     if not args.no_cpu_baseline:
@@ -1160,7 +1164,8 @@ def run_multistep(args, world, rank, local):
     if rank != 0:
         return
     pk = peaks()
-    f = multistep_fields(m, world, pk, None if args.chains > 1 or args.draft else measured_traffic(
+    f = multistep_fields(m, world, pk, None if args.chains > 1 else measured_traffic(
+        "multistep_kernel_draft" if args.draft else
         "multistep_kernel_verify" if args.verify else "multistep_kernel", "multistep_k8"))
     metric = ("SSD draft-model step Mtok·heads/s (8 previous drafts folded + 1 new token, "
               "1000-step chain)" if args.draft else
