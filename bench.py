@@ -70,7 +70,7 @@ MEASURED_TRAFFIC = {
         (46_773_888, MS_SRCS,
          "f33363be53b6bef03095edd84f7f3da335fe3838"),
     ("multistep_kernel_draft", "multistep_k8"):
-        (44_980_992, MS_SRCS,
+        (45_157_248, MS_SRCS,
          "f33363be53b6bef03095edd84f7f3da335fe3838"),
 }
 

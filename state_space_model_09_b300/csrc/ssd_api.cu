@@ -469,8 +469,9 @@ ssd_status launch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, const
 }
 
 // The instance for a shape: the decode shape of the Mamba-2 layers (bf16,
-// N = 128, K = 8, k_prev <= 8) with N and K fixed at compile time, else a
-// generic one.
+// N = 128, K = 8, k_prev <= 8) with N and K fixed at compile time; a verify
+// call of fewer new tokens at N = 128 (the draft model's step, K = 1) with N
+// fixed; else a generic one.
 template <bool VF>
 ssd_status dispatch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, const float *dtp,
                        const void *Bp, const int32_t *j, const void *x, const float *dt,
@@ -482,6 +483,8 @@ ssd_status dispatch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, con
 #define SSD_MS_ARGS grid, d, KP, xp, dtp, Bp, j, x, dt, A, B, C, D, h_cache, y, h_j, h_K, h_next, PS, s
   if (bf16 && small && d->seqlen == 8 && d->dstate == 128)
     return launch_ms<__nv_bfloat16, 8, 128, true, VF>(SSD_MS_ARGS);
+  if (VF && bf16 && small && d->dstate == 128)  // the draft model's short steps
+    return launch_ms<__nv_bfloat16, 8, 128, false, VF>(SSD_MS_ARGS);
   if (bf16)
     return small ? launch_ms<__nv_bfloat16, 8, 0, false, VF>(SSD_MS_ARGS)
                  : launch_ms<__nv_bfloat16, 16, 0, false, VF>(SSD_MS_ARGS);

@@ -28,6 +28,7 @@ def _steps(inp, io, s):
     (M(3, 8, 4, 64, 128, 1, 1, synth.BF16, 2), 71),   # the decode shape's specialised instance
     (M(2, 5, 4, 32, 64, 2, 4, synth.F32, 2), 72),     # groups, float32, K = 5
     (M(2, 12, 2, 128, 256, 1, 1, synth.BF16, 2), 77),  # 16-token instance, 128-column slices
+    (M(2, 3, 4, 64, 64, 1, 2, synth.BF16, 2), 78),    # bf16, N = 64: the generic instance
 ])
 def test_verify_matches_oracle(shape, seed):
     inp = synth.make_multistep_inputs(shape, seed, steps=2)
