@@ -619,7 +619,7 @@ ssd_status launch_fused_t(const Plan &pl, const void *x, const float *dt, const 
                           dim3(static_cast<unsigned>(ctas)), dim3(ssd::kFuThreads), L::kBytes, s,
                           mX, mB, mC, mY, dt, A, D, h0, h_final, Hin, flags, u, pl.T, H, GB, GC,
                           pl.nc, pl.softplus ? 1 : 0, static_cast<int>(pl.whole), pl.nseg, pl.cps,
-                          pl.seg_bh0, Fseg, Lseg);
+                          pl.seg_bh0, Fseg, Lseg, num_sms());
     if (st != SSD_OK) return st;
     record(events, ++ev, s);
     pdl = pdl_on(events);
@@ -628,7 +628,8 @@ ssd_status launch_fused_t(const Plan &pl, const void *x, const float *dt, const 
   st = launch_dependent(pdl, ssd::chunk_fused_hb<true, HP, SPC>, dim3(static_cast<unsigned>(ctas)),
                         dim3(ssd::kFuThreads), L::kBytes, s, mX, mB, mC, mY, dt, A, D, h0, h_final,
                         Hin, flags, u, pl.T, H, GB, GC, pl.nc, pl.softplus ? 1 : 0,
-                        static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg);
+                        static_cast<int>(pl.whole), pl.nseg, pl.cps, pl.seg_bh0, Fseg, Lseg,
+                        num_sms());
   if (st != SSD_OK) return st;
   record(events, ++ev, s);
   // the flagged (chunk, head) units, head by head (blocks that find none exit)

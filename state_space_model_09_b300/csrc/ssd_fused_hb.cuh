@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kFuThreads, 1)
                    float *__restrict__ h_final, __nv_bfloat16 *__restrict__ Hin,
                    uint8_t *__restrict__ flags, float *__restrict__ u, int64_t T, int H, int GB,
                    int GC, int nc, int softplus, int whole, int nseg, int cps, int64_t bh0,
-                   float *__restrict__ Fseg, float *__restrict__ Lseg) {
+                   float *__restrict__ Fseg, float *__restrict__ Lseg, int nsm) {
   using L = FusedHB;
   constexpr int S = L::S, N = L::N;
   constexpr int P = 128 / HP;  // the width of one head
@@ -384,9 +384,28 @@ __global__ void __launch_bounds__(kFuThreads, 1)
           tma_load_4d(Xs + xk * L::kTile + a * S * 128, &mapX, bar, atom_col(a), atom_head(a),
                       stage_t0(g), b);
       };
+      // The whole item most likely to start on an SM next (CTAs start in
+      // index order, one per SM, so about nsm after this one): its first two
+      // stages of x and its h0 into L2, a few stages before this item ends.
+      auto prefetch_next = [&]() {
+        const int nxt = cta + nsm;
+        if (!FULL || split || nxt >= whole) return;
+        const int bn = nxt / ipb, hn = HP * (nxt % ipb), nhn = min(HP, H - hn);
+        for (int gs = 0; gs < 2 && gs * S < T; ++gs)
+          for (int a = 0; a < (HP == 2 ? nhn : 2); ++a)
+            tma_prefetch_4d(&mapX, HP == 2 ? 0 : 64 * a, HP == 2 ? hn + a : hn, gs * S, bn);
+        if (h0) {
+          const float *src = h0 + (static_cast<int64_t>(bn) * H + hn) * N * P;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                           reinterpret_cast<uint64_t>(src)),
+                       "r"(static_cast<uint32_t>(nhn * N * P * 4))
+                       : "memory");
+        }
+      };
       for (int g = 0; g < min(L::kXSlots, nstages); ++g) load_x(g);
       for (int g = 0; g < nstages; ++g) {
         const int xk = g % L::kXSlots;
+        if (g == max(0, nstages - 4)) prefetch_next();
         const uint32_t par = (g / L::kXSlots) & 1;
         if (FULL) {
           if (!mbar_wait(&bars[kFuYstaged0 + xk], par, abort_flag) || *abort_flag) break;
