@@ -58,11 +58,11 @@ MEASURED_TRAFFIC = {
     # (kernel, workload): (DRAM bytes read + written per launch, the sources
     # the kernel is built from, sha1 of their concatenation when captured)
     ("chunk_fused_hb", "mamba2_2p7b"):
-        (347_219_200, FUSED_SRCS,
-         "bc936592d46e8d97cce5a6a6f3781bd098f950f2"),
+        (348_288_000, FUSED_SRCS,
+         "bb867851599ddb933a8594dae51214315db77d83"),
     ("chunk_fused_hb", "hybrid_llama3_8b"):
-        (406_737_408, FUSED_SRCS,
-         "bc936592d46e8d97cce5a6a6f3781bd098f950f2"),
+        (406_779_776, FUSED_SRCS,
+         "bb867851599ddb933a8594dae51214315db77d83"),
     ("multistep_kernel", "multistep_k8"):
         (68_773_888, MS_SRCS,
          "f33363be53b6bef03095edd84f7f3da335fe3838"),
