@@ -464,7 +464,8 @@ ssd_status launch_ms(dim3 grid, const ssd_dims *d, int KP, const void *xp, const
       D, h_cache, j, static_cast<IO *>(y), h_j, h_K, static_cast<int>(d->seqlen),
       static_cast<int>(d->nheads), static_cast<int>(d->ngroups_b), static_cast<int>(d->ngroups_c),
       static_cast<int>(d->dstate), static_cast<int>(d->headdim), PS, d->dt_softplus,
-      static_cast<const IO *>(xp), dtp, static_cast<const IO *>(Bp), h_next, KP);
+      static_cast<const IO *>(xp), dtp, static_cast<const IO *>(Bp), h_next, KP,
+      static_cast<int>(d->batch * d->nheads));
   return launch_status();
 }
 
@@ -1056,7 +1057,11 @@ ssd_status ssd_multistep(const ssd_dims *dims, const void *x, const float *dt, c
   // raw rows of B move in 16-byte granules
   if (N % R || (N * (dims->io_dtype == SSD_BF16 ? 2 : 4)) % 16) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(b), static_cast<unsigned>(P / PS));
+  // (b, h) items dealt out SM by SM (see multistep_kernel)
+  const int64_t nsm_ = num_sms();
+  if ((H * b + nsm_ - 1) / nsm_ > 65535) return SSD_ERR_UNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(nsm_), static_cast<unsigned>((H * b + nsm_ - 1) / nsm_),
+            static_cast<unsigned>(P / PS));
   return dispatch_ms<false>(grid, dims, 0, nullptr, nullptr, nullptr, j, x, dt, A, B, C, D, h_cache,
                             y, h_j, h_K, nullptr, PS, s);
 }

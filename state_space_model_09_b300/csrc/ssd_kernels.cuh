@@ -447,14 +447,29 @@ __global__ void __launch_bounds__(kMsThreads, KT <= 8 ? 12 : 8) multistep_kernel
     const float *__restrict__ h_cache, const int32_t *__restrict__ jacc, IO *__restrict__ y,
     float *__restrict__ h_j, float *__restrict__ h_K, int K_arg, int H, int GB, int GC, int N_arg,
     int P, int PS, int softplus, const IO *__restrict__ xp, const float *__restrict__ dtp,
-    const IO *__restrict__ Bp, float *__restrict__ h_next, int KP) {
+    const IO *__restrict__ Bp, float *__restrict__ h_next, int KP, int nitems) {
   static_assert(!KX || KT == 8, "the specialised row loop covers accepted counts 0..8");
   constexpr int KW = VF ? KPT : KT;
   constexpr int DEPTH = ms_depth(VF);
   const int N = NC ? NC : N_arg;
   const int K = KX ? KT : K_arg;
   extern __shared__ float4 sm_ms4[];
-  const int h = blockIdx.x, b = blockIdx.y, p0 = blockIdx.z * PS;
+  // Multistep: grid (SMs, rounds, P / PS).  CTAs are handed to the SMs in
+  // index order, so an SM's CTAs are consecutive (b, h) items and mostly run
+  // the same accepted-count specialisation of the row loop (fewer
+  // instruction-cache misses).  Verify: grid (H, b, P / PS) -- the grouping
+  // measured slower there.
+  int h, b;
+  if constexpr (VF) {
+    h = blockIdx.x;
+    b = blockIdx.y;
+  } else {
+    const int item = blockIdx.x * gridDim.y + blockIdx.y;
+    if (item >= nitems) return;
+    h = item % H;
+    b = item / H;
+  }
+  const int p0 = blockIdx.z * PS;
   const int lane = threadIdx.x;
   const int NS = N + 16 / static_cast<int>(sizeof(IO));  // padded raw row
   float *sCe = reinterpret_cast<float *>(sm_ms4);  // e_k C_k [N][KT]
