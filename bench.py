@@ -64,14 +64,14 @@ MEASURED_TRAFFIC = {
         (406_779_776, FUSED_SRCS,
          "bb867851599ddb933a8594dae51214315db77d83"),
     ("multistep_kernel", "multistep_k8"):
-        (68_773_888, MS_SRCS,
-         "f33363be53b6bef03095edd84f7f3da335fe3838"),
+        (68_785_152, MS_SRCS,
+         "4503a261542508fe7c15bcd2eba12bf6d229c1cc"),
     ("multistep_kernel_verify", "multistep_k8"):
-        (46_773_888, MS_SRCS,
-         "f33363be53b6bef03095edd84f7f3da335fe3838"),
+        (46_621_952, MS_SRCS,
+         "4503a261542508fe7c15bcd2eba12bf6d229c1cc"),
     ("multistep_kernel_draft", "multistep_k8"):
-        (45_157_248, MS_SRCS,
-         "f33363be53b6bef03095edd84f7f3da335fe3838"),
+        (44_964_480, MS_SRCS,
+         "4503a261542508fe7c15bcd2eba12bf6d229c1cc"),
 }
 
 
