@@ -99,6 +99,9 @@ def check(shape, seed, cuts, pairs=None, dt_softplus=True):
     (F(1, 300, 3, 32, 32, 1, 1, 64, synth.F32, "all"), 93, (64, 65, 200)),
     # bf16 outside the tensor-core envelope (N = 64)
     (F(2, 200, 4, 64, 64, 1, 2, 64, synth.BF16, "zero"), 94, (100,)),
+    # tensor-core correction on segments of exactly one tile, one token, one
+    # token short of a tile, and one tile and a bit
+    (F(1, 400, 4, 64, 128, 1, 1, 256, synth.BF16, "all"), 99, (128, 129, 256)),
 ])
 def test_segments_equal_whole_sequence(shape, seed, cuts):
     check(shape, seed, cuts)
